@@ -1,0 +1,194 @@
+"""CPU oracle for the three fused memory-bound chains (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  The oracle is plain C (``oracle.c``) evaluating the
+pages' formulas one operation at a time; this module only marshals numpy
+arrays into it.  Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it; the product package never does.
+
+Every function takes and returns host numpy arrays: fp32 as ``float32``,
+bf16 as raw ``uint16`` bit patterns.
+
+Sources: see ``oracle.h`` for the four pages ([P1]..[P4]) and the section each
+function follows.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _f32p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _u16p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def _f64p(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f32p_opt(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_float)()
+    return _f32p(a)
+
+
+def load(path=None):
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if path is None and _lib is not None:
+        return _lib
+    so = path or _build.DEFAULT_SO
+    if path is None and not os.path.exists(so):
+        _build.build()
+    lib = ctypes.CDLL(so)
+    F32P = ctypes.POINTER(ctypes.c_float)
+    U16P = ctypes.POINTER(ctypes.c_uint16)
+    F64P = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    f32 = ctypes.c_float
+    lib.oracle_relu_f32.argtypes = [f32]
+    lib.oracle_relu_f32.restype = f32
+    lib.oracle_gelu_tanh.argtypes = [ctypes.c_double]
+    lib.oracle_gelu_tanh.restype = ctypes.c_double
+    lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+    lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = ctypes.c_double
+    lib.oracle_add_relu_scale_f32.argtypes = [F32P, F32P, F32P, F32P, i64, f32]
+    lib.oracle_add_relu_scale_f32.restype = None
+    lib.oracle_add_relu_scale_bf16.argtypes = [U16P, U16P, U16P, U16P, i64, f32]
+    lib.oracle_add_relu_scale_bf16.restype = None
+    lib.oracle_bias_relu_branch_mean_epilogue.argtypes = [
+        F32P, F32P, F32P, F32P, F32P, i64, i64, f32, f32, F32P, F32P]
+    lib.oracle_bias_relu_branch_mean_epilogue.restype = None
+    lib.oracle_residual_layernorm_gelu_f32.argtypes = [
+        F32P, F32P, F32P, F32P, F32P, i64, i64, f32, F64P, F64P, F64P]
+    lib.oracle_residual_layernorm_gelu_f32.restype = None
+    lib.oracle_residual_layernorm_gelu_bf16.argtypes = [
+        U16P, U16P, U16P, U16P, U16P, i64, i64, f32, F64P, F64P, F64P]
+    lib.oracle_residual_layernorm_gelu_bf16.restype = None
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+# --------------------------------------------------------------------------
+# scalar helpers
+# --------------------------------------------------------------------------
+
+def relu_f32(v, lib=None):
+    return (lib or load()).oracle_relu_f32(float(v))
+
+
+def gelu_tanh(z, lib=None):
+    return (lib or load()).oracle_gelu_tanh(float(z))
+
+
+def bf16_from_double(v, lib=None):
+    return (lib or load()).oracle_bf16_from_double(float(v))
+
+
+def bf16_to_double(h, lib=None):
+    return (lib or load()).oracle_bf16_to_double(int(h))
+
+
+# --------------------------------------------------------------------------
+# o1: y = relu(x + b1) * scale + b2   ([P1] §1.1, §3.1)
+# --------------------------------------------------------------------------
+
+def add_relu_scale(x, b1, b2, scale=0.5, lib=None):
+    """fp32 (float32 arrays) or bf16 (uint16 bit patterns) pointwise chain."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    if not (x.shape == np.shape(b1) == np.shape(b2)):
+        raise ValueError("x, b1, b2 must have one shape")
+    dt = x.dtype
+    if dt == np.float32:
+        x, b1, b2 = (_c(a, np.float32) for a in (x, b1, b2))
+        y = np.empty_like(x)
+        lib.oracle_add_relu_scale_f32(_f32p(x), _f32p(b1), _f32p(b2), _f32p(y),
+                                      x.size, scale)
+    elif dt == np.uint16:
+        x, b1, b2 = (_c(a, np.uint16) for a in (x, b1, b2))
+        y = np.empty_like(x)
+        lib.oracle_add_relu_scale_bf16(_u16p(x), _u16p(b1), _u16p(b2), _u16p(y),
+                                       x.size, scale)
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    return y
+
+
+# --------------------------------------------------------------------------
+# o2: TorchInductor example chain   ([P4] "model", Figure 1)
+# --------------------------------------------------------------------------
+
+def bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
+                                   branch_scale=0.1, intermediates=False,
+                                   lib=None):
+    """y = (s - mean(s, 1)) * gamma + beta with s = relu(x*x_scale + bias)^2
+    + relu(...)*branch_scale.  With ``intermediates`` also returns (s, m)."""
+    lib = lib or load()
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    bias, gamma, beta = (_c(a, np.float32) for a in (bias, gamma, beta))
+    for v in (bias, gamma, beta):
+        if v.shape != (cols,):
+            raise ValueError("per-column vectors must have length cols")
+    y = np.empty_like(x)
+    s = np.empty_like(x) if intermediates else None
+    m = np.empty(rows, np.float32) if intermediates else None
+    lib.oracle_bias_relu_branch_mean_epilogue(
+        _f32p(x), _f32p(bias), _f32p(gamma), _f32p(beta), _f32p(y), rows, cols,
+        x_scale, branch_scale, _f32p_opt(s), _f32p_opt(m))
+    if intermediates:
+        return y, s, m
+    return y
+
+
+# --------------------------------------------------------------------------
+# o3: residual + LayerNorm + affine + GeLU-tanh   ([P2] §2.3, [P3] §4.3)
+# --------------------------------------------------------------------------
+
+def residual_layernorm_gelu(x, r, w, b, eps=1e-5, intermediates=False, lib=None):
+    """out = gelu_tanh(LayerNorm(x + r) * w + b).  float32 or uint16 (bf16)
+    inputs; the output has the input dtype.  With ``intermediates`` also
+    returns (mean, rstd, xhat) in float64."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    rows, hidden = x.shape
+    dt = x.dtype
+    out = np.empty_like(x)
+    mean = np.empty(rows, np.float64) if intermediates else None
+    rstd = np.empty(rows, np.float64) if intermediates else None
+    xhat = np.empty((rows, hidden), np.float64) if intermediates else None
+    if dt == np.float32:
+        r, w, b = (_c(a, np.float32) for a in (r, w, b))
+        fn, p = lib.oracle_residual_layernorm_gelu_f32, _f32p
+    elif dt == np.uint16:
+        r, w, b = (_c(a, np.uint16) for a in (r, w, b))
+        fn, p = lib.oracle_residual_layernorm_gelu_bf16, _u16p
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    if r.shape != x.shape or w.shape != (hidden,) or b.shape != (hidden,):
+        raise ValueError("shape mismatch")
+    fn(p(x), p(r), p(w), p(b), p(out), rows, hidden, eps, _f64p(mean),
+       _f64p(rstd), _f64p(xhat))
+    if intermediates:
+        return out, mean, rstd, xhat
+    return out

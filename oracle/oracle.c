@@ -1,0 +1,253 @@
+/*
+ * oracle.c -- CPU definitions of the three fused memory-bound chains.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h).  Plain loops in the order the
+ * pages write the formulas; no blocking, no fusion, no reordering.  Build with
+ * -O2 -ffp-contract=off and without -ffast-math, so each fp32 operation below
+ * is rounded on its own exactly as an eager fp32 tensor op would round it.
+ *
+ * Precision readings (where the pages do not fix a step, the plainest reading
+ * that the rest of the page supports):
+ *   o1  The pages' chain runs on fp32 tensors, one rounded op at a time
+ *       ([P1] §3.1 baseline: add, relu, mul, add), so the oracle is that fp32
+ *       sequence.  The bf16 variant widens its inputs, runs the same fp32
+ *       sequence and rounds the result once to bf16.
+ *   o2  The [P4] example is fp32 ("x is f32[1024, 1024]"): every pointwise op
+ *       is an fp32 op.  The row mean is a sum then a division by the row
+ *       length ([P4] §6.4: the reduction is a 'sum', the /1024 happens in the
+ *       consumer); the order of that sum is unspecified, so the oracle sums in
+ *       double and rounds the mean once to fp32.
+ *   o3  v = x + r is the fp32 add of the [P2] §2.3 kernel; the statistics,
+ *       normalisation, affine step and GeLU are evaluated in double (the
+ *       pages' rsqrtf / tanhf and one-pass E[v^2]-mean^2 are shortcuts of the
+ *       fp32 sketch, not the definition), and the output is rounded once.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+static const double ORACLE_PI = 3.14159265358979323846264338327950288;
+
+/* ------------------------------------------------------------------------ */
+/* scalar helpers                                                           */
+/* ------------------------------------------------------------------------ */
+
+float oracle_relu_f32(float v)
+{
+    /* [P1] §3.2 applies fmaxf(v, 0.0f).  v > 0 keeps v; every other value,
+     * including -0 and NaN, becomes +0. */
+    if (v > 0.0f)
+        return v;
+    return 0.0f;
+}
+
+double oracle_gelu_tanh(double z)
+{
+    /* [P2] §2.3: 0.5 * n * (1 + tanh(0.7978845608 * (n + 0.044715 * n^3)));
+     * 0.7978845608 is sqrt(2/pi) to ten digits. */
+    const double k = sqrt(2.0 / ORACLE_PI);
+    double u = k * (z + 0.044715 * z * z * z);
+    return 0.5 * z * (1.0 + tanh(u));
+}
+
+double oracle_bf16_to_double(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+uint16_t oracle_bf16_from_double(double v)
+{
+    /* bf16: 1 sign bit, 8 exponent bits (bias 127), 7 stored fraction bits.
+     * The value is rounded once, to the nearest multiple of the bf16 quantum
+     * at its binade, ties to even (rint in the default rounding mode). */
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(v);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0)
+        return sign;
+
+    int e;
+    (void)frexp(a, &e);            /* a = f * 2^e, 0.5 <= f < 1           */
+    int q = e - 8;                 /* 8 significant bits: quantum 2^(e-8) */
+    if (q < -133)                  /* below 2^-126: fixed subnormal step   */
+        q = -133;
+    double k = rint(ldexp(a, -q)); /* exact scaling, one rounding          */
+    double r = ldexp(k, q);
+    if (r >= ldexp(1.0, 128))      /* rounded past the largest finite     */
+        return (uint16_t)(sign | 0x7F80u);
+
+    float rf = (float)r;           /* exact: r has <= 8 significant bits   */
+    uint32_t bits;
+    memcpy(&bits, &rf, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+static float widen_bf16(uint16_t h)
+{
+    return (float)oracle_bf16_to_double(h);
+}
+
+/* ------------------------------------------------------------------------ */
+/* o1: y = relu(x + b1) * scale + b2                                        */
+/* [P1] §1.1 (the four eager steps) and §3.1 (the baseline function)        */
+/* ------------------------------------------------------------------------ */
+
+static float o1_element(float x, float b1, float b2, float scale)
+{
+    float tmp = x + b1;             /* step 1: x + b1    -> tmp1 */
+    tmp = oracle_relu_f32(tmp);     /* step 2: relu      -> tmp2 */
+    tmp = tmp * scale;              /* step 3: * scale   -> tmp3 */
+    tmp = tmp + b2;                 /* step 4: + b2      -> y    */
+    return tmp;
+}
+
+void oracle_add_relu_scale_f32(const float *x, const float *b1, const float *b2,
+                               float *y, int64_t n, float scale)
+{
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = o1_element(x[i], b1[i], b2[i], scale);
+}
+
+void oracle_add_relu_scale_bf16(const uint16_t *x, const uint16_t *b1,
+                                const uint16_t *b2, uint16_t *y, int64_t n,
+                                float scale)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float r = o1_element(widen_bf16(x[i]), widen_bf16(b1[i]),
+                             widen_bf16(b2[i]), scale);
+        y[i] = oracle_bf16_from_double((double)r);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* o2: TorchInductor example chain, [P4] "model" and Figure 1               */
+/* ------------------------------------------------------------------------ */
+
+static float o2_s(float x, float bias, float x_scale, float branch_scale)
+{
+    float t = x * x_scale;          /* t = x * 1.1 + bias (broadcast bias) */
+    t = t + bias;
+    float a = oracle_relu_f32(t);   /* a = relu(t)                          */
+    float p = a * a;                /* p = a * a                            */
+    float q = a * branch_scale;     /* q = a * 0.1                          */
+    float s = p + q;                /* s = p + q                            */
+    return s;
+}
+
+void oracle_bias_relu_branch_mean_epilogue(const float *x, const float *bias,
+                                           const float *gamma, const float *beta,
+                                           float *y, int64_t rows, int64_t cols,
+                                           float x_scale, float branch_scale,
+                                           float *s_out, float *m_out)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *xr = x + i * cols;
+
+        /* m = s.mean(dim=1, keepdim=True): row sum, then / cols */
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            sum += (double)o2_s(xr[j], bias[j], x_scale, branch_scale);
+        float m = (float)(sum / (double)cols);
+        if (m_out)
+            m_out[i] = m;
+
+        /* y = (s - m) * gamma + beta */
+        for (int64_t j = 0; j < cols; ++j) {
+            float s = o2_s(xr[j], bias[j], x_scale, branch_scale);
+            if (s_out)
+                s_out[i * cols + j] = s;
+            float d = s - m;
+            d = d * gamma[j];
+            y[i * cols + j] = d + beta[j];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* o3: residual + LayerNorm + affine + GeLU-tanh                            */
+/* [P2] §2.2-2.3 (fused kernel: v = x + residual, mean, var, rsqrt(var+eps),*/
+/* norm = (v-mean)*inv_std*weight + bias, GeLU) and [P3] §4.3 (two-pass     */
+/* variance sum((x-mean)^2)/cols, rsqrt(var + eps), * gamma + beta)         */
+/* ------------------------------------------------------------------------ */
+
+typedef float (*o3_load_fn)(const void *p, int64_t i);
+
+static float load_f32(const void *p, int64_t i) { return ((const float *)p)[i]; }
+static float load_bf16(const void *p, int64_t i)
+{
+    return widen_bf16(((const uint16_t *)p)[i]);
+}
+
+static void o3_rows(const void *x, const void *r, const void *w, const void *b,
+                    o3_load_fn load, void *out, int out_bf16, int64_t rows,
+                    int64_t hidden, float eps, double *mean_out,
+                    double *rstd_out, double *xhat_out)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        int64_t base = i * hidden;
+
+        /* mean = sum(v) / H, v = x + r in fp32 */
+        double sum = 0.0;
+        for (int64_t j = 0; j < hidden; ++j) {
+            float v = load(x, base + j) + load(r, base + j);
+            sum += (double)v;
+        }
+        double mean = sum / (double)hidden;
+
+        /* var = sum((v - mean)^2) / H  (biased, two passes) */
+        double sq = 0.0;
+        for (int64_t j = 0; j < hidden; ++j) {
+            float v = load(x, base + j) + load(r, base + j);
+            double d = (double)v - mean;
+            sq += d * d;
+        }
+        double var = sq / (double)hidden;
+        double rstd = 1.0 / sqrt(var + (double)eps);
+        if (mean_out)
+            mean_out[i] = mean;
+        if (rstd_out)
+            rstd_out[i] = rstd;
+
+        /* n = (v - mean) * rstd * w + b;  out = gelu_tanh(n) */
+        for (int64_t j = 0; j < hidden; ++j) {
+            float v = load(x, base + j) + load(r, base + j);
+            double xhat = ((double)v - mean) * rstd;
+            if (xhat_out)
+                xhat_out[base + j] = xhat;
+            double n = xhat * (double)load(w, j) + (double)load(b, j);
+            double g = oracle_gelu_tanh(n);
+            if (out_bf16)
+                ((uint16_t *)out)[base + j] = oracle_bf16_from_double(g);
+            else
+                ((float *)out)[base + j] = (float)g;
+        }
+    }
+}
+
+void oracle_residual_layernorm_gelu_f32(const float *x, const float *r,
+                                        const float *w, const float *b,
+                                        float *out, int64_t rows, int64_t hidden,
+                                        float eps, double *mean_out,
+                                        double *rstd_out, double *xhat_out)
+{
+    o3_rows(x, r, w, b, load_f32, out, 0, rows, hidden, eps, mean_out,
+            rstd_out, xhat_out);
+}
+
+void oracle_residual_layernorm_gelu_bf16(const uint16_t *x, const uint16_t *r,
+                                         const uint16_t *w, const uint16_t *b,
+                                         uint16_t *out, int64_t rows,
+                                         int64_t hidden, float eps,
+                                         double *mean_out, double *rstd_out,
+                                         double *xhat_out)
+{
+    o3_rows(x, r, w, b, load_bf16, out, 1, rows, hidden, eps, mean_out,
+            rstd_out, xhat_out);
+}

@@ -1,0 +1,86 @@
+/*
+ * oracle.h -- plain, slow, obviously correct CPU definitions of the three
+ * fused memory-bound chains.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes
+ * or calls this code; only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark load it.  It shares no source with the CUDA
+ * path.
+ *
+ * Sources (the four web pages on vertically fused memory-bound chains):
+ *   [P1] "PyTorch operator fusion in practice", www.0539edu.com/news/5489619
+ *   [P2] "Operator fusion and kernel optimisation: from CUDA Graph to
+ *        FlashAttention", plumephp.com/ai-kernel-fusion-optimization
+ *   [P3] "Kernel fusion" course chapter 4, www.5688vip.com (AI training
+ *        operator performance, chapter 04)
+ *   [P4] "TorchInductor Pipeline and operator fusion", blog.kkkzoz.top
+ *        (posts/ml-systems/ml-compilers/torchinductor-fusion)
+ *
+ * Conventions: all arrays are contiguous row-major; bf16 values travel as
+ * their raw 16-bit patterns (uint16_t).  Compile with -ffp-contract=off so
+ * that every fp32 operation written below is rounded separately.
+ */
+#ifndef MB_ORACLE_H
+#define MB_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- scalar helpers (exported so the tests can pin them directly) ---- */
+
+/* relu as the [P1] §3.2 kernel writes it (fmaxf(v, 0)), with the two cases
+ * fmaxf leaves open fixed: NaN -> +0 and -0 -> +0. */
+float oracle_relu_f32(float v);
+
+/* GeLU, tanh form, [P2] §2.3: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))),
+ * evaluated in double. */
+double oracle_gelu_tanh(double z);
+
+/* Round a double to the nearest bf16, ties to even (one rounding). */
+uint16_t oracle_bf16_from_double(double v);
+/* Exact widening of a bf16 bit pattern. */
+double oracle_bf16_to_double(uint16_t h);
+
+/* ---- o1: pointwise chain y = relu(x + b1) * scale + b2 ([P1] §1.1, §3.1) ---- */
+
+void oracle_add_relu_scale_f32(const float *x, const float *b1, const float *b2,
+                               float *y, int64_t n, float scale);
+void oracle_add_relu_scale_bf16(const uint16_t *x, const uint16_t *b1,
+                                const uint16_t *b2, uint16_t *y, int64_t n,
+                                float scale);
+
+/* ---- o2: TorchInductor example chain ([P4] "model", Figure 1, §6.4) ----
+ *   t = x*x_scale + bias; a = relu(t); p = a*a; q = a*branch_scale;
+ *   s = p + q; m = mean(s, dim=1); y = (s - m)*gamma + beta
+ * s_out (rows*cols) and m_out (rows) are optional intermediates (NULL skips). */
+void oracle_bias_relu_branch_mean_epilogue(const float *x, const float *bias,
+                                           const float *gamma, const float *beta,
+                                           float *y, int64_t rows, int64_t cols,
+                                           float x_scale, float branch_scale,
+                                           float *s_out, float *m_out);
+
+/* ---- o3: residual + LayerNorm + affine + GeLU-tanh ([P2] §2.2-2.3, [P3] §4.3)
+ *   v = x + r; mean, biased var over the row; rstd = 1/sqrt(var + eps);
+ *   n = (v - mean)*rstd*w + b; out = gelu_tanh(n)
+ * mean_out, rstd_out (rows) and xhat_out (rows*hidden, the pre-affine
+ * (v - mean)*rstd) are optional intermediates (NULL skips). */
+void oracle_residual_layernorm_gelu_f32(const float *x, const float *r,
+                                        const float *w, const float *b,
+                                        float *out, int64_t rows, int64_t hidden,
+                                        float eps, double *mean_out,
+                                        double *rstd_out, double *xhat_out);
+void oracle_residual_layernorm_gelu_bf16(const uint16_t *x, const uint16_t *r,
+                                         const uint16_t *w, const uint16_t *b,
+                                         uint16_t *out, int64_t rows,
+                                         int64_t hidden, float eps,
+                                         double *mean_out, double *rstd_out,
+                                         double *xhat_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MB_ORACLE_H */

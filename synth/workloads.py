@@ -1,0 +1,120 @@
+"""The five synthetic workloads, by name, with their seeds and tensor ids.
+
+Shapes and distributions are the pages' example workloads:
+
+* pointwise chain ``relu(x + b1) * 0.5 + b2`` on full-size fp32 ``randn``
+  tensors of 4 * 1024 * 1024 elements ([P1] §3.1), and a 4096-element small
+  case;
+* the TorchInductor example on ``x`` f32[1024, 1024] with f32[1024] ``bias``,
+  ``gamma``, ``beta`` ([P4] "model");
+* residual + LayerNorm + GeLU-tanh rows ([P2] §2.3) at hidden 4096 fp32 and
+  hidden 8192 bf16.
+
+N(mu, s) takes ``s`` as the standard deviation.  Tensor ids are assigned in
+the order each workload lists its tensors.
+"""
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import normal, uniform
+
+
+@dataclass(frozen=True)
+class Tensor:
+    name: str
+    tid: int
+    dist: str          # "normal" or "uniform"
+    a: float           # mean (normal) or low (uniform)
+    b: float           # std (normal) or high (uniform)
+    per_column: bool   # a length-cols vector broadcast over rows
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    chain: str         # "add_relu_scale" | "inductor" | "ln_gelu"
+    dtype: str         # "f32" | "bf16"
+    rows: int          # 1 for the pointwise chain
+    cols: int          # n for the pointwise chain
+    seed: int
+    tensors: tuple
+    params: dict = field(default_factory=dict)
+
+    @property
+    def elem_bytes(self):
+        return 2 if self.dtype == "bf16" else 4
+
+    def shape(self, t):
+        if t.per_column:
+            return (self.cols,)
+        if self.chain == "add_relu_scale":
+            return (self.cols,)
+        return (self.rows, self.cols)
+
+    def ideal_bytes(self, rows=None):
+        """Read-once / write-once bytes of one call (optionally for a prefix
+        of ``rows`` rows)."""
+        rows = self.rows if rows is None else rows
+        eb = self.elem_bytes
+        full = sum(1 for t in self.tensors if not t.per_column)
+        percol = sum(1 for t in self.tensors if t.per_column)
+        return rows * self.cols * eb * (full + 1) + percol * self.cols * eb
+
+    def generate(self, tensor, rows=None):
+        """Host array for one tensor (uint16 bit patterns for bf16).
+        ``rows`` limits row-shaped tensors to their first rows."""
+        shape = self.shape(tensor)
+        if rows is not None and not tensor.per_column and len(shape) == 2:
+            shape = (rows, shape[1])
+        fn = normal if tensor.dist == "normal" else uniform
+        return fn(self.seed, tensor.tid, shape, tensor.a, tensor.b, self.dtype)
+
+    def generate_all(self, rows=None):
+        return {t.name: self.generate(t, rows) for t in self.tensors}
+
+
+def _pointwise(name, n, seed):
+    return Workload(name, "add_relu_scale", "f32", 1, n, seed, (
+        Tensor("x", 0, "normal", 0.0, 1.0, False),
+        Tensor("b1", 1, "normal", 0.0, 1.0, False),
+        Tensor("b2", 2, "normal", 0.0, 1.0, False),
+    ), {"scale": 0.5})
+
+
+POINTWISE_TINY = _pointwise("pointwise_f32_4096", 4096, 0)
+POINTWISE_4M = _pointwise("pointwise_f32_4Mi", 4 * 1024 * 1024, 1)
+
+INDUCTOR_1024 = Workload("inductor_f32_1024x1024", "inductor", "f32", 1024, 1024, 2, (
+    Tensor("x", 0, "normal", 0.0, 1.0, False),
+    Tensor("bias", 1, "normal", 0.0, 0.1, True),
+    Tensor("gamma", 2, "uniform", 0.5, 1.5, True),
+    Tensor("beta", 3, "normal", 0.0, 0.1, True),
+), {"x_scale": 1.1, "branch_scale": 0.1})
+
+
+def _ln(name, dtype, rows, hidden, seed):
+    return Workload(name, "ln_gelu", dtype, rows, hidden, seed, (
+        Tensor("x", 0, "normal", 0.0, 1.0, False),
+        Tensor("r", 1, "normal", 0.0, 1.0, False),
+        Tensor("w", 2, "uniform", 0.5, 1.5, True),
+        Tensor("b", 3, "normal", 0.0, 0.1, True),
+    ), {"eps": 1e-5})
+
+
+LN_F32 = _ln("ln_gelu_f32_8192x4096", "f32", 8192, 4096, 3)
+LN_BF16 = _ln("ln_gelu_bf16_32768x8192", "bf16", 32768, 8192, 4)
+
+ALL = (POINTWISE_TINY, POINTWISE_4M, INDUCTOR_1024, LN_F32, LN_BF16)
+BY_NAME = {w.name: w for w in ALL}
+
+
+def sample_rows(rows, count, seed=12345):
+    """``count`` distinct row indices spread over ``rows``: the first, the
+    last, and a seeded random choice in between (sorted)."""
+    count = min(count, rows)
+    picks = {0, rows - 1}
+    rng = np.random.default_rng(seed)
+    while len(picks) < count:
+        picks.add(int(rng.integers(0, rows)))
+    return np.array(sorted(picks), dtype=np.int64)

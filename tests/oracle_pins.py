@@ -1,0 +1,331 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``pin_*`` takes a loaded oracle library (the real one, or a mutant built
+by ``test_oracle_mutants.py``) and raises ``AssertionError`` when the oracle
+disagrees with what the pages and the mathematics fix:
+
+* hand-computed fixtures from ``tests/golden/`` (exact dyadic arithmetic,
+  each citing the page whose formula it instantiates);
+* closed forms and invariants (row mean of s - m is 0, the LayerNorm output
+  before the affine step has mean 0 and variance var/(var+eps), GeLU's odd
+  part is z/2, ...);
+* special cases that reduce to library routines (torch CPU eager fp32 for
+  the fp32 op sequences, torch float64 ``layer_norm`` / ``gelu``, torch's
+  fp32 -> bf16 conversion).
+
+Pages: [P1] "PyTorch operator fusion in practice" (0539edu.com), [P2]
+"Operator fusion and kernel optimisation" (plumephp.com), [P3] course chapter
+4 "Kernel fusion" (5688vip.com), [P4] "TorchInductor Pipeline and operator
+fusion" (blog.kkkzoz.top).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+U32 = 2.0 ** -24   # unit roundoff of fp32
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bits(a):
+    return np.asarray(a, np.float32).view(np.uint32)
+
+
+# --------------------------------------------------------------------------
+# scalar helpers
+# --------------------------------------------------------------------------
+
+def pin_relu_cases(lib):
+    """[P1] §3.2 writes relu as fmaxf(v, 0); the two cases fmaxf leaves open
+    are fixed to +0 (see the readings)."""
+    for v, want in ((1.5, 1.5), (-1.0, 0.0), (0.0, 0.0), (2.0 ** -149, 2.0 ** -149),
+                    (-(2.0 ** -149), 0.0), (float("inf"), float("inf")),
+                    (float("-inf"), 0.0)):
+        got = oracle.relu_f32(v, lib=lib)
+        assert got == want, (v, got, want)
+    assert math.copysign(1.0, oracle.relu_f32(-0.0, lib=lib)) == 1.0
+    got = oracle.relu_f32(float("nan"), lib=lib)
+    assert got == 0.0 and math.copysign(1.0, got) == 1.0
+
+
+def pin_gelu_library(lib):
+    """GeLU tanh form ([P2] §2.3) against torch's float64
+    gelu(approximate='tanh') over [-12, 12]."""
+    z = np.linspace(-12.0, 12.0, 4801)
+    want = F.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    got = np.array([oracle.gelu_tanh(v, lib=lib) for v in z])
+    err = np.abs(got - want)
+    # 1 + tanh(u) cancels for z << 0: absolute error ~ |z|/2 * 2^-52 there
+    assert np.all(err <= 1e-14 * np.abs(want) + 1e-15 * np.abs(z)), err.max()
+
+
+def pin_gelu_invariants(lib):
+    """GeLU(0) = 0; GeLU(z) - GeLU(-z) = z (the tanh term is odd);
+    GeLU(z) -> z for large z and -> 0 for very negative z."""
+    assert oracle.gelu_tanh(0.0, lib=lib) == 0.0
+    for z in (1e-3, 0.25, 0.5, 1.0, 1.7, 3.0, 5.5, 9.0):
+        d = oracle.gelu_tanh(z, lib=lib) - oracle.gelu_tanh(-z, lib=lib)
+        assert abs(d - z) <= 4e-16 * max(z, 1.0), (z, d)
+    assert abs(oracle.gelu_tanh(12.0, lib=lib) - 12.0) < 1e-12
+    assert abs(oracle.gelu_tanh(-12.0, lib=lib)) < 1e-12
+    # Near 0: GeLU(z) = z/2 + sqrt(2/pi) z^2 / 2 + O(z^4)
+    z = 1e-4
+    want = z / 2 + math.sqrt(2 / math.pi) * z * z / 2
+    assert abs(oracle.gelu_tanh(z, lib=lib) - want) < 1e-15
+
+
+def pin_bf16_roundtrip(lib):
+    """Every finite bf16 value widens and rounds back to itself."""
+    for h in list(range(0, 0x7F80, 97)) + [0x0001, 0x007F, 0x0080, 0x3F80,
+                                           0x7F7F, 0x8001, 0xBF80, 0xFF7F]:
+        d = oracle.bf16_to_double(h, lib=lib)
+        assert oracle.bf16_from_double(d, lib=lib) == h, hex(h)
+
+
+def pin_bf16_rounding(lib):
+    """Nearest, ties to even: hand cases at 1.0 (quantum 2^-7), the overflow
+    edge and the subnormal range; then torch's fp32 -> bf16 on random fp32
+    values (a double holding an fp32 value rounds like that fp32)."""
+    cases = [
+        (1.0, 0x3F80),
+        (1.0 + 2.0 ** -8, 0x3F80),                  # tie -> even (down)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),              # tie -> even (up)
+        (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),     # just above the tie
+        (1.0 + 2.0 ** -8 - 2.0 ** -30, 0x3F80),     # just below the tie
+        (-1.0 - 2.0 ** -7, 0xBF81),
+        (2.0 ** -133, 0x0001),                      # smallest subnormal
+        (1.5 * 2.0 ** -133, 0x0002),                # tie -> even (up)
+        (2.0 ** -134, 0x0000),                      # tie -> even (zero)
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),     # largest finite
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),     # rounds up to inf
+        (float("inf"), 0x7F80),
+        (-0.0, 0x8000),
+    ]
+    for v, want in cases:
+        got = oracle.bf16_from_double(v, lib=lib)
+        assert got == want, (v, hex(got), hex(want))
+    rng = np.random.default_rng(7)
+    f = (rng.standard_normal(2000) * np.exp(rng.uniform(-30, 30, 2000))).astype(np.float32)
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_from_double(float(v), lib=lib) for v in f], np.uint16)
+    assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------------------------
+# o1: y = relu(x + b1) * scale + b2     [P1] §1.1, §3.1
+# --------------------------------------------------------------------------
+
+def pin_pointwise_golden(lib):
+    """Hand-computed dyadic cases: every step is exact in fp32."""
+    g = _golden("pointwise_f32.json")
+    for case in g["cases"]:
+        x, b1, b2 = (np.array(case[k], np.float32) for k in ("x", "b1", "b2"))
+        y = oracle.add_relu_scale(x, b1, b2, case["scale"], lib=lib)
+        assert np.array_equal(y, np.array(case["y"], np.float32)), (case, y)
+
+
+def pin_pointwise_library(lib):
+    """torch CPU eager fp32, the [P1] §3.1 baseline (add, relu, mul, add:
+    four separately rounded ops), bit for bit, at scale 0.5 and 0.3."""
+    w = __import__("synth.workloads", fromlist=["x"]).POINTWISE_TINY
+    t = w.generate_all()
+    x, b1, b2 = (torch.from_numpy(t[k]) for k in ("x", "b1", "b2"))
+    for scale in (0.5, 0.3):
+        want = (torch.relu(x + b1) * scale + b2).numpy()
+        got = oracle.add_relu_scale(t["x"], t["b1"], t["b2"], scale, lib=lib)
+        assert np.array_equal(_bits(got), _bits(want)), scale
+
+
+def pin_pointwise_special(lib):
+    """x + b1 <= 0 gives y = b2 exactly; scale 1, b2 = 0 gives relu(x + b1)."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(512).astype(np.float32)
+    b1 = (-x - np.abs(rng.standard_normal(512)).astype(np.float32))
+    b2 = rng.standard_normal(512).astype(np.float32)
+    y = oracle.add_relu_scale(x, b1, b2, 0.5, lib=lib)
+    assert np.array_equal(_bits(y), _bits(b2))
+    b1 = rng.standard_normal(512).astype(np.float32)
+    y = oracle.add_relu_scale(x, b1, np.zeros(512, np.float32), 1.0, lib=lib)
+    assert np.array_equal(_bits(y), _bits(np.maximum(x + b1, np.float32(0))))
+
+
+def pin_pointwise_bf16_library(lib):
+    """bf16 I/O: widen, fp32 chain (torch eager fp32), one bf16 rounding
+    (torch fp32 -> bf16)."""
+    n = 3000
+    x = synth.normal(11, 0, (n,), dtype="bf16")
+    b1 = synth.normal(11, 1, (n,), dtype="bf16")
+    b2 = synth.normal(11, 2, (n,), dtype="bf16")
+    xf, b1f, b2f = (torch.from_numpy(synth.bf16_bits_to_f32(a)) for a in (x, b1, b2))
+    want = (torch.relu(xf + b1f) * 0.5 + b2f).to(torch.bfloat16)
+    want = want.view(torch.int16).numpy().view(np.uint16)
+    got = oracle.add_relu_scale(x, b1, b2, 0.5, lib=lib)
+    assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------------------------
+# o2: TorchInductor example chain       [P4] "model", Figure 1
+# --------------------------------------------------------------------------
+
+def pin_inductor_golden(lib):
+    """Hand-computed dyadic 1x4 and 2x3 cases (x_scale, branch_scale chosen
+    dyadic so every step is exact)."""
+    g = _golden("inductor_f32.json")
+    for case in g["cases"]:
+        x = np.array(case["x"], np.float32)
+        vecs = [np.array(case[k], np.float32) for k in ("bias", "gamma", "beta")]
+        y = oracle.bias_relu_branch_mean_epilogue(
+            x, *vecs, case["x_scale"], case["branch_scale"], lib=lib)
+        assert np.array_equal(y, np.array(case["y"], np.float32)), (case["name"], y)
+
+
+def pin_inductor_library_s(lib):
+    """s (t = x*1.1 + bias; a = relu(t); p = a*a; q = a*0.1; s = p + q) against
+    torch CPU eager fp32 running the page's model() steps, bit for bit; the
+    mean against the float64 mean of that s to one fp32 rounding."""
+    w = __import__("synth.workloads", fromlist=["x"]).INDUCTOR_1024
+    t = w.generate_all(rows=64)
+    x, bias = torch.from_numpy(t["x"]), torch.from_numpy(t["bias"])
+    tt = x * 1.1 + bias
+    a = torch.relu(tt)
+    s_want = (a * a + a * 0.1).numpy()
+    y, s, m = oracle.bias_relu_branch_mean_epilogue(
+        t["x"], t["bias"], t["gamma"], t["beta"], 1.1, 0.1, intermediates=True,
+        lib=lib)
+    assert np.array_equal(_bits(s), _bits(s_want))
+    m_want = s_want.astype(np.float64).mean(axis=1)
+    assert np.all(np.abs(m - m_want) <= U32 * np.abs(m_want) * 1.01)
+
+
+def pin_inductor_closed_form(lib):
+    """Per row, sum_j (y - beta)/gamma = sum_j (s - m) = cols*(mean(s) - m),
+    which is zero up to the rounding of m and of the three epilogue ops."""
+    w = __import__("synth.workloads", fromlist=["x"]).INDUCTOR_1024
+    t = w.generate_all(rows=32)
+    y, s, m = oracle.bias_relu_branch_mean_epilogue(
+        t["x"], t["bias"], t["gamma"], t["beta"], 1.1, 0.1, intermediates=True,
+        lib=lib)
+    y64 = y.astype(np.float64)
+    g64 = t["gamma"].astype(np.float64)
+    b64 = t["beta"].astype(np.float64)
+    lhs = ((y64 - b64) / g64).sum(axis=1)
+    s64 = s.astype(np.float64)
+    m64 = m.astype(np.float64)[:, None]
+    bound = (s.shape[1] * U32 * np.abs(m64[:, 0])
+             + (2 * U32 * np.abs(s64 - m64) + U32 * np.abs(y64) / g64).sum(axis=1))
+    assert np.all(np.abs(lhs) <= 2 * bound), (np.abs(lhs) / bound).max()
+    # and m is the row mean of s
+    assert np.all(np.abs(m64[:, 0] - s64.mean(axis=1)) <= 1.01 * U32 * np.abs(m64[:, 0]))
+
+
+def pin_inductor_special(lib):
+    """A row with every t <= 0 gives s = 0, m = 0, y = beta exactly; a row of
+    one repeated x (bias 0) gives s constant, m = s, y = beta exactly."""
+    cols = 37
+    rng = np.random.default_rng(5)
+    gamma = rng.uniform(0.5, 1.5, cols).astype(np.float32)
+    beta = rng.standard_normal(cols).astype(np.float32)
+    x = np.stack([-np.abs(rng.standard_normal(cols)).astype(np.float32) - 0.5,
+                  np.full(cols, 0.75, np.float32)])
+    bias = np.zeros(cols, np.float32)
+    y = oracle.bias_relu_branch_mean_epilogue(x, bias, gamma, beta, 1.1, 0.1, lib=lib)
+    assert np.array_equal(_bits(y[0]), _bits(beta))
+    assert np.array_equal(_bits(y[1]), _bits(beta))
+
+
+# --------------------------------------------------------------------------
+# o3: residual + LayerNorm + GeLU-tanh  [P2] §2.2-2.3, [P3] §4.3
+# --------------------------------------------------------------------------
+
+def _ln_inputs(rows, hidden, seed, dtype="f32"):
+    x = synth.normal(seed, 0, (rows, hidden), dtype=dtype)
+    r = synth.normal(seed, 1, (rows, hidden), dtype=dtype)
+    w = synth.uniform(seed, 2, (hidden,), 0.5, 1.5, dtype=dtype)
+    b = synth.normal(seed, 3, (hidden,), 0.0, 0.1, dtype=dtype)
+    return x, r, w, b
+
+
+def pin_ln_closed_forms(lib):
+    """Before the affine step each row has mean 0 and variance
+    var/(var + eps) ([P3] §4.3: (x - mean)/sqrt(var + eps))."""
+    x, r, w, b = _ln_inputs(16, 1000, 21)
+    eps = 1e-5
+    out, mean, rstd, xhat = oracle.residual_layernorm_gelu(
+        x, r, w, b, eps, intermediates=True, lib=lib)
+    v = (x + r).astype(np.float64)            # fp32 add, exact widening
+    var = ((v - v.mean(axis=1, keepdims=True)) ** 2).mean(axis=1)
+    assert np.all(np.abs(xhat.mean(axis=1)) <= 1e-12)
+    want_var = var / (var + np.float64(np.float32(eps)))
+    assert np.all(np.abs((xhat ** 2).mean(axis=1) - want_var) <= 1e-12)
+    assert np.all(np.abs(mean - v.mean(axis=1)) <= 1e-12)
+
+
+def pin_ln_library(lib):
+    """torch float64 layer_norm + gelu(tanh) on v = x + r (fp32 add),
+    rounded to fp32: equal to within one fp32 rounding."""
+    for rows, hidden in ((8, 4096), (5, 33), (3, 1)):
+        x, r, w, b = _ln_inputs(rows, hidden, 22 + hidden)
+        v = torch.from_numpy(x) + torch.from_numpy(r)
+        n = F.layer_norm(v.double(), (hidden,), torch.from_numpy(w).double(),
+                         torch.from_numpy(b).double(), eps=float(np.float32(1e-5)))
+        want = F.gelu(n, approximate="tanh").numpy()
+        got = oracle.residual_layernorm_gelu(x, r, w, b, 1e-5, lib=lib)
+        err = np.abs(got.astype(np.float64) - want)
+        assert np.all(err <= 1.0001 * U32 * np.abs(want) + 1e-12), err.max()
+
+
+def pin_ln_special(lib):
+    """H = 1: v - mean = 0, so out = GeLU(b).  A row [a, -a]: mean 0,
+    var a^2, so n = +-a/sqrt(a^2 + eps) * w + b."""
+    b = np.array([0.375], np.float32)
+    out = oracle.residual_layernorm_gelu(
+        np.array([[1.25]], np.float32), np.array([[-4.0]], np.float32),
+        np.array([1.5], np.float32), b, 1e-5, lib=lib)
+    want = F.gelu(torch.tensor([0.375], dtype=torch.float64), approximate="tanh")
+    assert out[0, 0] == np.float32(want.item())
+    a, eps = 3.0, float(np.float32(1e-5))
+    w = np.array([1.0, 2.0], np.float32)
+    bb = np.array([0.5, -0.25], np.float32)
+    out, mean, rstd, xhat = oracle.residual_layernorm_gelu(
+        np.array([[a, -a]], np.float32), np.zeros((1, 2), np.float32), w, bb,
+        1e-5, intermediates=True, lib=lib)
+    k = a / math.sqrt(a * a + eps)
+    assert abs(mean[0]) == 0.0
+    assert abs(rstd[0] - 1 / math.sqrt(a * a + eps)) <= 1e-16
+    n = torch.tensor([k * 1.0 + 0.5, -k * 2.0 - 0.25], dtype=torch.float64)
+    want = F.gelu(n, approximate="tanh").numpy().astype(np.float32)
+    assert np.array_equal(out[0], want)
+
+
+def pin_ln_bf16_library(lib):
+    """bf16 I/O: widen x, r, w, b exactly, fp32 add, float64 layer_norm +
+    gelu, round once to bf16.  torch rounds float64 -> bf16 through fp32, so
+    the two may differ by one bf16 step where that double rounding bites."""
+    x, r, w, b = _ln_inputs(6, 520, 31, dtype="bf16")
+    xf, rf, wf, bf = (torch.from_numpy(synth.bf16_bits_to_f32(a)) for a in (x, r, w, b))
+    v = xf + rf
+    n = F.layer_norm(v.double(), (520,), wf.double(), bf.double(),
+                     eps=float(np.float32(1e-5)))
+    g = F.gelu(n, approximate="tanh")
+    got = oracle.residual_layernorm_gelu(x, r, w, b, 1e-5, lib=lib)
+    gw = synth.bf16_bits_to_f32(got).astype(np.float64)
+    gd = g.numpy()
+    # within half a bf16 step of the float64 value: the step is 2^-7 of the
+    # binade's lower end, so at most 2^-8 of the value
+    assert np.all(np.abs(gw - gd) <= 2.0 ** -8 * np.abs(gd) * 1.0001 + 1e-30)
+    want = g.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.mean(got == want) > 0.999
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

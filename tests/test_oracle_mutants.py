@@ -1,0 +1,81 @@
+"""Planted mistakes in the CPU oracle must fail a pin.
+
+Each case copies ``oracle/oracle.c`` to a temporary directory, applies one
+plausible mistake (a dropped term, a wrong sign, a wrong divisor, a transposed
+operand, a contracted multiply-add, a wrong rounding), builds it with the same
+flags, and runs every pin of ``oracle_pins`` against it: at least one pin must
+fail.  The real oracle is never modified.  Runs without a GPU.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from oracle import build as oracle_build
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle_build.__file__), "oracle.c")
+HDR = os.path.join(os.path.dirname(oracle_build.__file__), "oracle.h")
+
+MUTANTS = {
+    # o1: y = relu(x + b1) * scale + b2
+    "o1_sign_b2": ("tmp = tmp + b2;", "tmp = tmp - b2;"),
+    "o1_drop_relu": ("tmp = oracle_relu_f32(tmp);", "(void)0;"),
+    "o1_fixed_scale": ("tmp = tmp * scale;", "tmp = tmp * 0.5f;"),
+    "o1_fma": ("tmp = tmp * scale;              /* step 3: * scale   -> tmp3 */\n"
+               "    tmp = tmp + b2;",
+               "tmp = fmaf(tmp, scale, b2);"),
+    "relu_keeps_neg_zero": ("if (v > 0.0f)", "if (v >= 0.0f)"),
+    # o2: TorchInductor example chain
+    "o2_mean_divisor": ("float m = (float)(sum / (double)cols);",
+                        "float m = (float)(sum / (double)(cols + 1));"),
+    "o2_gamma_beta_swapped": ("d = d * gamma[j];", "d = d * beta[j];"),
+    "o2_branch_uses_x_scale": ("float q = a * branch_scale;", "float q = a * x_scale;"),
+    "o2_drop_x_scale": ("float t = x * x_scale;", "float t = x;"),
+    "o2_drop_square": ("float p = a * a;", "float p = a;"),
+    "o2_sign_mean": ("float d = s - m;", "float d = s + m;"),
+    "o2_no_relu": ("float a = oracle_relu_f32(t);", "float a = t;"),
+    # o3: residual + LayerNorm + GeLU
+    "o3_drop_eps": ("double rstd = 1.0 / sqrt(var + (double)eps);",
+                    "double rstd = 1.0 / sqrt(var);"),
+    "o3_unbiased_var": ("double var = sq / (double)hidden;",
+                        "double var = sq / (double)(hidden - 1);"),
+    "o3_uncentred_var": ("double d = (double)v - mean;", "double d = (double)v;"),
+    "o3_mean_divisor": ("double mean = sum / (double)hidden;",
+                        "double mean = sum / (double)(hidden + 1);"),
+    "o3_drop_rstd": ("double xhat = ((double)v - mean) * rstd;",
+                     "double xhat = ((double)v - mean);"),
+    "o3_w_b_swapped": ("double n = xhat * (double)load(w, j) + (double)load(b, j);",
+                       "double n = xhat * (double)load(b, j) + (double)load(w, j);"),
+    "o3_residual_sign": ("float v = load(x, base + j) + load(r, base + j);",
+                         "float v = load(x, base + j) - load(r, base + j);"),
+    "gelu_cubic_dropped": ("0.044715 * z * z * z", "0.044715 * z * z"),
+    "gelu_tanh_sign": ("return 0.5 * z * (1.0 + tanh(u));",
+                       "return 0.5 * z * (1.0 - tanh(u));"),
+    "gelu_half_dropped": ("return 0.5 * z * (1.0 + tanh(u));",
+                          "return z * (1.0 + tanh(u));"),
+    "bf16_truncates": ("double k = rint(ldexp(a, -q));",
+                       "double k = floor(ldexp(a, -q));"),
+    "bf16_extra_bit": ("int q = e - 8;", "int q = e - 9;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_a_pin(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    shutil.copy(HDR, tmp_path / "oracle.h")
+    (tmp_path / "oracle.c").write_text(mutated)
+    so = oracle_build.build(src=str(tmp_path / "oracle.c"),
+                            out=str(tmp_path / f"liboracle_{name}.so"))
+    lib = oracle.load(so)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
