@@ -1,0 +1,492 @@
+"""Benchmark of the fused memory-bound chains on GB300.
+
+One step = one call of each fused chain on its at-scale synthetic workload:
+
+    pointwise_f32_4Mi          y = relu(x + b1) * 0.5 + b2, 4 Mi fp32 elements
+    inductor_f32_1024x1024     the TorchInductor example chain, fp32
+    ln_gelu_f32_8192x4096      residual + LayerNorm + GeLU-tanh, fp32
+    ln_gelu_bf16_32768x8192    residual + LayerNorm + GeLU-tanh, bf16 I/O
+
+value = the step's read-once/write-once bytes / the step's kernel time
+(effective HBM GB/s), with every input resident in device memory and the L2
+flushed (by reading a 1 GiB buffer) before each call, outside the timed
+events.  Per-kernel microseconds per call, GB/s and fraction of the measured
+HBM copy bandwidth are reported alongside, with the unfused eager PyTorch
+chain timed the same way.  `e2e` repeats the measurement through the same
+public API from pinned host buffers, host<->device copies inside the timed
+region.  `cpu_baseline` times the CPU oracle on a sample of the same step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs the full per-GPU workload (weak scaling) and
+rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import workloads as W  # noqa: E402
+
+STEP = (W.POINTWISE_4M, W.INDUCTOR_1024, W.LN_F32, W.LN_BF16)
+METRIC = "effective HBM GB/s per fused-chain step (read-once/write-once bytes / kernel time)"
+UNIT = "GB/s"
+WORKLOAD = ("fused_chains_step: pointwise_f32_4Mi + inductor_f32_1024x1024 + "
+            "ln_gelu_f32_8192x4096 + ln_gelu_bf16_32768x8192")
+FLUSH_BYTES = 1 << 30
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0}
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-eager", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# environment
+# --------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": PEAKS_FALLBACK["hbm_gbs"], "source": "fallback"}
+
+
+def source_hash():
+    """Hash of the CUDA sources, to tell whether stored ncu counters still
+    describe the kernels being timed."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "memory_bound_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(p).read().splitlines()
+    except OSError:
+        return None
+    cur = source_hash()
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) >= 3 and not ln.startswith("#") and parts[0] == kernel_key and parts[1] == cur:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.index, self.proc, self.enabled = index, None, enabled
+
+    def __enter__(self):
+        if self.enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.enabled or self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.out.splitlines():
+            f = [c.strip() for c in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def _dev(a, bf16, device):
+    import torch
+    if bf16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def _pinned(a, bf16):
+    import torch
+    t = torch.from_numpy(a.view(np.int16) if bf16 else a).pin_memory()
+    return t.view(torch.bfloat16) if bf16 else t
+
+
+class Case:
+    """One workload's device buffers and its calls (ours and eager)."""
+
+    def __init__(self, w, device):
+        import torch
+        self.w = w
+        self.bf16 = w.dtype == "bf16"
+        host = w.generate_all()
+        self.host = host
+        self.dev = {k: _dev(v, self.bf16, device) for k, v in host.items()}
+        shape = (w.cols,) if w.chain == "add_relu_scale" else (w.rows, w.cols)
+        dt = torch.bfloat16 if self.bf16 else torch.float32
+        self.out = torch.empty(shape, dtype=dt, device=device)
+        self.ideal = w.ideal_bytes()
+        self.in_bytes = sum(v.nbytes for v in host.values())
+        self.out_bytes = self.out.numel() * self.out.element_size()
+
+    def call(self, d=None, out=None):
+        import memory_bound_gb300 as mb
+        d = d or self.dev
+        out = self.out if out is None else out
+        p = self.w.params
+        if self.w.chain == "add_relu_scale":
+            mb.fused_add_relu_scale(d["x"], d["b1"], d["b2"], p["scale"], out=out)
+        elif self.w.chain == "inductor":
+            mb.fused_bias_relu_branch_mean_epilogue(d["x"], d["bias"], d["gamma"], d["beta"],
+                                                    p["x_scale"], p["branch_scale"], out=out)
+        else:
+            mb.fused_residual_layernorm_gelu(d["x"], d["r"], d["w"], d["b"], p["eps"], out=out)
+
+    def eager(self):
+        """The unfused PyTorch eager chain (the pages' motivating baseline)."""
+        import torch
+        import torch.nn.functional as F
+        d, p = self.dev, self.w.params
+        if self.w.chain == "add_relu_scale":
+            return torch.relu(d["x"] + d["b1"]) * p["scale"] + d["b2"]
+        if self.w.chain == "inductor":
+            t = d["x"] * p["x_scale"] + d["bias"]
+            a = torch.relu(t)
+            s = a * a + a * p["branch_scale"]
+            m = s.mean(dim=1, keepdim=True)
+            return (s - m) * d["gamma"] + d["beta"]
+        return F.gelu(F.layer_norm(d["x"] + d["r"], (self.w.cols,), d["w"], d["b"], p["eps"]),
+                      approximate="tanh")
+
+
+def time_calls(cases, fn, steps, warmup, flush):
+    """Per case, CUDA-event milliseconds of `fn(case)` for each timed step,
+    with the L2 flushed before every call (outside the events)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for c in cases:
+            flush()
+            fn(c)
+    torch.cuda.synchronize()
+    ev = {c.w.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(steps)] for c in cases}
+    for k in range(steps):
+        for c in cases:
+            flush()
+            a, b = ev[c.w.name][k]
+            a.record(stream)
+            fn(c)
+            b.record(stream)
+    torch.cuda.synchronize()
+    return {name: [a.elapsed_time(b) for a, b in pairs] for name, pairs in ev.items()}
+
+
+def time_e2e(cases, steps, warmup):
+    """Through the public API from pinned host buffers: per step and case,
+    H2D of every input, the call, D2H of the output, all inside the events."""
+    import torch
+    stream = torch.cuda.current_stream()
+    pinned = []
+    for c in cases:
+        hin = {k: _pinned(v, c.bf16) for k, v in c.host.items()}
+        hout = torch.empty(c.out.shape, dtype=c.out.dtype).pin_memory()
+        pinned.append((c, hin, hout))
+
+    def once(c, hin, hout):
+        for k, t in hin.items():
+            c.dev[k].copy_(t, non_blocking=True)
+        c.call()
+        hout.copy_(c.out, non_blocking=True)
+
+    for _ in range(warmup):
+        for item in pinned:
+            once(*item)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for k in range(steps):
+        evs[k][0].record(stream)
+        for item in pinned:
+            once(*item)
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    bi = sum(c.in_bytes for c in cases)
+    bo = sum(c.out_bytes for c in cases)
+    return ms, bi, bo
+
+
+def cpu_sample(fraction):
+    """The inputs of a `fraction` sample of the step: the first rows of each
+    row workload, the first elements of the pointwise one."""
+    out = []
+    for w in STEP:
+        if w.chain == "add_relu_scale":
+            n = max(1, int(round(w.cols * fraction)))
+            t = {k: np.ascontiguousarray(v[:n]) for k, v in w.generate_all().items()}
+            out.append((w, t, 16 * n, f"{w.name}: {n} of {w.cols} elements"))
+        else:
+            rows = max(1, int(round(w.rows * fraction)))
+            t = w.generate_all(rows=rows)
+            out.append((w, t, w.ideal_bytes(rows), f"{w.name}: {rows} of {w.rows} rows"))
+    return out
+
+
+def cpu_baseline(sample):
+    """The CPU oracle, as it stands, on a sample from cpu_sample().
+    Returns (GB/s, seconds, sample description)."""
+    import oracle
+    tot_bytes, tot_s = 0, 0.0
+    for w, t, nbytes, _ in sample:
+        t0 = time.perf_counter()
+        if w.chain == "add_relu_scale":
+            oracle.add_relu_scale(t["x"], t["b1"], t["b2"], w.params["scale"])
+        elif w.chain == "inductor":
+            oracle.bias_relu_branch_mean_epilogue(t["x"], t["bias"], t["gamma"], t["beta"],
+                                                  w.params["x_scale"], w.params["branch_scale"])
+        else:
+            oracle.residual_layernorm_gelu(t["x"], t["r"], t["w"], t["b"], w.params["eps"])
+        tot_s += time.perf_counter() - t0
+        tot_bytes += nbytes
+    return tot_bytes / tot_s / 1e9, tot_s, "; ".join(d for *_, d in sample)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import memory_bound_gb300 as mb
+    from memory_bound_gb300 import build as lib_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0 or world > 1:
+        lib_build.build()
+    if world > 1:
+        dist.barrier()
+    mb.load_library()
+    mb.set_row_path("auto")
+
+    # CPU baseline first (rank 0, N=1 only), before any GPU work is timed
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, secs, sample = cpu_baseline(cpu_sample(0.25))
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first quarter of each workload ({sample}); {secs:.1f} s single-threaded"}
+
+    cases = [Case(w, device) for w in STEP]
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device).fill_(1.0)
+
+    def flush():
+        flush_buf.sum()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        t_wall0 = time.perf_counter()
+        ours = time_calls(cases, lambda c: c.call(), args.steps, args.warmup, flush)
+        t_wall = time.perf_counter() - t_wall0
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.summary()
+
+    eager = None
+    if not args.no_eager:
+        eager = time_calls(cases, lambda c: c.eager(), max(5, args.steps // 5), 2, flush)
+
+    e2e = None
+    if not args.no_e2e:
+        ms, bi, bo = time_e2e(cases, max(5, args.steps // 5), 2)
+        e2e = (statistics.mean(ms), bi, bo)
+
+    peaks = measured_peaks()
+    per_kernel = {}
+    step_ms = 0.0
+    step_bytes = 0
+    for c in cases:
+        t = ours[c.w.name]
+        mean_ms = statistics.mean(t)
+        step_ms += mean_ms
+        step_bytes += c.ideal
+        gbs = c.ideal / (mean_ms * 1e-3) / 1e9
+        entry = {"us_per_call": round(mean_ms * 1e3, 3),
+                 "us_median": round(statistics.median(t) * 1e3, 3),
+                 "us_p10": round(float(np.percentile(t, 10)) * 1e3, 3),
+                 "us_p90": round(float(np.percentile(t, 90)) * 1e3, 3),
+                 "ideal_bytes": c.ideal, "gbs": round(gbs, 1),
+                 "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                 "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+        if c.w.chain != "add_relu_scale":
+            entry["launch"] = mb.row_plan("ln" if c.w.chain == "ln_gelu" else "inductor",
+                                          c.w.dtype, c.w.rows, c.w.cols)
+        if eager:
+            em = statistics.mean(eager[c.w.name])
+            entry["eager_us_per_call"] = round(em * 1e3, 3)
+            entry["speedup_vs_eager"] = round(em / mean_ms, 2)
+        per_kernel[c.w.name] = entry
+
+    # max over ranks of the step time; every rank did the same work
+    if world > 1:
+        tt = torch.tensor([step_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+
+    dominant = max(cases, key=lambda c: per_kernel[c.w.name]["us_per_call"])
+    dk = per_kernel[dominant.w.name]
+    achieved = dominant.ideal / (dk["us_per_call"] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant.w.name,
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy burst)",
+                "traffic": stored_traffic(dominant.w.name),
+                "algorithmic_bytes_per_launch": dominant.ideal}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32+bf16", "data": "synthetic (seeded SplitMix64/Box-Muller)",
+            "config": {"workload": WORKLOAD, "l2": "flushed before every call (1 GiB read)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "timing": "CUDA events per call on the launching stream; "
+                                 "ms_per_step = sum of per-call means"},
+            "kernels": per_kernel, "roofline": roofline,
+            "gpu_launches": args.steps * len(cases),
+            "wall_s_timed_region": round(t_wall, 3)}
+    if clocks:
+        line["clocks"] = clocks
+    if e2e:
+        e_ms, bi, bo = e2e
+        line["e2e"] = {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                       "ms_per_step": round(e_ms, 3),
+                       "note": "pinned host buffers -> H2D -> fused call -> D2H, per step"}
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle, timed on the host cores
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import build as oracle_build
+    oracle_build.build()
+    full_cpu_s = 32.0                   # whole step on one core, measured order
+    total = args.steps + args.warmup
+    fraction = min(0.125, 120.0 / (total * full_cpu_s))
+    inputs = cpu_sample(fraction)
+    for _ in range(args.warmup):
+        cpu_baseline(inputs)
+    vals, secs = [], []
+    sample = ""
+    for _ in range(args.steps):
+        gbs, s, sample = cpu_baseline(inputs)
+        vals.append(gbs)
+        secs.append(s)
+    value = sum(vals) / len(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.mean(secs), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16 (oracle: fp32 / fp64)",
+            "data": "synthetic (seeded SplitMix64/Box-Muller)",
+            "config": {"workload": WORKLOAD,
+                       "sample": f"{fraction:.4f} of each workload per step"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * memory_bound.h -- C ABI of the fused memory-bound chain library
+ * (libmemory_bound.so, CUDA for sm_103a).
+ *
+ * Three vertically fused chains, each one kernel launch that reads its inputs
+ * from device memory once and writes its output once:
+ *
+ *   fused_add_relu_scale                  y = relu(x + b1) * scale + b2
+ *   fused_bias_relu_branch_mean_epilogue  the TorchInductor example chain
+ *   fused_residual_layernorm_gelu         GeLU_tanh(LayerNorm(x + r) * w + b)
+ *
+ * Sources (the pages these chains come from):
+ *   [P1] "PyTorch operator fusion in practice", www.0539edu.com/news/5489619
+ *   [P2] "Operator fusion and kernel optimisation: from CUDA Graph to
+ *        FlashAttention", plumephp.com/ai-kernel-fusion-optimization
+ *   [P3] "Kernel fusion", course chapter 4, www.5688vip.com
+ *   [P4] "TorchInductor Pipeline and operator fusion", blog.kkkzoz.top
+ *
+ * Conventions shared by every entry point:
+ *
+ *   Pointers    Device pointers (or any pointer the current device can
+ *               dereference).  The caller owns every buffer, outputs
+ *               included: the library never allocates, frees or copies
+ *               buffers and never synchronises the stream.
+ *   Layout      Contiguous, row-major.  Per-column vectors (length cols /
+ *               hidden) are broadcast over all rows (a stride-0 row view).
+ *   dtype       MB_F32 (IEEE binary32) or MB_BF16 (bfloat16, raw 16-bit
+ *               patterns).  All tensors of one call share the dtype;
+ *               arithmetic is fp32 and bf16 results are rounded to nearest,
+ *               ties to even.
+ *   Alignment   Every pointer must be aligned to its element size, else
+ *               MB_ERR_ALIGN.  Pointers that are 16-byte aligned (and rows
+ *               whose byte length is a multiple of 16) take the vectorised
+ *               paths; anything else still runs, on a scalar path.
+ *   Aliasing    The output may not overlap any input (MB_ERR_OVERLAP).
+ *               Inputs may overlap one another.
+ *   Sizes       Zero rows / zero elements is a no-op returning MB_OK without
+ *               touching the GPU.  Row lengths are 1 .. MB_MAX_COLS.
+ *   Stream      Work is enqueued on `stream` (0 = the legacy default stream)
+ *               on the current device.  The call is asynchronous; no host
+ *               synchronisation, allocation or host-device copy happens, so
+ *               calls may be captured into a CUDA graph.
+ *   Errors      Argument errors are found on the host before anything is
+ *               launched, and the call returns without side effects.
+ *               A failed launch returns MB_ERR_CUDA (see mb_last_cuda_error).
+ *               Faults during execution surface at the caller's next
+ *               synchronisation, as for any CUDA kernel.  The staged row path
+ *               waits on shared-memory barriers with a time limit; if a wait
+ *               ever ran out, the kernel stops early and records it in a
+ *               device flag that mb_device_error() reports.
+ *   Threads     Entry points may be called from several host threads.
+ *               mb_set_row_path changes process-wide state and should not
+ *               race with calls.
+ */
+#ifndef MEMORY_BOUND_H
+#define MEMORY_BOUND_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MB_ABI_VERSION 1
+
+/* Longest row (cols / hidden) the row chains accept. */
+#define MB_MAX_COLS 32768
+
+typedef enum mb_status {
+    MB_OK = 0,
+    MB_ERR_NULL = 1,      /* a pointer that must be read or written is NULL     */
+    MB_ERR_SHAPE = 2,     /* negative size, zero row length, or above a limit   */
+    MB_ERR_DTYPE = 3,     /* dtype code not supported by this entry point      */
+    MB_ERR_OVERLAP = 4,   /* the output range overlaps an input range          */
+    MB_ERR_ALIGN = 5,     /* a pointer is not aligned to its element size      */
+    MB_ERR_VALUE = 6,     /* a scalar argument is NaN/inf, or eps < 0          */
+    MB_ERR_CUDA = 7,      /* the CUDA runtime reported an error                */
+    MB_ERR_DEVICE = 8     /* a kernel recorded a device-side failure           */
+} mb_status;
+
+typedef enum mb_dtype {
+    MB_F32 = 0,
+    MB_BF16 = 1
+} mb_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Fused chains                                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * y[i] = relu(x[i] + b1[i]) * scale + b2[i],   0 <= i < n.
+ *
+ * [P1] §1.1 (the chain and its four eager kernels) and §3.2 (the fused
+ * float4 kernel, with relu written fmaxf(v, 0)).  fp32: the four operations
+ * are rounded one at a time in that order (no fused multiply-add), so the
+ * result equals the eager fp32 sequence bit for bit.  relu maps every value
+ * that is not > 0 (including -0 and NaN) to +0.  bf16: inputs are widened
+ * exactly, the same fp32 sequence runs, and y is rounded once to bf16.
+ *
+ *   x, b1, b2  n elements each (inputs)         y  n elements (output)
+ *   n >= 0     scale finite                     dtype MB_F32 or MB_BF16
+ */
+mb_status fused_add_relu_scale(const void *x, const void *b1, const void *b2,
+                               void *y, int64_t n, float scale, mb_dtype dtype,
+                               cudaStream_t stream);
+
+/*
+ * TorchInductor example chain, row by row over a rows x cols fp32 matrix:
+ *   t = x * x_scale + bias[j];  a = relu(t);  p = a * a;  q = a * branch_scale;
+ *   s = p + q;  m[i] = mean_j s[i, j];  y = (s - m[i]) * gamma[j] + beta[j]
+ *
+ * [P4] the example model at the top of the post (x_scale = 1.1,
+ * branch_scale = 0.1), Figure 1, §6.4 (the mean is a row sum divided by the
+ * row length) and §08 (one persistent-reduction kernel: x read once, the row
+ * sum kept on chip, y written once).  The pointwise steps are rounded one at
+ * a time as fp32 ops; the row sum is an fp32 tree sum; relu as above.
+ *
+ *   x      rows x cols (input)          bias, gamma, beta   cols each (input)
+ *   y      rows x cols (output)         rows >= 0, 1 <= cols <= MB_MAX_COLS
+ *   x_scale, branch_scale finite
+ */
+mb_status fused_bias_relu_branch_mean_epilogue(const float *x, const float *bias,
+                                               const float *gamma,
+                                               const float *beta, float *y,
+                                               int64_t rows, int64_t cols,
+                                               float x_scale, float branch_scale,
+                                               cudaStream_t stream);
+
+/*
+ * out = GeLU_tanh(LayerNorm(x + r) * w + b), row by row over rows x hidden:
+ *   v = x + r;  mean = sum(v)/H;  var = sum((v - mean)^2)/H  (biased);
+ *   rstd = 1/sqrt(var + eps);  n = (v - mean) * rstd * w[j] + b[j];
+ *   out = 0.5 n (1 + tanh(sqrt(2/pi) (n + 0.044715 n^3)))
+ *
+ * [P2] §2.2-2.3 (the residual + LayerNorm + GeLU fused kernel; the affine
+ * step is applied before the GeLU, as its code does) and [P3] §4.3 (LayerNorm:
+ * mean, two-pass variance, (v - mean)/sqrt(var + eps) * gamma + beta).
+ * v is the fp32 sum of the (widened) inputs; statistics are fp32 tree sums
+ * over the row held on chip (two passes); the output is rounded once to the
+ * I/O dtype.
+ *
+ *   x, r   rows x hidden (input)        w, b   hidden each (input)
+ *   out    rows x hidden (output)       rows >= 0, 1 <= hidden <= MB_MAX_COLS
+ *   eps    finite, >= 0                 dtype  MB_F32 or MB_BF16 (all tensors)
+ */
+mb_status fused_residual_layernorm_gelu(const void *x, const void *r,
+                                        const void *w, const void *b, void *out,
+                                        int64_t rows, int64_t hidden, float eps,
+                                        mb_dtype dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status, diagnostics and tuning                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Static, NUL-terminated description of a status code. */
+const char *mb_status_string(mb_status s);
+
+/* MB_ABI_VERSION of the loaded library. */
+int mb_abi_version(void);
+
+/* The cudaError_t (as int) behind the last MB_ERR_CUDA returned on the
+ * calling host thread; 0 if none. */
+int mb_last_cuda_error(void);
+
+/*
+ * Reads and clears the device-side failure flags of the current device
+ * (bit 0: a staged-row barrier wait ran out of time).  Synchronises the
+ * device.  *flags receives the bits; returns MB_ERR_DEVICE if any bit was
+ * set, MB_OK if none, MB_ERR_NULL / MB_ERR_CUDA on failure.
+ */
+mb_status mb_device_error(uint32_t *flags);
+
+/* Row-chain execution paths (both row chains). */
+typedef enum mb_row_path {
+    MB_ROW_AUTO = 0,     /* choose by shape and alignment (default)            */
+    MB_ROW_WARP = 1,     /* one warp per row, row in registers                */
+    MB_ROW_DIRECT = 2,   /* one CTA per row, vector loads into registers      */
+    MB_ROW_STAGED = 3    /* one CTA per row, rows staged into shared memory by
+                            bulk async copies in a multi-stage ring            */
+} mb_row_path;
+
+/*
+ * Process-wide override of the row-chain path and launch shape, for tuning
+ * and testing.  ctas_per_sm and stages of 0 mean "choose automatically".
+ * A forced path that cannot serve a shape (MB_ROW_WARP beyond 256 vectors per
+ * row, MB_ROW_STAGED on unaligned rows or rows too long to double-buffer)
+ * falls back to the automatic choice.  Returns MB_ERR_VALUE on a bad code or
+ * a negative count.
+ */
+mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages);
+
+/*
+ * The launch the row chains would use for a shape, without launching:
+ * out[0] = path (mb_row_path), out[1] = threads per CTA, out[2] = CTAs,
+ * out[3] = values per thread slot (vectors per thread), out[4] = vector width
+ * in elements, out[5] = ring stages (staged path, else 0),
+ * out[6] = dynamic shared memory bytes.  `chain` is 0 for the LayerNorm
+ * chain, 1 for the TorchInductor chain; `aligned` says whether every pointer
+ * is 16-byte aligned.  Queries the current device (SM count, shared memory).
+ */
+mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,
+                      int aligned, int32_t out[7]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEMORY_BOUND_H */

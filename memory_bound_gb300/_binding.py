@@ -1,0 +1,217 @@
+"""ctypes binding of libmemory_bound.so (argument marshalling only)."""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libmemory_bound.so")
+
+MB_F32, MB_BF16 = 0, 1
+MB_MAX_COLS = 32768
+ROW_PATHS = {"auto": 0, "warp": 1, "direct": 2, "staged": 3}
+
+STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_NULL", 2: "MB_ERR_SHAPE", 3: "MB_ERR_DTYPE",
+                4: "MB_ERR_OVERLAP", 5: "MB_ERR_ALIGN", 6: "MB_ERR_VALUE",
+                7: "MB_ERR_CUDA", 8: "MB_ERR_DEVICE"}
+
+# Entry points declared in include/memory_bound.h: name -> (restype, argtypes)
+_P, _I64, _F, _I, _U32P, _I32P = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
+                                  ctypes.c_int, ctypes.POINTER(ctypes.c_uint32),
+                                  ctypes.POINTER(ctypes.c_int32))
+SIGNATURES = {
+    "fused_add_relu_scale": (_I, [_P, _P, _P, _P, _I64, _F, _I, _P]),
+    "fused_bias_relu_branch_mean_epilogue": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _F, _P]),
+    "fused_residual_layernorm_gelu": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]),
+    "mb_status_string": (ctypes.c_char_p, [_I]),
+    "mb_abi_version": (_I, []),
+    "mb_last_cuda_error": (_I, []),
+    "mb_device_error": (_I, [_U32P]),
+    "mb_set_row_path": (_I, [_I, _I, _I]),
+    "mb_row_plan": (_I, [_I, _I, _I64, _I64, _I, _I32P]),
+}
+
+_lib = None
+
+
+class MBError(RuntimeError):
+    """A non-MB_OK status from the library."""
+
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        msg = f"{fn}: {name} ({status_string(status)})"
+        if detail:
+            msg += f"; {detail}"
+        super().__init__(msg)
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load_library(path=None):
+    """Load libmemory_bound.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with memory_bound_gb300.build.build() "
+            "(the fused chains have no other implementation)")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class _Raw:
+    """The C entry points, loaded on first use."""
+
+    def __getattr__(self, name):
+        if name not in SIGNATURES:
+            raise AttributeError(name)
+        return getattr(load_library(), name)
+
+
+raw = _Raw()
+
+
+def status_string(status):
+    return load_library().mb_status_string(int(status)).decode()
+
+
+def _check(fn, status, detail=""):
+    if status != 0:
+        if status == 7:
+            detail = (detail + f" cudaError={load_library().mb_last_cuda_error()}").strip()
+        raise MBError(fn, status, detail)
+
+
+# --------------------------------------------------------------------------
+# torch tensor front end
+# --------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return MB_F32
+    if t.dtype == torch.bfloat16:
+        return MB_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _stream_handle(t):
+    torch = _torch()
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _require(tensors, dtype):
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (row-major)")
+        if t.dtype != dtype:
+            raise TypeError("all tensors of a call must share one dtype")
+        if t.device != tensors[0].device:
+            raise ValueError("all tensors of a call must be on one device")
+
+
+def fused_add_relu_scale(x, b1, b2, scale=0.5, out=None):
+    """y = relu(x + b1) * scale + b2, elementwise (float32 or bfloat16)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(x)
+    _require([x, b1, b2, out], x.dtype)
+    if not (x.numel() == b1.numel() == b2.numel() == out.numel()):
+        raise ValueError("x, b1, b2 and out must have one size")
+    with torch.cuda.device(x.device):
+        st = load_library().fused_add_relu_scale(
+            x.data_ptr(), b1.data_ptr(), b2.data_ptr(), out.data_ptr(), x.numel(),
+            float(scale), _dtype_code(x), _stream_handle(x))
+    _check("fused_add_relu_scale", st)
+    return out
+
+
+def fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
+                                         branch_scale=0.1, out=None):
+    """The TorchInductor example chain on a 2-D float32 x (rows x cols)."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, cols)")
+    if out is None:
+        out = torch.empty_like(x)
+    _require([x, bias, gamma, beta, out], torch.float32)
+    rows, cols = x.shape
+    for v in (bias, gamma, beta):
+        if v.numel() != cols:
+            raise ValueError("per-column vectors must have cols elements")
+    if out.numel() != x.numel():
+        raise ValueError("out must match x")
+    with torch.cuda.device(x.device):
+        st = load_library().fused_bias_relu_branch_mean_epilogue(
+            x.data_ptr(), bias.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+            out.data_ptr(), rows, cols, float(x_scale), float(branch_scale),
+            _stream_handle(x))
+    _check("fused_bias_relu_branch_mean_epilogue", st)
+    return out
+
+
+def fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None):
+    """GeLU_tanh(LayerNorm(x + r) * w + b) over the last dim of a 2-D x."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, hidden)")
+    if out is None:
+        out = torch.empty_like(x)
+    _require([x, r, w, b, out], x.dtype)
+    rows, hidden = x.shape
+    if r.shape != x.shape or w.numel() != hidden or b.numel() != hidden:
+        raise ValueError("shape mismatch")
+    if out.numel() != x.numel():
+        raise ValueError("out must match x")
+    with torch.cuda.device(x.device):
+        st = load_library().fused_residual_layernorm_gelu(
+            x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(),
+            rows, hidden, float(eps), _dtype_code(x), _stream_handle(x))
+    _check("fused_residual_layernorm_gelu", st)
+    return out
+
+
+def device_error():
+    """Read and clear the current device's failure flags (synchronises)."""
+    flags = ctypes.c_uint32(0)
+    st = load_library().mb_device_error(ctypes.byref(flags))
+    if st not in (0, 8):
+        _check("mb_device_error", st)
+    return flags.value
+
+
+def set_row_path(path="auto", ctas_per_sm=0, stages=0):
+    """Process-wide override of the row-chain path ("auto", "warp",
+    "direct", "staged") and launch shape (0 = automatic)."""
+    code = ROW_PATHS[path] if isinstance(path, str) else int(path)
+    _check("mb_set_row_path", load_library().mb_set_row_path(code, ctas_per_sm, stages))
+
+
+def row_plan(chain, dtype, rows, cols, aligned=True):
+    """The launch a row chain would use: dict(path, threads, ctas, vpt, vec,
+    stages, smem).  chain: "ln" or "inductor"; dtype: "f32" or "bf16"."""
+    out = (ctypes.c_int32 * 7)()
+    code = {"ln": 0, "inductor": 1}[chain]
+    dt = {"f32": MB_F32, "bf16": MB_BF16}[dtype]
+    st = load_library().mb_row_plan(code, dt, rows, cols, int(bool(aligned)), out)
+    _check("mb_row_plan", st)
+    keys = ("path", "threads", "ctas", "vpt", "vec", "stages", "smem")
+    d = dict(zip(keys, list(out)))
+    d["path"] = {v: k for k, v in ROW_PATHS.items()}[d["path"]]
+    return d

@@ -1,0 +1,244 @@
+// api.cu -- the C ABI (include/memory_bound.h): argument checks, per-device
+// state, dispatch to the kernels, status reporting.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "memory_bound.h"
+
+namespace mb {
+
+namespace {
+
+// Device-side failure flags (one word per device; each device that loads the
+// library gets its own copy of this variable).
+__device__ unsigned g_dev_err = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+    int smem_per_sm = 0;
+    unsigned *dev_err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+RowTuning g_tuning{MB_ROW_AUTO, 0, 0};
+thread_local int g_last_cuda_error = 0;
+
+mb_status device_ctx(cudaStream_t stream, LaunchCtx *ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return MB_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_per_sm,
+                                        cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+                cudaSuccess ||
+            (e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.dev_err), g_dev_err)) !=
+                cudaSuccess)
+            return cuda_fail(e);
+        d.ready = true;
+    }
+    *ctx = LaunchCtx{stream, dev, d.sm_count, d.smem_optin, d.smem_per_sm, d.dev_err};
+    return MB_OK;
+}
+
+inline uintptr_t addr(const void *p) { return reinterpret_cast<uintptr_t>(p); }
+
+// [a, a + na) and [b, b + nb) share a byte.
+inline bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+    if (na <= 0 || nb <= 0) return false;
+    return addr(a) < addr(b) + (uintptr_t)nb && addr(b) < addr(a) + (uintptr_t)na;
+}
+
+inline bool aligned_to(const void *p, uintptr_t a) { return (addr(p) & (a - 1)) == 0; }
+
+inline int elem_size(mb_dtype d) { return d == MB_BF16 ? 2 : 4; }
+
+bool valid_dtype(mb_dtype d) { return d == MB_F32 || d == MB_BF16; }
+
+// Row-length check shared by the row chains.
+mb_status check_rows(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 1 || cols > MB_MAX_COLS) return MB_ERR_SHAPE;
+    // rows * cols elements must be addressable
+    if (rows > INT64_MAX / cols / 4) return MB_ERR_SHAPE;
+    return MB_OK;
+}
+
+}  // namespace
+
+mb_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return MB_ERR_CUDA;
+}
+
+}  // namespace mb
+
+using namespace mb;
+
+extern "C" {
+
+mb_status fused_add_relu_scale(const void *x, const void *b1, const void *b2, void *y,
+                               int64_t n, float scale, mb_dtype dtype, cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
+    if (n < 0 || n > INT64_MAX / 8) return MB_ERR_SHAPE;
+    if (!std::isfinite(scale)) return MB_ERR_VALUE;
+    if (n == 0) return MB_OK;
+    if (!x || !b1 || !b2 || !y) return MB_ERR_NULL;
+    const int es = elem_size(dtype);
+    for (const void *p : {x, b1, b2, static_cast<const void *>(y)})
+        if (!aligned_to(p, es)) return MB_ERR_ALIGN;
+    const int64_t bytes = n * es;
+    if (overlaps(y, bytes, x, bytes) || overlaps(y, bytes, b1, bytes) ||
+        overlaps(y, bytes, b2, bytes))
+        return MB_ERR_OVERLAP;
+    // Vector path when all four pointers sit at the same offset within 16
+    // bytes: a scalar head brings them to a 16-byte boundary together.
+    const uintptr_t m = addr(x) & 15;
+    const bool vec = (addr(b1) & 15) == m && (addr(b2) & 15) == m && (addr(y) & 15) == m;
+    int64_t head = vec ? (int64_t)((16 - m) & 15) / es : 0;
+    if (head > n) head = n;
+    LaunchCtx ctx;
+    mb_status st = device_ctx(stream, &ctx);
+    if (st != MB_OK) return st;
+    return add_relu_scale_run(ctx, dtype, x, b1, b2, y, n, scale, vec, (int)head);
+}
+
+mb_status fused_residual_layernorm_gelu(const void *x, const void *r, const void *w,
+                                        const void *b, void *out, int64_t rows,
+                                        int64_t hidden, float eps, mb_dtype dtype,
+                                        cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
+    mb_status st = check_rows(rows, hidden);
+    if (st != MB_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return MB_ERR_VALUE;
+    if (rows == 0) return MB_OK;
+    if (!x || !r || !w || !b || !out) return MB_ERR_NULL;
+    const int es = elem_size(dtype);
+    for (const void *p : {x, r, w, b, static_cast<const void *>(out)})
+        if (!aligned_to(p, es)) return MB_ERR_ALIGN;
+    const int64_t big = rows * hidden * es, small = hidden * es;
+    if (overlaps(out, big, x, big) || overlaps(out, big, r, big) ||
+        overlaps(out, big, w, small) || overlaps(out, big, b, small))
+        return MB_ERR_OVERLAP;
+    bool aligned = true;
+    for (const void *p : {x, r, w, b, static_cast<const void *>(out)})
+        aligned = aligned && aligned_to(p, 16);
+    LaunchCtx ctx;
+    if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
+    RowTuning tun = g_tuning;
+    if (dtype == MB_F32)
+        return ln_gelu_rows_f32(ctx, tun, x, r, w, b, out, rows, (int)hidden, eps, aligned,
+                                nullptr, true);
+    return ln_gelu_rows_bf16(ctx, tun, x, r, w, b, out, rows, (int)hidden, eps, aligned,
+                             nullptr, true);
+}
+
+mb_status fused_bias_relu_branch_mean_epilogue(const float *x, const float *bias,
+                                               const float *gamma, const float *beta,
+                                               float *y, int64_t rows, int64_t cols,
+                                               float x_scale, float branch_scale,
+                                               cudaStream_t stream) {
+    mb_status st = check_rows(rows, cols);
+    if (st != MB_OK) return st;
+    if (!std::isfinite(x_scale) || !std::isfinite(branch_scale)) return MB_ERR_VALUE;
+    if (rows == 0) return MB_OK;
+    if (!x || !bias || !gamma || !beta || !y) return MB_ERR_NULL;
+    for (const void *p : {(const void *)x, (const void *)bias, (const void *)gamma,
+                          (const void *)beta, (const void *)y})
+        if (!aligned_to(p, 4)) return MB_ERR_ALIGN;
+    const int64_t big = rows * cols * 4, small = cols * 4;
+    if (overlaps(y, big, x, big) || overlaps(y, big, bias, small) ||
+        overlaps(y, big, gamma, small) || overlaps(y, big, beta, small))
+        return MB_ERR_OVERLAP;
+    bool aligned = true;
+    for (const void *p : {(const void *)x, (const void *)bias, (const void *)gamma,
+                          (const void *)beta, (const void *)y})
+        aligned = aligned && aligned_to(p, 16);
+    LaunchCtx ctx;
+    if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
+    return inductor_rows_f32(ctx, g_tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
+                             branch_scale, aligned, nullptr, true);
+}
+
+const char *mb_status_string(mb_status s) {
+    switch (s) {
+        case MB_OK: return "ok";
+        case MB_ERR_NULL: return "a required pointer is NULL";
+        case MB_ERR_SHAPE: return "invalid or unsupported size";
+        case MB_ERR_DTYPE: return "unsupported dtype";
+        case MB_ERR_OVERLAP: return "output overlaps an input";
+        case MB_ERR_ALIGN: return "pointer not aligned to its element size";
+        case MB_ERR_VALUE: return "invalid scalar argument";
+        case MB_ERR_CUDA: return "CUDA runtime error";
+        case MB_ERR_DEVICE: return "device-side failure recorded";
+    }
+    return "unknown status";
+}
+
+int mb_abi_version(void) { return MB_ABI_VERSION; }
+
+int mb_last_cuda_error(void) { return g_last_cuda_error; }
+
+mb_status mb_device_error(uint32_t *flags) {
+    if (!flags) return MB_ERR_NULL;
+    LaunchCtx ctx;
+    mb_status st = device_ctx(0, &ctx);
+    if (st != MB_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned v = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_dev_err, sizeof v)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyToSymbol(g_dev_err, &zero, sizeof zero)) != cudaSuccess)
+        return cuda_fail(e);
+    *flags = v;
+    return v ? MB_ERR_DEVICE : MB_OK;
+}
+
+mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages) {
+    if (path < MB_ROW_AUTO || path > MB_ROW_STAGED || ctas_per_sm < 0 || stages < 0)
+        return MB_ERR_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_tuning = RowTuning{(int)path, ctas_per_sm, stages};
+    return MB_OK;
+}
+
+mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int aligned,
+                      int32_t out[7]) {
+    if (!out) return MB_ERR_NULL;
+    if (chain != 0 && chain != 1) return MB_ERR_VALUE;
+    if (!valid_dtype(dtype) || (chain == 1 && dtype != MB_F32)) return MB_ERR_DTYPE;
+    mb_status st = check_rows(rows, cols);
+    if (st != MB_OK) return st;
+    LaunchCtx ctx;
+    if ((st = device_ctx(0, &ctx)) != MB_OK) return st;
+    RowPlan p;
+    if (chain == 1)
+        st = inductor_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+                               (int)cols, 1.0f, 1.0f, aligned != 0, &p, false);
+    else if (dtype == MB_F32)
+        st = ln_gelu_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+                              (int)cols, 0.0f, aligned != 0, &p, false);
+    else
+        st = ln_gelu_rows_bf16(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+                               (int)cols, 0.0f, aligned != 0, &p, false);
+    if (st != MB_OK) return st;
+    out[0] = p.path; out[1] = p.threads; out[2] = p.ctas; out[3] = p.vpt;
+    out[4] = p.vec; out[5] = p.stages; out[6] = p.smem;
+    return MB_OK;
+}
+
+}  // extern "C"

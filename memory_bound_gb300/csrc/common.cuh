@@ -1,0 +1,222 @@
+// common.cuh -- device helpers shared by the fused-chain kernels (sm_103a).
+//
+// 16-byte fragments of fp32 / bf16 values, fp32 arithmetic helpers, warp and
+// block reductions, and inline-PTX wrappers for mbarrier and bulk async copies
+// (the Blackwell data-movement path used to stage rows into shared memory).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace mb {
+
+// Device-side failure bits (reported through mb_device_error).
+constexpr unsigned kDevErrWaitTimeout = 1u;
+
+// A barrier wait gives up after this many nanoseconds of %globaltimer (or this
+// many polls, whichever comes first).  Real waits finish in microseconds.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr unsigned kWaitLimitPolls = 1u << 28;
+
+// ---------------------------------------------------------------------------
+// scalar fp32 helpers
+// ---------------------------------------------------------------------------
+
+// relu with every value that is not > 0 (including -0 and NaN) mapped to +0.
+__device__ __forceinline__ float relu_f(float v) { return v > 0.0f ? v : 0.0f; }
+
+// 2^x and 1/x via the SFU (ex2.approx / rcp.approx, flush-to-zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// GeLU, tanh form, through the identity (1 + tanh(u)) / 2 = 1 / (1 + e^(-2u)):
+//   gelu(n) = n / (1 + 2^(n * (c1 + c2 n^2)))
+// with u = sqrt(2/pi) (n + 0.044715 n^3), c1 = -2 log2(e) sqrt(2/pi) and
+// c2 = 0.044715 c1.  No 1 + tanh cancellation for n << 0; the limits are exact
+// (2^t overflows to inf -> -0 for n << 0, underflows to 0 -> n for n >> 0).
+__device__ __forceinline__ float gelu_tanh_f(float n) {
+    constexpr double kSqrt2OverPi = 0.79788456080286535587989211986876;
+    constexpr double kLog2e = 1.4426950408889634073599246810019;
+    constexpr float c1 = (float)(-2.0 * kLog2e * kSqrt2OverPi);
+    constexpr float c2 = (float)(-2.0 * kLog2e * kSqrt2OverPi * 0.044715);
+    float n2 = n * n;
+    float t = n * fmaf(c2, n2, c1);
+    float e = ex2_approx(t);
+    return n * rcp_approx(1.0f + e);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 packing (raw 16-bit patterns, little-endian pairs in 32-bit words)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ uint16_t f_to_bf16(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// Fragments: VEC consecutive elements of one tensor as fp32 values.
+// VEC * sizeof(T) == 16 uses one 128-bit access; VEC == 1 is a scalar access.
+// T is float or uint16_t (bf16 bits).
+// ---------------------------------------------------------------------------
+
+template <typename T> struct Elem;
+template <> struct Elem<float> { static constexpr int kVec = 4; };
+template <> struct Elem<uint16_t> { static constexpr int kVec = 8; };
+
+template <typename T, int VEC> struct Frag {
+    float f[VEC];
+
+    __device__ __forceinline__ void unpack(const uint4 &u) {
+        if constexpr (sizeof(T) == 4) {
+            f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+            f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+        } else {
+            f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+            f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+            f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+            f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+        }
+    }
+    __device__ __forceinline__ uint4 pack() const {
+        uint4 u;
+        if constexpr (sizeof(T) == 4) {
+            u.x = __float_as_uint(f[0]); u.y = __float_as_uint(f[1]);
+            u.z = __float_as_uint(f[2]); u.w = __float_as_uint(f[3]);
+        } else {
+            u.x = pack_bf16x2(f[0], f[1]); u.y = pack_bf16x2(f[2], f[3]);
+            u.z = pack_bf16x2(f[4], f[5]); u.w = pack_bf16x2(f[6], f[7]);
+        }
+        return u;
+    }
+    __device__ __forceinline__ static float to_f(T v) {
+        if constexpr (sizeof(T) == 4) return v; else return bf16_to_f(v);
+    }
+    __device__ __forceinline__ static T from_f(float v) {
+        if constexpr (sizeof(T) == 4) return v; else return f_to_bf16(v);
+    }
+
+    // streaming load of row data (evict-first in cache)
+    __device__ __forceinline__ void load_stream(const T *p) {
+        if constexpr (VEC * sizeof(T) == 16) unpack(__ldcs(reinterpret_cast<const uint4 *>(p)));
+        else f[0] = to_f(__ldcs(p));
+    }
+    // cached read-only load (per-column vectors, reused by every row)
+    __device__ __forceinline__ void load_cached(const T *p) {
+        if constexpr (VEC * sizeof(T) == 16) unpack(__ldg(reinterpret_cast<const uint4 *>(p)));
+        else f[0] = to_f(__ldg(p));
+    }
+    __device__ __forceinline__ void load_shared(const T *p) {
+        if constexpr (VEC * sizeof(T) == 16) unpack(*reinterpret_cast<const uint4 *>(p));
+        else f[0] = to_f(*p);
+    }
+    __device__ __forceinline__ void store_stream(T *p) const {
+        if constexpr (VEC * sizeof(T) == 16) __stcs(reinterpret_cast<uint4 *>(p), pack());
+        else __stcs(p, from_f(f[0]));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// reductions (every lane / thread ends with the bitwise-same value)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+// Sum over the CTA.  `red` holds 32 floats of shared memory; callers alternate
+// between two such buffers so that one reduction's reads cannot race with the
+// next one's writes.  Every thread sums the per-warp partials in the same
+// order, so all threads get the same result.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    v = warp_sum(v);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[warp] = v;
+    __syncthreads();
+    const int nw = blockDim.x >> 5;
+    float s = 0.0f;
+    for (int i = 0; i < nw; ++i) s += red[i];
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk async copy (global -> shared), inline PTX
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory, completing on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after kWaitLimitNs
+// (or kWaitLimitPolls polls).  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (unsigned i = 0; i < kWaitLimitPolls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+}  // namespace mb

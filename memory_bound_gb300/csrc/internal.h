@@ -1,0 +1,56 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI; see include/memory_bound.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "memory_bound.h"
+
+namespace mb {
+
+// What a launcher needs to know about the current device and stream.
+struct LaunchCtx {
+    cudaStream_t stream;
+    int device;
+    int sm_count;
+    int smem_optin;        // max dynamic shared memory per block (opt-in)
+    int smem_per_sm;       // shared memory per multiprocessor
+    unsigned *dev_err;     // device-side failure flags of this device
+};
+
+// Process-wide row-chain override (mb_set_row_path).
+struct RowTuning {
+    int path;              // mb_row_path
+    int ctas_per_sm;       // 0 = automatic
+    int stages;            // 0 = automatic
+};
+
+// The launch a row chain uses (mb_row_plan reports it).
+struct RowPlan {
+    int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
+};
+
+// Chains implemented in their own translation units.  `launch == false`
+// only fills `plan`.
+mb_status add_relu_scale_run(const LaunchCtx &ctx, mb_dtype dtype, const void *x,
+                             const void *b1, const void *b2, void *y, int64_t n,
+                             float scale, bool aligned16, int head);
+
+mb_status ln_gelu_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
+                           const void *r, const void *w, const void *b, void *out,
+                           int64_t rows, int cols, float eps, bool aligned,
+                           RowPlan *plan, bool launch);
+mb_status ln_gelu_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
+                            const void *r, const void *w, const void *b, void *out,
+                            int64_t rows, int cols, float eps, bool aligned,
+                            RowPlan *plan, bool launch);
+mb_status inductor_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const float *x,
+                            const float *bias, const float *gamma, const float *beta,
+                            float *y, int64_t rows, int cols, float x_scale,
+                            float branch_scale, bool aligned, RowPlan *plan, bool launch);
+
+// Records a CUDA error for mb_last_cuda_error and returns MB_ERR_CUDA.
+mb_status cuda_fail(cudaError_t e);
+
+}  // namespace mb

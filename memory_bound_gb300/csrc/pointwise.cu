@@ -1,0 +1,117 @@
+// pointwise.cu -- y = relu(x + b1) * scale + b2, one streaming pass.
+//
+// "PyTorch operator fusion in practice" (0539edu.com) §1.1 and §3.2: the four
+// eager kernels (add, relu, mul, add) become one kernel that reads x, b1, b2
+// once and writes y once, with 16-byte vector accesses.  Here the grid is
+// sized to the SM count and each thread keeps UNROLL independent 16-byte
+// loads per input in flight; the unaligned head and the ragged tail are done
+// in-kernel (no padding by the caller).
+#include "common.cuh"
+#include "internal.h"
+
+namespace mb {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ float add_relu_scale_1(float x, float b1, float b2, float scale) {
+    float t = __fadd_rn(x, b1);       // x + b1
+    t = relu_f(t);                    // relu
+    t = __fmul_rn(t, scale);          // * scale
+    return __fadd_rn(t, b2);          // + b2
+}
+
+// Elements [0, head) and [head + nvec*VEC, n) are done one by one by the
+// first threads of block 0; [head, head + nvec*VEC) by 16-byte fragments.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kThreads)
+add_relu_scale_kernel(const T *__restrict__ x, const T *__restrict__ b1,
+                      const T *__restrict__ b2, T *__restrict__ y, int64_t n, int head,
+                      int64_t nvec, float scale) {
+    using F = Frag<T, VEC>;
+    using F1 = Frag<T, 1>;
+    const int64_t body_end = head + nvec * VEC;
+    if (blockIdx.x == 0) {
+        const int t = threadIdx.x;
+        const int64_t tail = n - body_end;
+        int64_t i = -1;
+        if (t < head) i = t;
+        else if (t - head < tail) i = body_end + (t - head);
+        if (i >= 0) {
+            F1 fx, f1, f2, fy;
+            fx.load_stream(x + i); f1.load_stream(b1 + i); f2.load_stream(b2 + i);
+            fy.f[0] = add_relu_scale_1(fx.f[0], f1.f[0], f2.f[0], scale);
+            fy.store_stream(y + i);
+        }
+    }
+    const T *xv = x + head, *b1v = b1 + head, *b2v = b2 + head;
+    T *yv = y + head;
+    const int64_t stride = (int64_t)gridDim.x * kThreads * kUnroll;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nvec;
+         base += stride) {
+        F fx[kUnroll], f1[kUnroll], f2[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) {
+                fx[u].load_stream(xv + i * VEC);
+                f1[u].load_stream(b1v + i * VEC);
+                f2[u].load_stream(b2v + i * VEC);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) {
+                F fy;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    fy.f[e] = add_relu_scale_1(fx[u].f[e], f1[u].f[e], f2[u].f[e], scale);
+                fy.store_stream(yv + i * VEC);
+            }
+        }
+    }
+}
+
+template <typename T>
+mb_status launch(const LaunchCtx &ctx, const void *x, const void *b1, const void *b2, void *y,
+                 int64_t n, float scale, bool vec, int head) {
+    constexpr int VN = Elem<T>::kVec;
+    const void *fn;
+    int64_t nvec;
+    if (vec) {
+        fn = (const void *)add_relu_scale_kernel<T, VN>;
+        nvec = (n - head) / VN;
+    } else {
+        fn = (const void *)add_relu_scale_kernel<T, 1>;
+        head = 0;
+        nvec = n;
+    }
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (occ < 1) occ = 1;
+    int64_t want = (nvec + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
+    if (want < 1) want = 1;   // block 0 also does the head and tail
+    const int64_t cap = (int64_t)occ * ctx.sm_count;
+    const int grid = (int)(want < cap ? want : cap);
+    const T *px = static_cast<const T *>(x), *p1 = static_cast<const T *>(b1),
+            *p2 = static_cast<const T *>(b2);
+    T *py = static_cast<T *>(y);
+    void *args[] = {&px, &p1, &p2, &py, &n, &head, &nvec, &scale};
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, ctx.stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MB_OK;
+}
+
+}  // namespace
+
+mb_status add_relu_scale_run(const LaunchCtx &ctx, mb_dtype dtype, const void *x,
+                             const void *b1, const void *b2, void *y, int64_t n, float scale,
+                             bool vec, int head) {
+    if (dtype == MB_F32) return launch<float>(ctx, x, b1, b2, y, n, scale, vec, head);
+    return launch<uint16_t>(ctx, x, b1, b2, y, n, scale, vec, head);
+}
+
+}  // namespace mb

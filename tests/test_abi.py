@@ -1,0 +1,115 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import memory_bound_gb300 as mb
+from memory_bound_gb300 import build as lib_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "memory_bound.h")
+
+MB_OK, MB_ERR_NULL, MB_ERR_SHAPE, MB_ERR_DTYPE, MB_ERR_OVERLAP = 0, 1, 2, 3, 4
+MB_ERR_ALIGN, MB_ERR_VALUE = 5, 6
+
+# Fake but 16-byte aligned, non-overlapping "device" addresses: none of the
+# calls below gets as far as using them.
+A, B, C, D, E = (0x10000000 * k for k in range(1, 6))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return mb.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if not n.startswith("defined")))
+
+
+def test_header_declares_the_three_chains():
+    names = declared_functions()
+    for n in ("fused_add_relu_scale", "fused_residual_layernorm_gelu",
+              "fused_bias_relu_branch_mean_epilogue"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding knows each of them
+    assert set(names) <= set(mb._binding.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mb_abi_version() == 1
+    for s in range(9):
+        assert len(mb.status_string(s)) > 0
+    assert mb.status_string(99) == "unknown status"
+
+
+def test_pointwise_argument_checks(lib):
+    f = lib.fused_add_relu_scale
+    assert f(A, B, C, D, 0, 0.5, 0, None) == MB_OK          # empty: no-op
+    assert f(A, B, C, D, 10, 0.5, 2, None) == MB_ERR_DTYPE
+    assert f(A, B, C, D, -1, 0.5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, 10, float("nan"), 0, None) == MB_ERR_VALUE
+    assert f(A, B, C, D, 10, float("inf"), 0, None) == MB_ERR_VALUE
+    assert f(None, B, C, D, 10, 0.5, 0, None) == MB_ERR_NULL
+    assert f(A, B, C, None, 10, 0.5, 0, None) == MB_ERR_NULL
+    assert f(A + 2, B, C, D, 10, 0.5, 0, None) == MB_ERR_ALIGN   # f32 needs 4
+    assert f(A + 1, B, C, D, 10, 0.5, 1, None) == MB_ERR_ALIGN   # bf16 needs 2
+    assert f(A, B, C, A + 36, 10, 0.5, 0, None) == MB_ERR_OVERLAP
+    assert f(A, B, C, C - 4, 10, 0.5, 0, None) == MB_ERR_OVERLAP  # y ends inside b2
+
+
+def test_layernorm_argument_checks(lib):
+    f = lib.fused_residual_layernorm_gelu
+    assert f(A, B, C, D, E, 0, 64, 1e-5, 0, None) == MB_OK
+    assert f(A, B, C, D, E, 4, 0, 1e-5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, E, 4, mb.MB_MAX_COLS + 1, 1e-5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, E, -1, 64, 1e-5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, E, 4, 64, -1e-5, 0, None) == MB_ERR_VALUE
+    assert f(A, B, C, D, E, 4, 64, float("nan"), 1, None) == MB_ERR_VALUE
+    assert f(A, B, C, D, E, 4, 64, 1e-5, 5, None) == MB_ERR_DTYPE
+    assert f(A, B, None, D, E, 4, 64, 1e-5, 0, None) == MB_ERR_NULL
+    assert f(A, B, C, D, A + 64, 4, 64, 1e-5, 0, None) == MB_ERR_OVERLAP
+    assert f(A, B, C, D, C - 16, 4, 64, 1e-5, 0, None) == MB_ERR_OVERLAP  # over w
+    assert f(A, B, C + 2, D, E, 4, 64, 1e-5, 0, None) == MB_ERR_ALIGN
+
+
+def test_inductor_argument_checks(lib):
+    f = lib.fused_bias_relu_branch_mean_epilogue
+    assert f(A, B, C, D, E, 0, 1024, 1.1, 0.1, None) == MB_OK
+    assert f(A, B, C, D, E, 8, 0, 1.1, 0.1, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, E, 8, 1024, float("nan"), 0.1, None) == MB_ERR_VALUE
+    assert f(A, None, C, D, E, 8, 1024, 1.1, 0.1, None) == MB_ERR_NULL
+    assert f(A, B, C, D, A + 4096, 8, 1024, 1.1, 0.1, None) == MB_ERR_OVERLAP
+    assert f(A + 1, B, C, D, E, 8, 1024, 1.1, 0.1, None) == MB_ERR_ALIGN
+
+
+def test_row_path_setter_validates(lib):
+    assert lib.mb_set_row_path(9, 0, 0) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(0, -1, 0) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(3, 2, 4) == MB_OK
+    assert lib.mb_set_row_path(0, 0, 0) == MB_OK
+
+
+def test_null_out_pointers(lib):
+    assert lib.mb_device_error(None) == MB_ERR_NULL
+    assert lib.mb_row_plan(0, 0, 8, 64, 1, None) == MB_ERR_NULL
+
+
+def test_binding_rejects_without_gpu_work():
+    import torch
+    x = torch.zeros(8)
+    with pytest.raises(ValueError):
+        mb.fused_add_relu_scale(x, x, x)          # CPU tensors are refused
