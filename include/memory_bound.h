@@ -182,13 +182,16 @@ typedef enum mb_row_path {
 
 /*
  * Process-wide override of the row-chain path and launch shape, for tuning
- * and testing.  ctas_per_sm and stages of 0 mean "choose automatically".
- * A forced path that cannot serve a shape (MB_ROW_WARP beyond 256 vectors per
- * row, MB_ROW_STAGED on unaligned rows or rows too long to double-buffer)
- * falls back to the automatic choice.  Returns MB_ERR_VALUE on a bad code or
- * a negative count.
+ * and testing.  ctas_per_sm (CTAs resident per SM), stages (ring depth of the
+ * staged path) and vec_per_thread (16-byte vectors each thread holds per row
+ * on the CTA paths; a power of two) of 0 mean "choose automatically"; a
+ * value that cannot serve a shape is ignored.  A forced path that cannot
+ * serve a shape (MB_ROW_WARP beyond 256 vectors per row, MB_ROW_STAGED on
+ * unaligned rows or rows too long for one stage) falls back to the automatic
+ * choice.  Returns MB_ERR_VALUE on a bad code or a negative count.
  */
-mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages);
+mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
+                          int vec_per_thread);
 
 /*
  * The launch the row chains would use for a shape, without launching:

@@ -25,7 +25,7 @@ SIGNATURES = {
     "mb_abi_version": (_I, []),
     "mb_last_cuda_error": (_I, []),
     "mb_device_error": (_I, [_U32P]),
-    "mb_set_row_path": (_I, [_I, _I, _I]),
+    "mb_set_row_path": (_I, [_I, _I, _I, _I]),
     "mb_row_plan": (_I, [_I, _I, _I64, _I64, _I, _I32P]),
 }
 
@@ -196,11 +196,12 @@ def device_error():
     return flags.value
 
 
-def set_row_path(path="auto", ctas_per_sm=0, stages=0):
+def set_row_path(path="auto", ctas_per_sm=0, stages=0, vec_per_thread=0):
     """Process-wide override of the row-chain path ("auto", "warp",
     "direct", "staged") and launch shape (0 = automatic)."""
     code = ROW_PATHS[path] if isinstance(path, str) else int(path)
-    _check("mb_set_row_path", load_library().mb_set_row_path(code, ctas_per_sm, stages))
+    _check("mb_set_row_path", load_library().mb_set_row_path(code, ctas_per_sm, stages,
+                                                             vec_per_thread))
 
 
 def row_plan(chain, dtype, rows, cols, aligned=True):

@@ -29,7 +29,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-RowTuning g_tuning{MB_ROW_AUTO, 0, 0};
+RowTuning g_tuning{MB_ROW_AUTO, 0, 0, 0};
 thread_local int g_last_cuda_error = 0;
 
 mb_status device_ctx(cudaStream_t stream, LaunchCtx *ctx) {
@@ -208,11 +208,13 @@ mb_status mb_device_error(uint32_t *flags) {
     return v ? MB_ERR_DEVICE : MB_OK;
 }
 
-mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages) {
-    if (path < MB_ROW_AUTO || path > MB_ROW_STAGED || ctas_per_sm < 0 || stages < 0)
+mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
+                          int vec_per_thread) {
+    if (path < MB_ROW_AUTO || path > MB_ROW_STAGED || ctas_per_sm < 0 || stages < 0 ||
+        vec_per_thread < 0)
         return MB_ERR_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);
-    g_tuning = RowTuning{(int)path, ctas_per_sm, stages};
+    g_tuning = RowTuning{(int)path, ctas_per_sm, stages, vec_per_thread};
     return MB_OK;
 }
 

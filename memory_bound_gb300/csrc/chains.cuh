@@ -22,9 +22,20 @@ template <typename TT> struct LnGeluChain {
         T *out;
         float eps;
     };
+    // per-column values of one slot: none before the reduction, w and b after
+    template <int VEC> struct PrePC {};
+    template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
+    static constexpr int kPostPC = 2;     // per-column vectors the epilogue reads
     template <int VEC>
-    __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[2], const Args &, int,
-                                               float (&v)[VEC]) {
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
+    template <int VEC>
+    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
+        pc.w.load_cached(a.w + col);
+        pc.b.load_cached(a.b + col);
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[2], const PrePC<VEC> &,
+                                               const Args &, float (&v)[VEC]) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) v[e] = __fadd_rn(in[0].f[e], in[1].f[e]);
     }
@@ -33,14 +44,12 @@ template <typename TT> struct LnGeluChain {
     }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float rstd,
-                                                const Args &a, int col, float (&o)[VEC]) {
-        Frag<T, VEC> w, b;
-        w.load_cached(a.w + col);
-        b.load_cached(a.b + col);
+                                                const PostPC<VEC> &pc, const Args &,
+                                                float (&o)[VEC]) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             const float xhat = (v[e] - mean) * rstd;
-            o[e] = gelu_tanh_f(fmaf(xhat, w.f[e], b.f[e]));
+            o[e] = gelu_tanh_f(fmaf(xhat, pc.w.f[e], pc.b.f[e]));
         }
     }
 };
@@ -65,14 +74,26 @@ struct InductorChain {
         float x_scale;
         float branch_scale;
     };
+    // per-column values of one slot: bias before the reduction, gamma and beta after
+    template <int VEC> struct PrePC { Frag<float, VEC> bias; };
+    template <int VEC> struct PostPC { Frag<float, VEC> gamma, beta; };
+    static constexpr int kPostPC = 2;
     template <int VEC>
-    __device__ __forceinline__ static void pre(const Frag<float, VEC> (&in)[1], const Args &a,
-                                               int col, float (&v)[VEC]) {
-        Frag<float, VEC> bias;
-        bias.load_cached(a.bias + col);
+    __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc) {
+        pc.bias.load_cached(a.bias + col);
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
+        pc.gamma.load_cached(a.gamma + col);
+        pc.beta.load_cached(a.beta + col);
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void pre(const Frag<float, VEC> (&in)[1],
+                                               const PrePC<VEC> &pc, const Args &a,
+                                               float (&v)[VEC]) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            const float t = __fadd_rn(__fmul_rn(in[0].f[e], a.x_scale), bias.f[e]);
+            const float t = __fadd_rn(__fmul_rn(in[0].f[e], a.x_scale), pc.bias.f[e]);
             const float r = relu_f(t);
             const float p = __fmul_rn(r, r);
             const float q = __fmul_rn(r, a.branch_scale);
@@ -82,13 +103,11 @@ struct InductorChain {
     __device__ __forceinline__ static float rstd(float, int, const Args &) { return 0.0f; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
-                                                const Args &a, int col, float (&o)[VEC]) {
-        Frag<float, VEC> g, b;
-        g.load_cached(a.gamma + col);
-        b.load_cached(a.beta + col);
+                                                const PostPC<VEC> &pc, const Args &,
+                                                float (&o)[VEC]) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-            o[e] = __fadd_rn(__fmul_rn(__fsub_rn(v[e], mean), g.f[e]), b.f[e]);
+            o[e] = __fadd_rn(__fmul_rn(__fsub_rn(v[e], mean), pc.gamma.f[e]), pc.beta.f[e]);
     }
 };
 

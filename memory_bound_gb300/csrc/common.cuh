@@ -144,17 +144,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Sum over the CTA.  `red` holds 32 floats of shared memory; callers alternate
 // between two such buffers so that one reduction's reads cannot race with the
-// next one's writes.  Every thread sums the per-warp partials in the same
-// order, so all threads get the same result.
+// next one's writes.  After the barrier every warp runs the same butterfly
+// over the per-warp partials (lane i holds partial i, zero past the last
+// warp), so all threads get the bitwise-same result.
 __device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v);
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) red[warp] = v;
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    const int nw = blockDim.x >> 5;
-    float s = 0.0f;
-    for (int i = 0; i < nw; ++i) s += red[i];
-    return s;
+    return warp_sum(lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f);
 }
 
 // ---------------------------------------------------------------------------

@@ -24,6 +24,7 @@ struct RowTuning {
     int path;              // mb_row_path
     int ctas_per_sm;       // 0 = automatic
     int stages;            // 0 = automatic
+    int vpt;               // vector slots per thread, 0 = automatic
 };
 
 // The launch a row chain uses (mb_row_plan reports it).

@@ -50,15 +50,16 @@ add_relu_scale_kernel(const T *__restrict__ x, const T *__restrict__ b1,
     const int64_t stride = (int64_t)gridDim.x * kThreads * kUnroll;
     for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nvec;
          base += stride) {
+        // All 3 * kUnroll loads are issued before any is used; slots past the
+        // end re-read the last fragment (in bounds) and are not stored.
         F fx[kUnroll], f1[kUnroll], f2[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int64_t i = base + (int64_t)u * kThreads;
-            if (i < nvec) {
-                fx[u].load_stream(xv + i * VEC);
-                f1[u].load_stream(b1v + i * VEC);
-                f2[u].load_stream(b2v + i * VEC);
-            }
+            int64_t i = base + (int64_t)u * kThreads;
+            i = i < nvec ? i : nvec - 1;
+            fx[u].load_stream(xv + i * VEC);
+            f1[u].load_stream(b1v + i * VEC);
+            f2[u].load_stream(b2v + i * VEC);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {

@@ -2,15 +2,18 @@
 //
 // A chain C supplies, per row of `cols` elements:
 //   pre   (per element)   the pointwise prologue, giving v from the row inputs
+//                         and the per-column values it needs (PrePC)
 //   mean  = sum(v) / cols (always), and with C::kTwoPass
 //   rstd  = C::rstd(sum((v - mean)^2), cols, args)   (second pass over v)
-//   post  (per element)   the epilogue from v, mean, rstd
+//   post  (per element)   the epilogue from v, mean, rstd and its per-column
+//                         values (PostPC)
 // The row is read from device memory once and held in registers (v) between
 // the passes; the output is written once.
 //
 // Engines:
-//   rows_warp_kernel  one warp per row (rows of <= 256 vectors): loads straight
-//                     into registers, shuffle reductions only, no barriers.
+//   rows_warp_kernel  one warp per row (rows of <= 256 vectors): every load of
+//                     the row and of its per-column values is issued at once,
+//                     shuffle reductions only, no barriers.
 //   rows_cta_kernel   one CTA per row, persistent over rows (row b, b + G, ...):
 //     DIRECT  vector loads into registers;
 //     STAGED  one elected thread streams whole rows into a ring of shared
@@ -19,6 +22,8 @@
 //             slot of row i is refilled with row i + nstage as soon as the
 //             first reduction barrier shows that every thread has copied row
 //             i into registers.
+// Several CTAs share an SM, each with its own row in flight, so one CTA's
+// loads overlap the others' reductions and epilogues.
 #pragma once
 
 #include "common.cuh"
@@ -30,6 +35,7 @@ constexpr int kCtaMaxThreads = 1024;
 constexpr int kWarpBlock = 256;
 constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
+constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
 
 // ---------------------------------------------------------------------------
 // one warp per row
@@ -45,19 +51,29 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
     for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows;
          row += nw) {
         const int64_t base = row * cols;
+        // Every load of the row and of its per-column values is issued before
+        // any is used: slots past the row end re-read the last vector (in
+        // bounds) and are masked below.
+        Frag<T, VEC> in[VPL][NIN];
+        typename C::template PrePC<VEC> pre[VPL];
+        typename C::template PostPC<VEC> post[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int vc = min(lane + 32 * k, nvec - 1);
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) in[k][i].load_stream(a.in[i] + base + vc * VEC);
+            C::template load_pre<VEC>(a, vc * VEC, pre[k]);
+            C::template load_post<VEC>(a, vc * VEC, post[k]);
+        }
         float v[VPL][VEC];
         float lsum = 0.0f;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
-            const int vi = lane + 32 * k;
-            if (vi < nvec) {
-                Frag<T, VEC> in[NIN];
+            C::template pre<VEC>(in[k], pre[k], a, v[k]);
+            float part = 0.0f;
 #pragma unroll
-                for (int i = 0; i < NIN; ++i) in[i].load_stream(a.in[i] + base + vi * VEC);
-                C::template pre<VEC>(in, a, vi * VEC, v[k]);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) lsum += v[k][e];
-            }
+            for (int e = 0; e < VEC; ++e) part += v[k][e];
+            lsum += lane + 32 * k < nvec ? part : 0.0f;
         }
         const float mean = warp_sum(lsum) / (float)cols;
         float rstd = 0.0f;
@@ -65,13 +81,13 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             float lm2 = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
-                if (lane + 32 * k < nvec) {
+                float part = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float d = v[k][e] - mean;
-                        lm2 = fmaf(d, d, lm2);
-                    }
+                for (int e = 0; e < VEC; ++e) {
+                    const float d = v[k][e] - mean;
+                    part = fmaf(d, d, part);
                 }
+                lm2 += lane + 32 * k < nvec ? part : 0.0f;
             }
             rstd = C::rstd(warp_sum(lm2), cols, a);
         }
@@ -80,7 +96,7 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             const int vi = lane + 32 * k;
             if (vi < nvec) {
                 Frag<T, VEC> o;
-                C::template post<VEC>(v[k], mean, rstd, a, vi * VEC, o.f);
+                C::template post<VEC>(v[k], mean, rstd, post[k], a, o.f);
                 o.store_stream(a.out + base + vi * VEC);
             }
         }
@@ -95,6 +111,13 @@ __global__ void __launch_bounds__(kCtaMaxThreads)
 rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, unsigned *err) {
     using T = typename C::T;
     constexpr int NIN = C::kInputs;
+    // The epilogue's per-column values are loaded with the row (before the
+    // reduction barriers) only when that costs at most 8 registers: the
+    // streaming shapes gain more from registers (CTAs per SM) than from the
+    // earlier loads, which hit L1 anyway.
+    constexpr bool kEarlyPost = VPT * VEC * C::kPostPC <= 8;
+    using PrePC = typename C::template PrePC<VEC>;
+    using PostPC = typename C::template PostPC<VEC>;
     extern __shared__ __align__(1024) unsigned char smem[];
     float *red = reinterpret_cast<float *>(smem);                  // [2][32]
     volatile int *abort_flag = reinterpret_cast<int *>(smem + 256); // [2]
@@ -137,33 +160,47 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
     }
 
     int rb = 0;
+    int s = 0;              // ring slot of row li (li mod nstage)
+    uint32_t parity = 0;    // barrier phase parity of row li ((li / nstage) & 1)
     int64_t li = 0;
     for (; li < nlocal; ++li) {
         const int64_t row = first + li * G;
         const int64_t base = row * cols;
-        const int s = STAGED ? (int)(li % nstage) : 0;
         const T *stage = reinterpret_cast<const T *>(ring + (size_t)s * stage_bytes);
+
+        // Per-column values first (they do not depend on the ring), then the
+        // row: all loads before any use.  Slots past the row end re-read the
+        // last vector and are masked.
+        PrePC pre[VPT];
+        PostPC post[kEarlyPost ? VPT : 1];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
+            C::template load_pre<VEC>(a, vc * VEC, pre[k]);
+            if constexpr (kEarlyPost) C::template load_post<VEC>(a, vc * VEC, post[k]);
+        }
         if constexpr (STAGED) {
-            const uint32_t parity = (uint32_t)((li / nstage) & 1);
             if (!mbar_wait_bounded(smem_addr(&bars[s]), parity)) abort_flag[li & 1] = 1;
         }
-
+        Frag<T, VEC> in[VPT][NIN];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) {
+                if constexpr (STAGED) in[k][i].load_shared(stage + (size_t)i * cols + vc * VEC);
+                else in[k][i].load_stream(a.in[i] + base + vc * VEC);
+            }
+        }
         float v[VPT][VEC];
         float lsum = 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int vi = tid + k * blockDim.x;
-            if (vi < nvec) {
-                Frag<T, VEC> in[NIN];
+            C::template pre<VEC>(in[k], pre[k], a, v[k]);
+            float part = 0.0f;
 #pragma unroll
-                for (int i = 0; i < NIN; ++i) {
-                    if constexpr (STAGED) in[i].load_shared(stage + (size_t)i * cols + vi * VEC);
-                    else in[i].load_stream(a.in[i] + base + vi * VEC);
-                }
-                C::template pre<VEC>(in, a, vi * VEC, v[k]);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) lsum += v[k][e];
-            }
+            for (int e = 0; e < VEC; ++e) part += v[k][e];
+            lsum += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
         }
         // Barrier inside: after it every thread has its row slice in registers.
         const float sum = block_sum(lsum, red + 32 * rb);
@@ -178,13 +215,13 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             float lm2 = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                if (tid + k * (int)blockDim.x < nvec) {
+                float part = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float d = v[k][e] - mean;
-                        lm2 = fmaf(d, d, lm2);
-                    }
+                for (int e = 0; e < VEC; ++e) {
+                    const float d = v[k][e] - mean;
+                    part = fmaf(d, d, part);
                 }
+                lm2 += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
             }
             rstd = C::rstd(block_sum(lm2, red + 32 * rb), cols, a);
             rb ^= 1;
@@ -194,9 +231,19 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             const int vi = tid + k * blockDim.x;
             if (vi < nvec) {
                 Frag<T, VEC> o;
-                C::template post<VEC>(v[k], mean, rstd, a, vi * VEC, o.f);
+                if constexpr (kEarlyPost) {
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, o.f);
+                } else {
+                    PostPC pc;
+                    C::template load_post<VEC>(a, vi * VEC, pc);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, o.f);
+                }
                 o.store_stream(a.out + base + vi * VEC);
             }
+        }
+        if (++s == nstage) {
+            s = 0;
+            parity ^= 1u;
         }
     }
     if constexpr (STAGED) {
@@ -204,8 +251,15 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
         // CTA's copies still in flight before its shared memory goes away.
         if (li < nlocal && tid == 0) {
             atomicOr(err, kDevErrWaitTimeout);
-            for (int64_t lj = li; lj < nlocal && lj < li + nstage; ++lj)
-                (void)mbar_wait_bounded(smem_addr(&bars[lj % nstage]), (uint32_t)((lj / nstage) & 1));
+            int ss = s;
+            uint32_t pp = parity;
+            for (int64_t lj = li; lj < nlocal && lj < li + nstage; ++lj) {
+                (void)mbar_wait_bounded(smem_addr(&bars[ss]), pp);
+                if (++ss == nstage) {
+                    ss = 0;
+                    pp ^= 1u;
+                }
+            }
         }
     }
 }
@@ -228,7 +282,6 @@ template <class C> struct RowEngine {
     using T = typename C::T;
     static constexpr int kVecN = Elem<T>::kVec;
 
-    // Kernel table.  Index: vectors per thread slot as a power of two.
     static const void *warp_fn(int vpl, bool vec) {
         if (vec) {
             switch (vpl) {
@@ -281,18 +334,29 @@ template <class C> struct RowEngine {
         return nullptr;
     }
 
+    // CTAs of `fn` resident per SM with `threads` threads and `smem` bytes.
+    static mb_status occupancy(const LaunchCtx &ctx, const void *fn, int threads, int smem,
+                               int *occ) {
+        cudaError_t e = allow_smem(fn, ctx, smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, fn, threads, smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return MB_OK;
+    }
+
     static mb_status plan(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows, int cols,
                           bool aligned, RowPlan *p, const void **fn) {
         const bool vec = aligned && (cols % kVecN) == 0;
         const int VEC = vec ? kVecN : 1;
         const int nvec = cols / VEC;
         const bool warp_ok = nvec <= 32 * 8;
-        const int64_t stage_bytes = (int64_t)C::kInputs * cols * (int64_t)sizeof(T);
+        const int stage_bytes = C::kInputs * cols * (int)sizeof(T);
+        const bool stage_fits = kHdrBytes + stage_bytes <= ctx.smem_optin;
 
         int path = tun.path;
         if (path == MB_ROW_WARP && !warp_ok) path = MB_ROW_AUTO;
-        if (path == MB_ROW_STAGED && !vec) path = MB_ROW_AUTO;
-        if (path == MB_ROW_AUTO) path = warp_ok ? MB_ROW_WARP : (vec ? MB_ROW_STAGED : MB_ROW_DIRECT);
+        if (path == MB_ROW_STAGED && (!vec || !stage_fits)) path = MB_ROW_AUTO;
+        if (path == MB_ROW_AUTO)
+            path = warp_ok ? MB_ROW_WARP : (vec && stage_fits ? MB_ROW_STAGED : MB_ROW_DIRECT);
 
         p->vec = VEC;
         if (path == MB_ROW_WARP) {
@@ -300,8 +364,8 @@ template <class C> struct RowEngine {
             while (vpl * 32 < nvec) vpl *= 2;
             *fn = warp_fn(vpl, vec);
             int occ = 0;
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, *fn, kWarpBlock, 0);
-            if (e != cudaSuccess) return cuda_fail(e);
+            mb_status st = occupancy(ctx, *fn, kWarpBlock, 0, &occ);
+            if (st != MB_OK) return st;
             if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
             if (occ < 1) occ = 1;
             const int64_t want = (rows + kWarpBlock / 32 - 1) / (kWarpBlock / 32);
@@ -311,43 +375,62 @@ template <class C> struct RowEngine {
             return MB_OK;
         }
 
-        // CTA engine: smallest VPT giving <= 512 threads, else <= 1024.
-        int vpt = 0;
-        for (int cand = 1; cand <= max_vpt(vec); cand *= 2)
-            if (ceil_div(nvec, cand) <= 512) { vpt = cand; break; }
-        if (!vpt)
-            for (int cand = 1; cand <= max_vpt(vec); cand *= 2)
-                if (ceil_div(nvec, cand) <= kCtaMaxThreads) { vpt = cand; break; }
-        if (!vpt) return MB_ERR_SHAPE;
-        const int threads = round_up32(ceil_div(nvec, vpt));
-
-        int stages = 0, smem = kHdrBytes;
-        int target = tun.ctas_per_sm > 0 ? tun.ctas_per_sm : (threads <= 512 ? 2 : 1);
-        if (path == MB_ROW_STAGED) {
-            for (; target >= 1; --target) {
-                const int per_cta = ctx.smem_per_sm / target - 1024;   // 1 KB reserved per CTA
-                const int budget = (per_cta < ctx.smem_optin ? per_cta : ctx.smem_optin) - kHdrBytes;
-                int64_t n = budget / stage_bytes;
-                if (n > kMaxStages) n = kMaxStages;
-                if (tun.stages > 0 && tun.stages < n) n = tun.stages;
-                if (n >= 2 || (tun.stages == 1 && n >= 1)) { stages = (int)n; break; }
+        // CTA engine.  Each resident CTA keeps one row in flight, so pick the
+        // vectors-per-thread that lets the most CTAs share an SM, counting up
+        // to kRowsInFlight (measured on GB300: four rows per SM keep HBM busy),
+        // then the most threads per SM; one ring stage counted for the staged
+        // path.
+        const bool staged = path == MB_ROW_STAGED;
+        const int smem1 = kHdrBytes + (staged ? stage_bytes : 0);
+        int best_vpt = 0, best_occ = 0, best_threads = 0;
+        for (int cand = 1; cand <= max_vpt(vec); cand *= 2) {
+            if (tun.vpt > 0 && cand != tun.vpt) continue;
+            if (ceil_div(nvec, cand) > kCtaMaxThreads) continue;
+            const int threads = round_up32(ceil_div(nvec, cand));
+            const void *f = cta_fn(cand, vec, staged);
+            if (!f) continue;
+            int occ = 0;
+            mb_status st = occupancy(ctx, f, threads, smem1, &occ);
+            if (st != MB_OK) return st;
+            if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
+            if (occ < 1) continue;
+            const int rows_in_flight = occ < kRowsInFlight ? occ : kRowsInFlight;
+            const int best_rows = best_occ < kRowsInFlight ? best_occ : kRowsInFlight;
+            if (rows_in_flight > best_rows ||
+                (rows_in_flight == best_rows && occ * threads > best_occ * best_threads)) {
+                best_vpt = cand; best_occ = occ; best_threads = threads;
             }
-            if (!stages) path = MB_ROW_DIRECT;
-            else smem = kHdrBytes + (int)(stages * stage_bytes);
         }
-        *fn = cta_fn(vpt, vec, path == MB_ROW_STAGED);
-        if (!*fn) return MB_ERR_SHAPE;
-        cudaError_t e = allow_smem(*fn, ctx, smem);
-        if (e != cudaSuccess) return cuda_fail(e);
-        int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, *fn, threads, smem);
-        if (e != cudaSuccess) return cuda_fail(e);
+        if (!best_vpt && tun.vpt > 0) {
+            RowTuning t2 = tun;
+            t2.vpt = 0;
+            return plan(ctx, t2, rows, cols, aligned, p, fn);
+        }
+        if (!best_vpt) return MB_ERR_SHAPE;
+
+        int stages = 0, smem = kHdrBytes, occ = best_occ;
+        if (staged) {
+            // One stage per CTA when several CTAs share an SM (their rows
+            // overlap one another); two when a CTA is alone.  A requested
+            // depth is honoured as far as shared memory allows.
+            int want = tun.stages > 0 ? tun.stages : (best_occ >= 2 ? 1 : 2);
+            if (want > kMaxStages) want = kMaxStages;
+            while (want > 1 && (int64_t)occ * (kHdrBytes + 1024 + (int64_t)want * stage_bytes) >
+                                   ctx.smem_per_sm)
+                --want;
+            while (want > 1 && kHdrBytes + (int64_t)want * stage_bytes > ctx.smem_optin) --want;
+            stages = want;
+            smem = kHdrBytes + stages * stage_bytes;
+        }
+        *fn = cta_fn(best_vpt, vec, staged);
+        int occ2 = 0;
+        mb_status st = occupancy(ctx, *fn, best_threads, smem, &occ2);
+        if (st != MB_OK) return st;
+        if (occ2 < occ) occ = occ2;
         if (occ < 1) occ = 1;
-        if (path == MB_ROW_STAGED && occ > target) occ = target;
-        if (path == MB_ROW_DIRECT && tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ)
-            occ = tun.ctas_per_sm;
         const int64_t cap = (int64_t)occ * ctx.sm_count;
-        p->path = path; p->threads = threads; p->vpt = vpt; p->stages = stages; p->smem = smem;
+        p->path = path; p->threads = best_threads; p->vpt = best_vpt; p->stages = stages;
+        p->smem = smem;
         p->ctas = (int)(rows < cap ? rows : cap);
         return MB_OK;
     }

@@ -97,10 +97,11 @@ def test_inductor_argument_checks(lib):
 
 
 def test_row_path_setter_validates(lib):
-    assert lib.mb_set_row_path(9, 0, 0) == MB_ERR_VALUE
-    assert lib.mb_set_row_path(0, -1, 0) == MB_ERR_VALUE
-    assert lib.mb_set_row_path(3, 2, 4) == MB_OK
-    assert lib.mb_set_row_path(0, 0, 0) == MB_OK
+    assert lib.mb_set_row_path(9, 0, 0, 0) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(0, -1, 0, 0) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(0, 0, 0, -2) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(3, 2, 4, 1) == MB_OK
+    assert lib.mb_set_row_path(0, 0, 0, 0) == MB_OK
 
 
 def test_null_out_pointers(lib):

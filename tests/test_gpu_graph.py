@@ -1,0 +1,108 @@
+"""The fused chains inside a captured CUDA graph.
+
+The library neither allocates nor synchronises, so its calls can be captured
+once and replayed (the way the pages remove per-launch overhead for small,
+launch-bound calls: capture a sequence of kernels, then launch the graph).
+Each test captures the calls, replays the graph on two different input sets
+copied into the captured buffers, and checks every replay against the CPU
+oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_gb300 as mb
+import oracle
+from synth import workloads as W
+
+from gpu_util import assert_bitexact, assert_close, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    from memory_bound_gb300 import build as lib_build
+    lib_build.build()
+    torch.cuda.set_device(0)
+    mb.set_row_path("auto")
+    yield
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+
+
+def _capture(fn):
+    fn()                                   # first call outside: plans and attributes
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    return g
+
+
+def _inputs(w, seed):
+    """The workload's tensors drawn with another seed (same distributions)."""
+    import dataclasses
+    return dataclasses.replace(w, seed=seed).generate_all(
+        rows=min(w.rows, 256) if w.chain != "add_relu_scale" else None)
+
+
+@pytest.mark.parametrize("w", [W.POINTWISE_TINY, W.POINTWISE_4M], ids=lambda w: w.name)
+def test_graph_pointwise(w):
+    t0 = w.generate_all()
+    dev = {k: to_dev(v) for k, v in t0.items()}
+    out = torch.empty_like(dev["x"])
+    g = _capture(lambda: mb.fused_add_relu_scale(dev["x"], dev["b1"], dev["b2"], 0.5, out=out))
+    for seed in (100, 101):
+        t = _inputs(w, seed)
+        for k in dev:
+            dev[k].copy_(to_dev(t[k]))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bitexact(to_host(out), oracle.add_relu_scale(t["x"], t["b1"], t["b2"], 0.5),
+                        f"replay seed {seed}")
+
+
+def test_graph_inductor_sequence():
+    """Ten captured calls on ten buffer sets, replayed twice."""
+    w = W.INDUCTOR_1024
+    sets = []
+    for k in range(10):
+        t = _inputs(w, 200 + k)
+        sets.append(({n: to_dev(v) for n, v in t.items()}, torch.empty((256, 1024), device="cuda")))
+
+    def calls():
+        for d, y in sets:
+            mb.fused_bias_relu_branch_mean_epilogue(d["x"], d["bias"], d["gamma"], d["beta"],
+                                                    1.1, 0.1, out=y)
+
+    g = _capture(calls)
+    for rep in range(2):
+        for d, _ in sets:
+            d["x"].mul_(-1.0 if rep else 1.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for d, y in sets:
+            h = {n: to_host(v) for n, v in d.items()}
+            want = oracle.bias_relu_branch_mean_epilogue(h["x"], h["bias"], h["gamma"], h["beta"])
+            assert_close(to_host(y), want, what=f"replay {rep}")
+
+
+@pytest.mark.parametrize("w", [W.LN_F32, W.LN_BF16], ids=lambda w: w.name)
+def test_graph_layernorm(w):
+    bf16 = w.dtype == "bf16"
+    t0 = _inputs(w, 300)
+    dev = {k: to_dev(v, bf16) for k, v in t0.items()}
+    out = torch.empty_like(dev["x"])
+    g = _capture(lambda: mb.fused_residual_layernorm_gelu(dev["x"], dev["r"], dev["w"], dev["b"],
+                                                          1e-5, out=out))
+    for seed in (301, 302):
+        t = _inputs(w, seed)
+        for k in dev:
+            dev[k].copy_(to_dev(t[k], bf16))
+        g.replay()
+        torch.cuda.synchronize()
+        want = oracle.residual_layernorm_gelu(t["x"], t["r"], t["w"], t["b"], 1e-5)
+        assert_close(to_host(out), want, bf16=bf16, what=f"replay seed {seed}")
+    assert np.all(np.isfinite(to_host(out).astype(np.float32) if not bf16 else 1.0))

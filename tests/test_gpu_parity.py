@@ -185,8 +185,9 @@ def test_inductor_shapes_and_paths(shape, path, row_path):
 
 
 def test_inductor_degenerate_rows():
-    """Rows whose t is never positive give y = beta exactly; a constant row
-    (bias 0) gives s constant, m = s and y = beta exactly."""
+    """Rows whose t is never positive give s = 0, m = 0 and y = beta exactly.
+    A constant row (bias 0) gives s constant; its fp32 tree-sum mean equals s
+    only to rounding (3s is not exact in fp32), so y = beta to tolerance."""
     cols = 1024
     x = np.stack([-np.abs(rng_f32(1, (cols,))) - 0.5, np.full(cols, 0.75, np.float32)])
     bias = np.zeros(cols, np.float32)
@@ -195,7 +196,9 @@ def test_inductor_degenerate_rows():
     y = to_host(mb.fused_bias_relu_branch_mean_epilogue(
         to_dev(x), to_dev(bias), to_dev(gamma), to_dev(beta), 1.1, 0.1))
     assert_bitexact(y[0], beta, "all-negative row")
-    assert_bitexact(y[1], beta, "constant row")
+    want = oracle.bias_relu_branch_mean_epilogue(x, bias, gamma, beta)
+    assert_bitexact(want[1], beta, "oracle constant row")
+    assert_close(y[1], want[1], what="constant row")
 
 
 def test_inductor_offset_pointers():
@@ -269,12 +272,15 @@ def test_ln_shapes_and_paths(shape, path, bf16, row_path):
     check_guard(buf)
 
 
-@pytest.mark.parametrize("ctas,stages", [(1, 1), (1, 2), (2, 2), (1, 5), (2, 3), (1, 0), (3, 0)])
+@pytest.mark.parametrize("ctas,stages,vpt", [(1, 1, 0), (1, 2, 0), (2, 2, 0), (1, 5, 0),
+                                             (2, 3, 0), (1, 0, 0), (3, 0, 0), (4, 1, 0),
+                                             (0, 0, 1), (0, 0, 2), (0, 0, 4), (2, 2, 4)])
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
-def test_ln_staged_ring_shapes(ctas, stages, bf16, row_path):
-    """The staged ring at several depths and CTAs per SM (row counts that are
-    not multiples of the grid, so CTAs end at different ring phases)."""
-    row_path("staged", ctas, stages)
+def test_ln_staged_ring_shapes(ctas, stages, vpt, bf16, row_path):
+    """The staged ring at several depths, CTAs per SM and vectors per thread
+    (row counts that are not multiples of the grid, so CTAs end at different
+    ring phases)."""
+    row_path("staged", ctas, stages, vpt)
     rows, hidden = 1111, 4096 if not bf16 else 8192
     x, r, w, b = _ln_inputs(rows, hidden, 7 + ctas * 10 + stages, bf16)
     out = _run_ln(x, r, w, b, bf16)
@@ -322,7 +328,7 @@ def test_ln_empty_rows():
 
 def test_row_plan_reports_paths():
     p = mb.row_plan("ln", "bf16", 32768, 8192)
-    assert p["path"] == "staged" and p["stages"] >= 2 and p["vec"] == 8
+    assert p["path"] == "staged" and p["stages"] >= 1 and p["vec"] == 8
     p = mb.row_plan("ln", "f32", 8192, 4096)
     assert p["path"] == "staged" and p["vec"] == 4
     p = mb.row_plan("inductor", "f32", 1024, 1024)
