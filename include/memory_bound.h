@@ -194,6 +194,14 @@ mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
                           int vec_per_thread);
 
 /*
+ * Process-wide override of the pointwise chain's launch shape, for tuning and
+ * testing: blocks_per_sm (0 = as many as fit) and unroll, the 16-byte
+ * fragments per input each thread keeps in flight (1, 2, 4 or 8; 0 = the
+ * default 4).  Returns MB_ERR_VALUE on a negative count or another unroll.
+ */
+mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
+
+/*
  * The launch the row chains would use for a shape, without launching:
  * out[0] = path (mb_row_path), out[1] = threads per CTA, out[2] = CTAs,
  * out[3] = values per thread slot (vectors per thread), out[4] = vector width

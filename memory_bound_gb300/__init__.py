@@ -18,5 +18,5 @@ from ._binding import (  # noqa: F401
     MB_BF16, MB_F32, MB_MAX_COLS, MBError, ROW_PATHS, device_error,
     fused_add_relu_scale, fused_bias_relu_branch_mean_epilogue,
     fused_residual_layernorm_gelu, library_path, load_library, raw, row_plan,
-    set_row_path, status_string,
+    set_pointwise_shape, set_row_path, status_string,
 )

@@ -26,6 +26,7 @@ SIGNATURES = {
     "mb_last_cuda_error": (_I, []),
     "mb_device_error": (_I, [_U32P]),
     "mb_set_row_path": (_I, [_I, _I, _I, _I]),
+    "mb_set_pointwise_shape": (_I, [_I, _I]),
     "mb_row_plan": (_I, [_I, _I, _I64, _I64, _I, _I32P]),
 }
 
@@ -202,6 +203,12 @@ def set_row_path(path="auto", ctas_per_sm=0, stages=0, vec_per_thread=0):
     code = ROW_PATHS[path] if isinstance(path, str) else int(path)
     _check("mb_set_row_path", load_library().mb_set_row_path(code, ctas_per_sm, stages,
                                                              vec_per_thread))
+
+
+def set_pointwise_shape(blocks_per_sm=0, unroll=0):
+    """Process-wide override of the pointwise launch shape (0 = automatic)."""
+    _check("mb_set_pointwise_shape",
+           load_library().mb_set_pointwise_shape(blocks_per_sm, unroll))
 
 
 def row_plan(chain, dtype, rows, cols, aligned=True):

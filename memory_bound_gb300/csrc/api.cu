@@ -30,6 +30,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 RowTuning g_tuning{MB_ROW_AUTO, 0, 0, 0};
+PointwiseTuning g_pw_tuning{0, 0};
 thread_local int g_last_cuda_error = 0;
 
 mb_status device_ctx(cudaStream_t stream, LaunchCtx *ctx) {
@@ -114,7 +115,7 @@ mb_status fused_add_relu_scale(const void *x, const void *b1, const void *b2, vo
     LaunchCtx ctx;
     mb_status st = device_ctx(stream, &ctx);
     if (st != MB_OK) return st;
-    return add_relu_scale_run(ctx, dtype, x, b1, b2, y, n, scale, vec, (int)head);
+    return add_relu_scale_run(ctx, g_pw_tuning, dtype, x, b1, b2, y, n, scale, vec, (int)head);
 }
 
 mb_status fused_residual_layernorm_gelu(const void *x, const void *r, const void *w,
@@ -215,6 +216,15 @@ mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
         return MB_ERR_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);
     g_tuning = RowTuning{(int)path, ctas_per_sm, stages, vec_per_thread};
+    return MB_OK;
+}
+
+mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll) {
+    if (blocks_per_sm < 0 || !(unroll == 0 || unroll == 1 || unroll == 2 || unroll == 4 ||
+                               unroll == 8))
+        return MB_ERR_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_pw_tuning = PointwiseTuning{blocks_per_sm, unroll};
     return MB_OK;
 }
 

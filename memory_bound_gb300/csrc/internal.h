@@ -27,6 +27,12 @@ struct RowTuning {
     int vpt;               // vector slots per thread, 0 = automatic
 };
 
+// Process-wide pointwise override (mb_set_pointwise_shape).
+struct PointwiseTuning {
+    int blocks_per_sm;     // 0 = as many as fit
+    int unroll;            // 16-byte fragments per input in flight per thread; 0 = 4
+};
+
 // The launch a row chain uses (mb_row_plan reports it).
 struct RowPlan {
     int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
@@ -34,9 +40,9 @@ struct RowPlan {
 
 // Chains implemented in their own translation units.  `launch == false`
 // only fills `plan`.
-mb_status add_relu_scale_run(const LaunchCtx &ctx, mb_dtype dtype, const void *x,
-                             const void *b1, const void *b2, void *y, int64_t n,
-                             float scale, bool aligned16, int head);
+mb_status add_relu_scale_run(const LaunchCtx &ctx, const PointwiseTuning &tun, mb_dtype dtype,
+                             const void *x, const void *b1, const void *b2, void *y, int64_t n,
+                             float scale, bool vec, int head);
 
 mb_status ln_gelu_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                            const void *r, const void *w, const void *b, void *out,

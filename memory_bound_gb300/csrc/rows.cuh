@@ -368,9 +368,15 @@ template <class C> struct RowEngine {
             if (st != MB_OK) return st;
             if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
             if (occ < 1) occ = 1;
-            const int64_t want = (rows + kWarpBlock / 32 - 1) / (kWarpBlock / 32);
+            // Few rows: smaller blocks, so the rows spread over every SM
+            // (at least two blocks per SM when the rows allow it).
+            int threads = kWarpBlock;
+            while (threads > 32 && (rows + threads / 32 - 1) / (threads / 32) < 2 * ctx.sm_count)
+                threads /= 2;
+            occ *= kWarpBlock / threads;
+            const int64_t want = (rows + threads / 32 - 1) / (threads / 32);
             const int64_t cap = (int64_t)occ * ctx.sm_count;
-            p->path = path; p->threads = kWarpBlock; p->vpt = vpl; p->stages = 0; p->smem = 0;
+            p->path = path; p->threads = threads; p->vpt = vpl; p->stages = 0; p->smem = 0;
             p->ctas = (int)(want < cap ? want : cap);
             return MB_OK;
         }

@@ -104,6 +104,13 @@ def test_row_path_setter_validates(lib):
     assert lib.mb_set_row_path(0, 0, 0, 0) == MB_OK
 
 
+def test_pointwise_shape_setter_validates(lib):
+    assert lib.mb_set_pointwise_shape(-1, 0) == MB_ERR_VALUE
+    assert lib.mb_set_pointwise_shape(0, 3) == MB_ERR_VALUE
+    assert lib.mb_set_pointwise_shape(2, 8) == MB_OK
+    assert lib.mb_set_pointwise_shape(0, 0) == MB_OK
+
+
 def test_null_out_pointers(lib):
     assert lib.mb_device_error(None) == MB_ERR_NULL
     assert lib.mb_row_plan(0, 0, 8, 64, 1, None) == MB_ERR_NULL

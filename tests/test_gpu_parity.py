@@ -110,6 +110,22 @@ def test_pointwise_unaligned(offsets, bf16):
     assert not bool(ybig[:offsets[3]].any()) and not bool(ybig[offsets[3] + n:].any())
 
 
+@pytest.mark.parametrize("blocks,unroll", [(1, 1), (2, 2), (0, 8), (3, 4), (0, 1)])
+@pytest.mark.parametrize("n", [1 << 20, 4 * 1024 * 1024 + 5, 777777])
+def test_pointwise_launch_shapes(blocks, unroll, n):
+    """Other launch shapes: several fragments per thread and per block, and
+    ragged block shares."""
+    x, b1, b2 = (rng_f32(n + k, (n,)) for k in range(3))
+    mb.set_pointwise_shape(blocks, unroll)
+    try:
+        buf, y = guarded_empty((n,), torch.float32)
+        mb.fused_add_relu_scale(to_dev(x), to_dev(b1), to_dev(b2), 0.5, out=y)
+        assert_bitexact(to_host(y), oracle.add_relu_scale(x, b1, b2, 0.5), f"{blocks},{unroll}")
+        check_guard(buf)
+    finally:
+        mb.set_pointwise_shape(0, 0)
+
+
 @pytest.mark.parametrize("scale", [0.3, 1.0, -2.0, 0.0, 1e-30, 3.0])
 def test_pointwise_scales(scale):
     n = 65537
