@@ -15,6 +15,7 @@ template <typename TT> struct LnGeluChain {
     using T = TT;
     static constexpr int kInputs = 2;     // x, r
     static constexpr bool kTwoPass = true;
+    static constexpr bool kMaxFirst = false;
     struct Args {
         const T *in[2];
         const T *w;
@@ -39,7 +40,15 @@ template <typename TT> struct LnGeluChain {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) v[e] = __fadd_rn(in[0].f[e], in[1].f[e]);
     }
-    __device__ __forceinline__ static float rstd(float m2, int cols, const Args &a) {
+    // mean = sum(v) / H; second pass sum((v - mean)^2); rstd = 1/sqrt(var + eps)
+    __device__ __forceinline__ static float stat1(float sum, int cols, const Args &) {
+        return sum / (float)cols;
+    }
+    __device__ __forceinline__ static float p2(float &v, float mean, float acc) {
+        const float d = v - mean;
+        return fmaf(d, d, acc);
+    }
+    __device__ __forceinline__ static float stat2(float m2, int cols, const Args &a) {
         return rsqrtf(m2 / (float)cols + a.eps);
     }
     template <int VEC>
@@ -65,6 +74,7 @@ struct InductorChain {
     using T = float;
     static constexpr int kInputs = 1;     // x
     static constexpr bool kTwoPass = false;
+    static constexpr bool kMaxFirst = false;
     struct Args {
         const float *in[1];
         const float *bias;
@@ -100,7 +110,12 @@ struct InductorChain {
             v[e] = __fadd_rn(p, q);
         }
     }
-    __device__ __forceinline__ static float rstd(float, int, const Args &) { return 0.0f; }
+    // m = sum(s) / cols (a row sum divided by the row length); no second pass
+    __device__ __forceinline__ static float stat1(float sum, int cols, const Args &) {
+        return sum / (float)cols;
+    }
+    __device__ __forceinline__ static float p2(float &, float, float acc) { return acc; }
+    __device__ __forceinline__ static float stat2(float, int, const Args &) { return 0.0f; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
                                                 const PostPC<VEC> &pc, const Args &,

@@ -142,6 +142,21 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+// Maximum over the CTA; same buffer discipline as block_sum below.
+__device__ __forceinline__ float block_max(float v, float *red) {
+    v = warp_max(v);
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return warp_max(lane < (int)(blockDim.x >> 5) ? red[lane] : -INFINITY);
+}
+
 // Sum over the CTA.  `red` holds 32 floats of shared memory; callers alternate
 // between two such buffers so that one reduction's reads cannot race with the
 // next one's writes.  After the barrier every warp runs the same butterfly

@@ -3,9 +3,10 @@
 // A chain C supplies, per row of `cols` elements:
 //   pre   (per element)   the pointwise prologue, giving v from the row inputs
 //                         and the per-column values it needs (PrePC)
-//   mean  = sum(v) / cols (always), and with C::kTwoPass
-//   rstd  = C::rstd(sum((v - mean)^2), cols, args)   (second pass over v)
-//   post  (per element)   the epilogue from v, mean, rstd and its per-column
+//   s1    = C::stat1(R1, cols, args), R1 = sum(v), or max(v) with C::kMaxFirst
+//   s2    = C::stat2(R2, cols, args) with C::kTwoPass, where R2 sums the terms
+//           C::p2 forms from each v and s1 (p2 may also rewrite v in place)
+//   post  (per element)   the epilogue from v, s1, s2 and its per-column
 //                         values (PostPC)
 // The row is read from device memory once and held in registers (v) between
 // the passes; the output is written once.
@@ -37,6 +38,23 @@ constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
 constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
 
+// Folds one slot's VEC values into the running first-pass partial (a sum, or a
+// maximum with C::kMaxFirst); slots past the row end leave it unchanged.
+template <class C, int VEC>
+__device__ __forceinline__ float fold1(float acc, const float (&v)[VEC], bool valid) {
+    if constexpr (C::kMaxFirst) {
+        float m = v[0];
+#pragma unroll
+        for (int e = 1; e < VEC; ++e) m = fmaxf(m, v[e]);
+        return valid ? fmaxf(acc, m) : acc;
+    } else {
+        float part = 0.0f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) part += v[e];
+        return acc + (valid ? part : 0.0f);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // one warp per row
 // ---------------------------------------------------------------------------
@@ -66,30 +84,24 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             C::template load_post<VEC>(a, vc * VEC, post[k]);
         }
         float v[VPL][VEC];
-        float lsum = 0.0f;
+        float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             C::template pre<VEC>(in[k], pre[k], a, v[k]);
-            float part = 0.0f;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) part += v[k][e];
-            lsum += lane + 32 * k < nvec ? part : 0.0f;
+            l1 = fold1<C, VEC>(l1, v[k], lane + 32 * k < nvec);
         }
-        const float mean = warp_sum(lsum) / (float)cols;
+        const float mean = C::stat1(C::kMaxFirst ? warp_max(l1) : warp_sum(l1), cols, a);
         float rstd = 0.0f;
         if constexpr (C::kTwoPass) {
-            float lm2 = 0.0f;
+            float l2 = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
                 float part = 0.0f;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float d = v[k][e] - mean;
-                    part = fmaf(d, d, part);
-                }
-                lm2 += lane + 32 * k < nvec ? part : 0.0f;
+                for (int e = 0; e < VEC; ++e) part = C::p2(v[k][e], mean, part);
+                l2 += lane + 32 * k < nvec ? part : 0.0f;
             }
-            rstd = C::rstd(warp_sum(lm2), cols, a);
+            rstd = C::stat2(warp_sum(l2), cols, a);
         }
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
@@ -193,37 +205,31 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             }
         }
         float v[VPT][VEC];
-        float lsum = 0.0f;
+        float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             C::template pre<VEC>(in[k], pre[k], a, v[k]);
-            float part = 0.0f;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) part += v[k][e];
-            lsum += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
+            l1 = fold1<C, VEC>(l1, v[k], tid + k * (int)blockDim.x < nvec);
         }
         // Barrier inside: after it every thread has its row slice in registers.
-        const float sum = block_sum(lsum, red + 32 * rb);
+        const float r1 = C::kMaxFirst ? block_max(l1, red + 32 * rb) : block_sum(l1, red + 32 * rb);
         rb ^= 1;
         if constexpr (STAGED) {
             if (abort_flag[li & 1]) break;
             if (tid == 0 && li + nstage < nlocal) issue(s, li + nstage);
         }
-        const float mean = sum / (float)cols;
+        const float mean = C::stat1(r1, cols, a);
         float rstd = 0.0f;
         if constexpr (C::kTwoPass) {
-            float lm2 = 0.0f;
+            float l2 = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 float part = 0.0f;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float d = v[k][e] - mean;
-                    part = fmaf(d, d, part);
-                }
-                lm2 += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
+                for (int e = 0; e < VEC; ++e) part = C::p2(v[k][e], mean, part);
+                l2 += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
             }
-            rstd = C::rstd(block_sum(lm2, red + 32 * rb), cols, a);
+            rstd = C::stat2(block_sum(l2, red + 32 * rb), cols, a);
             rb ^= 1;
         }
 #pragma unroll

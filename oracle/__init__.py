@@ -76,6 +76,19 @@ def load(path=None):
     lib.oracle_residual_layernorm_gelu_bf16.argtypes = [
         U16P, U16P, U16P, U16P, U16P, i64, i64, f32, F64P, F64P, F64P]
     lib.oracle_residual_layernorm_gelu_bf16.restype = None
+    lib.oracle_bias_relu_branch_mean_epilogue_bf16.argtypes = [
+        U16P, U16P, U16P, U16P, U16P, i64, i64, f32, f32]
+    lib.oracle_bias_relu_branch_mean_epilogue_bf16.restype = None
+    lib.oracle_layernorm_act_f32.argtypes = [
+        F32P, F32P, F32P, F32P, F32P, F32P, i64, i64, f32, ctypes.c_int]
+    lib.oracle_layernorm_act_f32.restype = None
+    lib.oracle_layernorm_act_bf16.argtypes = [
+        U16P, U16P, U16P, U16P, U16P, U16P, i64, i64, f32, ctypes.c_int]
+    lib.oracle_layernorm_act_bf16.restype = None
+    lib.oracle_row_softmax_f32.argtypes = [F32P, F32P, i64, i64]
+    lib.oracle_row_softmax_f32.restype = None
+    lib.oracle_row_softmax_bf16.argtypes = [U16P, U16P, i64, i64]
+    lib.oracle_row_softmax_bf16.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -161,6 +174,23 @@ def bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
     return y
 
 
+def bias_relu_branch_mean_epilogue_bf16(x, bias, gamma, beta, x_scale=1.1,
+                                        branch_scale=0.1, lib=None):
+    """o2 with bf16 I/O (uint16 bit patterns): widen, fp32 steps, round y once."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    rows, cols = x.shape
+    bias, gamma, beta = (_c(a, np.uint16) for a in (bias, gamma, beta))
+    for v in (bias, gamma, beta):
+        if v.shape != (cols,):
+            raise ValueError("per-column vectors must have length cols")
+    y = np.empty_like(x)
+    lib.oracle_bias_relu_branch_mean_epilogue_bf16(
+        _u16p(x), _u16p(bias), _u16p(gamma), _u16p(beta), _u16p(y), rows, cols,
+        x_scale, branch_scale)
+    return y
+
+
 # --------------------------------------------------------------------------
 # o3: residual + LayerNorm + affine + GeLU-tanh   ([P2] §2.3, [P3] §4.3)
 # --------------------------------------------------------------------------
@@ -192,3 +222,56 @@ def residual_layernorm_gelu(x, r, w, b, eps=1e-5, intermediates=False, lib=None)
     if intermediates:
         return out, mean, rstd, xhat
     return out
+
+
+# --------------------------------------------------------------------------
+# o4: LayerNorm family   ([P3] §4.3, [P2] §2.1-2.3)
+# --------------------------------------------------------------------------
+
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+
+
+def layernorm_act(x, r, w, b, eps=1e-5, act=ACT_GELU, want_h=False, lib=None):
+    """out = act(LayerNorm(x (+ r)) * w + b); r may be None.  With ``want_h``
+    also returns h = x + r (or x) rounded to the I/O type."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    rows, hidden = x.shape
+    dt = x.dtype
+    if dt == np.float32:
+        cv, fn, p, nullp = np.float32, lib.oracle_layernorm_act_f32, _f32p, ctypes.POINTER(ctypes.c_float)()
+    elif dt == np.uint16:
+        cv, fn, p, nullp = np.uint16, lib.oracle_layernorm_act_bf16, _u16p, ctypes.POINTER(ctypes.c_uint16)()
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    w, b = _c(w, cv), _c(b, cv)
+    if r is not None:
+        r = _c(r, cv)
+        if r.shape != x.shape:
+            raise ValueError("shape mismatch")
+    if w.shape != (hidden,) or b.shape != (hidden,):
+        raise ValueError("shape mismatch")
+    out = np.empty_like(x)
+    h = np.empty_like(x) if want_h else None
+    fn(p(x), p(r) if r is not None else nullp, p(w), p(b), p(out),
+       p(h) if h is not None else nullp, rows, hidden, eps, int(act))
+    return (out, h) if want_h else out
+
+
+# --------------------------------------------------------------------------
+# o5: row softmax   ([P1] §4.1-4.2, [P2] §3.2)
+# --------------------------------------------------------------------------
+
+def row_softmax(x, lib=None):
+    """Softmax of each row (float32, or uint16 bf16 bit patterns)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    y = np.empty_like(x)
+    if x.dtype == np.float32:
+        lib.oracle_row_softmax_f32(_f32p(x), _f32p(y), rows, cols)
+    elif x.dtype == np.uint16:
+        lib.oracle_row_softmax_bf16(_u16p(x), _u16p(y), rows, cols)
+    else:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    return y

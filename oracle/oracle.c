@@ -21,6 +21,10 @@
  *       normalisation, affine step and GeLU are evaluated in double (the
  *       pages' rsqrtf / tanhf and one-pass E[v^2]-mean^2 are shortcuts of the
  *       fp32 sketch, not the definition), and the output is rounded once.
+ *   o4  The LayerNorm family follows o3 with the residual optional, the
+ *       residual sum optionally written out (rounded once to the I/O type) and
+ *       the activation chosen (none, relu, gelu-tanh).
+ *   o5  Row softmax in double, relative to the row maximum, rounded once.
  */
 #include "oracle.h"
 
@@ -250,4 +254,143 @@ void oracle_residual_layernorm_gelu_bf16(const uint16_t *x, const uint16_t *r,
 {
     o3_rows(x, r, w, b, load_bf16, out, 1, rows, hidden, eps, mean_out,
             rstd_out, xhat_out);
+}
+
+/* ------------------------------------------------------------------------ */
+/* o2 with bf16 I/O                                                         */
+/* ------------------------------------------------------------------------ */
+
+void oracle_bias_relu_branch_mean_epilogue_bf16(const uint16_t *x, const uint16_t *bias,
+                                                const uint16_t *gamma, const uint16_t *beta,
+                                                uint16_t *y, int64_t rows, int64_t cols,
+                                                float x_scale, float branch_scale)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const uint16_t *xr = x + i * cols;
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            sum += (double)o2_s(widen_bf16(xr[j]), widen_bf16(bias[j]), x_scale,
+                                branch_scale);
+        float m = (float)(sum / (double)cols);
+        for (int64_t j = 0; j < cols; ++j) {
+            float s = o2_s(widen_bf16(xr[j]), widen_bf16(bias[j]), x_scale, branch_scale);
+            float d = s - m;
+            d = d * widen_bf16(gamma[j]);
+            float o = d + widen_bf16(beta[j]);
+            y[i * cols + j] = oracle_bf16_from_double((double)o);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* o4: LayerNorm family                                                     */
+/* [P3] §4.3 (mean, var = sum((x - mean)^2)/cols, (x - mean)/sqrt(var + eps) */
+/* * gamma + beta); [P2] §2.1 (LayerNorm -> ReLU fused) and §2.2-2.3         */
+/* (residual + LayerNorm, then GeLU)                                         */
+/* ------------------------------------------------------------------------ */
+
+static double o4_act(double n, int act)
+{
+    if (act == 1)
+        return n > 0.0 ? n : 0.0;      /* relu, every value not > 0 to +0 */
+    if (act == 2)
+        return oracle_gelu_tanh(n);
+    return n;
+}
+
+static void o4_rows(const void *x, const void *r, const void *w, const void *b,
+                    o3_load_fn load, void *out, void *h_out, int bf16, int64_t rows,
+                    int64_t hidden, float eps, int act)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        int64_t base = i * hidden;
+        double sum = 0.0;
+        for (int64_t j = 0; j < hidden; ++j) {
+            float v = load(x, base + j);
+            if (r)
+                v = v + load(r, base + j);
+            sum += (double)v;
+        }
+        double mean = sum / (double)hidden;
+        double sq = 0.0;
+        for (int64_t j = 0; j < hidden; ++j) {
+            float v = load(x, base + j);
+            if (r)
+                v = v + load(r, base + j);
+            double d = (double)v - mean;
+            sq += d * d;
+        }
+        double rstd = 1.0 / sqrt(sq / (double)hidden + (double)eps);
+        for (int64_t j = 0; j < hidden; ++j) {
+            float v = load(x, base + j);
+            if (r)
+                v = v + load(r, base + j);
+            if (h_out) {
+                if (bf16)
+                    ((uint16_t *)h_out)[base + j] = oracle_bf16_from_double((double)v);
+                else
+                    ((float *)h_out)[base + j] = v;
+            }
+            double n = ((double)v - mean) * rstd * (double)load(w, j) + (double)load(b, j);
+            double g = o4_act(n, act);
+            if (bf16)
+                ((uint16_t *)out)[base + j] = oracle_bf16_from_double(g);
+            else
+                ((float *)out)[base + j] = (float)g;
+        }
+    }
+}
+
+void oracle_layernorm_act_f32(const float *x, const float *r, const float *w,
+                              const float *b, float *out, float *h_out, int64_t rows,
+                              int64_t hidden, float eps, int act)
+{
+    o4_rows(x, r, w, b, load_f32, out, h_out, 0, rows, hidden, eps, act);
+}
+
+void oracle_layernorm_act_bf16(const uint16_t *x, const uint16_t *r, const uint16_t *w,
+                               const uint16_t *b, uint16_t *out, uint16_t *h_out,
+                               int64_t rows, int64_t hidden, float eps, int act)
+{
+    o4_rows(x, r, w, b, load_bf16, out, h_out, 1, rows, hidden, eps, act);
+}
+
+/* ------------------------------------------------------------------------ */
+/* o5: row softmax                                                          */
+/* [P1] §4.1-4.2 and [P2] §3.2: softmax over each score row, normalised by  */
+/* the row maximum before exponentiation                                     */
+/* ------------------------------------------------------------------------ */
+
+static void o5_rows(const void *x, o3_load_fn load, void *y, int bf16, int64_t rows,
+                    int64_t cols)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        int64_t base = i * cols;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = (double)load(x, base + j);
+            if (v > m)
+                m = v;
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            sum += exp((double)load(x, base + j) - m);
+        for (int64_t j = 0; j < cols; ++j) {
+            double p = exp((double)load(x, base + j) - m) / sum;
+            if (bf16)
+                ((uint16_t *)y)[base + j] = oracle_bf16_from_double(p);
+            else
+                ((float *)y)[base + j] = (float)p;
+        }
+    }
+}
+
+void oracle_row_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols)
+{
+    o5_rows(x, load_f32, y, 0, rows, cols);
+}
+
+void oracle_row_softmax_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols)
+{
+    o5_rows(x, load_bf16, y, 1, rows, cols);
 }

@@ -79,6 +79,31 @@ void oracle_residual_layernorm_gelu_bf16(const uint16_t *x, const uint16_t *r,
                                          double *mean_out, double *rstd_out,
                                          double *xhat_out);
 
+/* ---- o2 with bf16 I/O: inputs widened exactly, the same fp32 steps and
+ * double row sum, y rounded once to bf16. */
+void oracle_bias_relu_branch_mean_epilogue_bf16(const uint16_t *x, const uint16_t *bias,
+                                                const uint16_t *gamma, const uint16_t *beta,
+                                                uint16_t *y, int64_t rows, int64_t cols,
+                                                float x_scale, float branch_scale);
+
+/* ---- o4: LayerNorm family ([P3] §4.3 LayerNorm; [P2] §2.1-2.3 residual add,
+ * LayerNorm -> ReLU, LayerNorm + GeLU):
+ *   v = x (+ r when r is not NULL), in fp32;  h_out = v (when not NULL);
+ *   out = act((v - mean) * rstd * w + b),  act: 0 none, 1 relu, 2 gelu_tanh.
+ * Statistics as in o3 (double, biased two-pass variance, eps inside sqrt). */
+void oracle_layernorm_act_f32(const float *x, const float *r, const float *w,
+                              const float *b, float *out, float *h_out, int64_t rows,
+                              int64_t hidden, float eps, int act);
+void oracle_layernorm_act_bf16(const uint16_t *x, const uint16_t *r, const uint16_t *w,
+                               const uint16_t *b, uint16_t *out, uint16_t *h_out,
+                               int64_t rows, int64_t hidden, float eps, int act);
+
+/* ---- o5: row softmax ([P1] §4.1-4.2, [P2] §3.2: the softmax of each score
+ * row, taken relative to the row maximum):
+ *   m = max_j x_j;  e_j = exp(x_j - m);  y_j = e_j / sum_k e_k   (in double) */
+void oracle_row_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols);
+void oracle_row_softmax_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols);
+
 #ifdef __cplusplus
 }
 #endif

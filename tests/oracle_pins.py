@@ -328,4 +328,126 @@ def pin_ln_bf16_library(lib):
     assert np.mean(got == want) > 0.999
 
 
+# --------------------------------------------------------------------------
+# o2 with bf16 I/O
+# --------------------------------------------------------------------------
+
+def pin_inductor_bf16_library(lib):
+    """bf16 inputs widened, the page's model() steps in torch eager fp32, one
+    rounding to bf16: equal except where the mean's summation order moves a
+    value across a bf16 rounding boundary (then one bf16 step apart)."""
+    x = synth.normal(41, 0, (48, 1024), dtype="bf16")
+    bias = synth.normal(41, 1, (1024,), 0.0, 0.1, dtype="bf16")
+    gamma = synth.uniform(41, 2, (1024,), 0.5, 1.5, dtype="bf16")
+    beta = synth.normal(41, 3, (1024,), 0.0, 0.1, dtype="bf16")
+    xf, bf, gf, btf = (torch.from_numpy(synth.bf16_bits_to_f32(a)) for a in (x, bias, gamma, beta))
+    a = torch.relu(xf * 1.1 + bf)
+    s = a * a + a * 0.1
+    m = s.double().mean(dim=1, keepdim=True).float()
+    want = ((s - m) * gf + btf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bias_relu_branch_mean_epilogue_bf16(x, bias, gamma, beta, lib=lib)
+    g, w = synth.bf16_bits_to_f32(got).astype(np.float64), synth.bf16_bits_to_f32(want).astype(np.float64)
+    assert np.all(np.abs(g - w) <= 2.0 ** -7 * np.abs(w) + 1e-30)
+    assert np.mean(got == want) > 0.999
+    # all-negative row: y = beta exactly
+    xn = synth.f32_to_bf16_bits(-np.abs(synth.bf16_bits_to_f32(x[:1])) - 1.0)
+    yn = oracle.bias_relu_branch_mean_epilogue_bf16(xn, np.zeros(1024, np.uint16), gamma, beta, lib=lib)
+    assert np.array_equal(yn[0], beta)
+
+
+# --------------------------------------------------------------------------
+# o4: LayerNorm family
+# --------------------------------------------------------------------------
+
+def pin_layernorm_act_library(lib):
+    """Every (residual, activation) combination against torch float64
+    layer_norm followed by relu / gelu(tanh), on v = x + r in fp32: within one
+    fp32 rounding; h equals the fp32 sum bit for bit."""
+    x, r, w, b = _ln_inputs(7, 515, 51)
+    eps = float(np.float32(1e-5))
+    for res in (False, True):
+        v = torch.from_numpy(x) + torch.from_numpy(r) if res else torch.from_numpy(x)
+        n = F.layer_norm(v.double(), (515,), torch.from_numpy(w).double(),
+                         torch.from_numpy(b).double(), eps=eps)
+        for act, f in ((0, lambda t: t), (1, torch.relu),
+                       (2, lambda t: F.gelu(t, approximate="tanh"))):
+            want = f(n).numpy()
+            got, h = oracle.layernorm_act(x, r if res else None, w, b, 1e-5, act,
+                                          want_h=True, lib=lib)
+            err = np.abs(got.astype(np.float64) - want)
+            assert np.all(err <= 1.0001 * U32 * np.abs(want) + 1e-30), (res, act, err.max())
+            assert np.array_equal(_bits(h), _bits(v.numpy())), (res, act)
+
+
+def pin_layernorm_plain_closed_form(lib):
+    """act none, w = 1, b = 0: each row has mean 0 and variance
+    var/(var + eps) up to the final fp32 rounding ([P3] §4.3)."""
+    x, _, _, _ = _ln_inputs(9, 800, 52)
+    ones, zeros = np.ones(800, np.float32), np.zeros(800, np.float32)
+    y = oracle.layernorm_act(x, None, ones, zeros, 1e-5, 0, lib=lib).astype(np.float64)
+    v = x.astype(np.float64)
+    var = v.var(axis=1)
+    assert np.all(np.abs(y.mean(axis=1)) <= 4 * U32)
+    want = var / (var + np.float64(np.float32(1e-5)))
+    assert np.all(np.abs((y * y).mean(axis=1) - want) <= 8 * U32)
+    # relu of the same: exactly max(y, 0) with -0 mapped to +0
+    yr = oracle.layernorm_act(x, None, ones, zeros, 1e-5, 1, lib=lib)
+    assert np.array_equal(_bits(yr), _bits(np.where(y > 0, y, 0.0).astype(np.float32)))
+
+
+def pin_layernorm_act_bf16(lib):
+    """bf16: out within half a bf16 step of float64; h is the fp32 sum
+    rounded to bf16 (torch's fp32 -> bf16)."""
+    x, r, w, b = _ln_inputs(5, 264, 53, dtype="bf16")
+    xf, rf, wf, bf = (torch.from_numpy(synth.bf16_bits_to_f32(a)) for a in (x, r, w, b))
+    v = xf + rf
+    n = F.layer_norm(v.double(), (264,), wf.double(), bf.double(), eps=float(np.float32(1e-5)))
+    got, h = oracle.layernorm_act(x, r, w, b, 1e-5, 1, want_h=True, lib=lib)
+    want = torch.relu(n).numpy()
+    g = synth.bf16_bits_to_f32(got).astype(np.float64)
+    assert np.all(np.abs(g - want) <= 2.0 ** -8 * np.abs(want) * 1.0001 + 1e-30)
+    assert np.array_equal(h, v.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+
+
+# --------------------------------------------------------------------------
+# o5: row softmax
+# --------------------------------------------------------------------------
+
+def pin_softmax_library(lib):
+    """torch float64 softmax of the fp32 rows: within one fp32 rounding."""
+    x = synth.normal(61, 0, (12, 1000), 0.0, 3.0)
+    want = torch.softmax(torch.from_numpy(x).double(), dim=1).numpy()
+    got = oracle.row_softmax(x, lib=lib)
+    assert np.all(np.abs(got.astype(np.float64) - want) <= 1.0001 * U32 * want + 1e-45)
+
+
+def pin_softmax_closed_forms(lib):
+    """Rows sum to 1; a constant row gives 1/cols; [a, b] gives
+    (sigmoid(a - b), sigmoid(b - a)); a shift by 1000 changes nothing (and
+    must not overflow); a row spanning +-1000 puts all mass on its maximum."""
+    x = synth.normal(62, 0, (6, 333))
+    y = oracle.row_softmax(x, lib=lib).astype(np.float64)
+    assert np.all(np.abs(y.sum(axis=1) - 1.0) <= 333 * U32)
+    c = oracle.row_softmax(np.full((2, 7), 3.25, np.float32), lib=lib)
+    assert np.all(c == np.float32(1.0 / 7.0))
+    ab = np.array([[1.5, -0.75], [-2.0, 4.0]], np.float32)
+    want = torch.sigmoid(torch.tensor([[2.25, -2.25], [-6.0, 6.0]], dtype=torch.float64))
+    got = oracle.row_softmax(ab, lib=lib).astype(np.float64)
+    assert np.all(np.abs(got - want.numpy()) <= U32 * want.numpy() * 1.0001)
+    q = np.round(synth.normal(63, 0, (3, 50)) * 1024) / 1024           # exact + 1000
+    s0 = oracle.row_softmax(q.astype(np.float32), lib=lib)
+    s1 = oracle.row_softmax((q + 1000.0).astype(np.float32), lib=lib)
+    assert np.all(np.isfinite(s1)) and np.array_equal(s0, s1)
+    wide = oracle.row_softmax(np.array([[0.0, 1000.0, -1000.0]], np.float32), lib=lib)
+    assert np.array_equal(wide, np.array([[0.0, 1.0, 0.0]], np.float32))
+
+
+def pin_softmax_bf16(lib):
+    """bf16 rows: within half a bf16 step of the float64 softmax."""
+    x = synth.normal(64, 0, (4, 640), 0.0, 2.0, dtype="bf16")
+    want = torch.softmax(torch.from_numpy(synth.bf16_bits_to_f32(x)).double(), dim=1).numpy()
+    g = synth.bf16_bits_to_f32(oracle.row_softmax(x, lib=lib)).astype(np.float64)
+    assert np.all(np.abs(g - want) <= 2.0 ** -8 * want * 1.0001 + 1e-40)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

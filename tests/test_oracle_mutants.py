@@ -58,6 +58,22 @@ MUTANTS = {
     "bf16_truncates": ("double k = rint(ldexp(a, -q));",
                        "double k = floor(ldexp(a, -q));"),
     "bf16_extra_bit": ("int q = e - 8;", "int q = e - 9;"),
+    # o2 bf16
+    "o2bf16_drop_beta": ("float o = d + widen_bf16(beta[j]);", "float o = d;"),
+    # o4: LayerNorm family
+    "o4_relu_dropped": ("return n > 0.0 ? n : 0.0;      /* relu", "return n;      /* relu"),
+    "o4_drop_eps": ("double rstd = 1.0 / sqrt(sq / (double)hidden + (double)eps);",
+                    "double rstd = 1.0 / sqrt(sq / (double)hidden);"),
+    "o4_h_is_x": ("((float *)h_out)[base + j] = v;",
+                  "((float *)h_out)[base + j] = load(x, base + j);"),
+    "o4_residual_ignored_in_stats": ("            if (r)\n                v = v + load(r, base + j);\n            sum += (double)v;",
+                                     "            sum += (double)v;"),
+    # o5: row softmax
+    "o5_sum_unshifted": ("sum += exp((double)load(x, base + j) - m);",
+                         "sum += exp((double)load(x, base + j));"),
+    "o5_divide_by_cols": ("double p = exp((double)load(x, base + j) - m) / sum;",
+                          "double p = exp((double)load(x, base + j) - m) / (double)cols;"),
+    "o5_min_not_max": ("if (v > m)\n                m = v;", "if (v < m || m == -INFINITY)\n                m = v;"),
 }
 
 
