@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-eager", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the further chains (softmax, LayerNorm family, bf16 Inductor)")
     return ap.parse_args(argv)
 
 
@@ -202,6 +204,8 @@ class Case:
         self.sets = [first] + [{k: v.clone() for k, v in first.items()}
                                for _ in range(self.nsets - 1)]
         self.outs = [torch.empty(shape, dtype=dt, device=device) for _ in range(self.nsets)]
+        self.houts = ([torch.empty(shape, dtype=dt, device=device) for _ in range(self.nsets)]
+                      if w.params.get("write_h") else None)
         self.dev, self.out = self.sets[0], self.outs[0]
         self.in_bytes = sum(v.nbytes for v in host.values())
         self.out_bytes = self.out.numel() * self.out.element_size()
@@ -215,6 +219,12 @@ class Case:
         elif self.w.chain == "inductor":
             mb.fused_bias_relu_branch_mean_epilogue(d["x"], d["bias"], d["gamma"], d["beta"],
                                                     p["x_scale"], p["branch_scale"], out=out)
+        elif self.w.chain == "softmax":
+            mb.fused_row_softmax(d["x"], out=out)
+        elif self.w.chain == "lnact":
+            mb.fused_layernorm_act(d["x"], d["w"], d["b"], r=d.get("r"), eps=p["eps"],
+                                   act=p["act"], out=out,
+                                   h_out=self.houts[k % self.nsets] if p["write_h"] else None)
         else:
             mb.fused_residual_layernorm_gelu(d["x"], d["r"], d["w"], d["b"], p["eps"], out=out)
 
@@ -225,6 +235,12 @@ class Case:
         d, p = self.sets[k % self.nsets], self.w.params
         if self.w.chain == "add_relu_scale":
             return torch.relu(d["x"] + d["b1"]) * p["scale"] + d["b2"]
+        if self.w.chain == "softmax":
+            return torch.softmax(d["x"], dim=1)
+        if self.w.chain == "lnact":
+            v = d["x"] + d["r"] if "r" in d else d["x"]
+            n = F.layer_norm(v, (self.w.cols,), d["w"], d["b"], p["eps"])
+            return torch.relu(n) if p["act"] == "relu" else F.gelu(n, approximate="tanh")
         if self.w.chain == "inductor":
             t = d["x"] * p["x_scale"] + d["bias"]
             a = torch.relu(t)
@@ -472,6 +488,26 @@ def run_ours(args):
             entry["speedup_vs_eager"] = round(em / mean_ms, 2)
         per_kernel[c.w.name] = entry
 
+    # The scope table's further chains, measured the same way (not part of
+    # the step or its value).
+    next_rows = None
+    if not args.no_next:
+        nxt = [Case(w, device, l2_bytes) for w in W.NEXT]
+        t_next = time_graph(nxt, lambda c, k: c.call(k), args.steps, args.warmup)
+        e_next = (time_graph(nxt, lambda c, k: c.eager(k), max(5, args.steps // 5), 2)
+                  if not args.no_eager else None)
+        next_rows = {}
+        for c in nxt:
+            ms = t_next[c.w.name]
+            gbs = c.ideal / (ms * 1e-3) / 1e9
+            ent = {"us_per_call": round(ms * 1e3, 3), "ideal_bytes": c.ideal,
+                   "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+            if e_next:
+                ent["eager_us_per_call"] = round(e_next[c.w.name] * 1e3, 3)
+                ent["speedup_vs_eager"] = round(e_next[c.w.name] / ms, 2)
+            next_rows[c.w.name] = ent
+        del nxt
+
     step_ms, value = aggregate_ranks(step_ms, step_bytes, world, device)
 
     dominant = max(cases, key=lambda c: per_kernel[c.w.name]["us_per_call"])
@@ -502,6 +538,8 @@ def run_ours(args):
             "wall_s_timed_region": round(t_wall, 3)}
     if clocks:
         line["clocks"] = clocks
+    if next_rows:
+        line["next_rows"] = next_rows
     if e2e:
         e_ms, bi, bo = e2e
         line["e2e"] = {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": UNIT,

@@ -9,6 +9,10 @@
  *   fused_bias_relu_branch_mean_epilogue  the TorchInductor example chain
  *   fused_residual_layernorm_gelu         GeLU_tanh(LayerNorm(x + r) * w + b)
  *
+ * and, built on the same row engines: fused_layernorm_act (LayerNorm with an
+ * optional residual, residual-stream output and activation), fused_row_softmax
+ * and the bf16 variant of the TorchInductor chain.
+ *
  * Sources (the pages these chains come from):
  *   [P1] "PyTorch operator fusion in practice", www.0539edu.com/news/5489619
  *   [P2] "Operator fusion and kernel optimisation: from CUDA Graph to
@@ -150,6 +154,60 @@ mb_status fused_residual_layernorm_gelu(const void *x, const void *r,
                                         mb_dtype dtype, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Further chains: the LayerNorm family, row softmax, bf16 Inductor chain   */
+/* ------------------------------------------------------------------------ */
+
+typedef enum mb_activation {
+    MB_ACT_NONE = 0,
+    MB_ACT_RELU = 1,        /* every value not > 0 (including -0, NaN) -> +0 */
+    MB_ACT_GELU_TANH = 2
+} mb_activation;
+
+/*
+ * The LayerNorm family, row by row over rows x hidden:
+ *   v = x + r  (or v = x when r is NULL);  h_out = v  (when h_out is not NULL);
+ *   mean, biased two-pass variance, rstd = 1/sqrt(var + eps);
+ *   out = act((v - mean) * rstd * w[j] + b[j])
+ *
+ * [P3] §4.3 (LayerNorm: mean, two-pass variance, (x - mean)/sqrt(var + eps) *
+ * gamma + beta), [P2] §2.1 (LayerNorm -> ReLU in one kernel) and §2.2-2.3
+ * (residual + LayerNorm, then GeLU).  h_out is the residual stream a
+ * Transformer block carries on: the fp32 sum rounded once to the I/O dtype.
+ * Arithmetic as in fused_residual_layernorm_gelu.
+ *
+ *   x, r   rows x hidden (input; r may be NULL)     w, b  hidden each (input)
+ *   out    rows x hidden (output)                    h_out rows x hidden (output, may be NULL)
+ *   act    an mb_activation; other codes give MB_ERR_VALUE
+ *   out and h_out may not overlap each other or any input.
+ */
+mb_status fused_layernorm_act(const void *x, const void *r, const void *w, const void *b,
+                              void *out, void *h_out, int64_t rows, int64_t hidden,
+                              float eps, mb_activation act, mb_dtype dtype,
+                              cudaStream_t stream);
+
+/*
+ * Row softmax over rows x cols:  y[i, j] = exp(x[i, j] - m_i) / sum_k exp(x[i, k] - m_i),
+ * m_i the row maximum.  [P1] §4.1-4.2 and [P2] §3.2 (the softmax of a score
+ * row, normalised by the row maximum; here the row is held on chip, so it is
+ * read once).  fp32 arithmetic; exponentials on the SFU (2^(d log2 e)).
+ *
+ *   x  rows x cols (input)    y  rows x cols (output)    1 <= cols <= MB_MAX_COLS
+ */
+mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols,
+                            mb_dtype dtype, cudaStream_t stream);
+
+/*
+ * fused_bias_relu_branch_mean_epilogue with bf16 I/O: x, bias, gamma, beta
+ * and y are bf16 bit patterns; inputs are widened exactly, the same fp32
+ * steps run, and y is rounded once to bf16.
+ */
+mb_status fused_bias_relu_branch_mean_epilogue_bf16(const void *x, const void *bias,
+                                                    const void *gamma, const void *beta,
+                                                    void *y, int64_t rows, int64_t cols,
+                                                    float x_scale, float branch_scale,
+                                                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status, diagnostics and tuning                                           */
 /* ------------------------------------------------------------------------ */
 
@@ -206,9 +264,10 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * out[0] = path (mb_row_path), out[1] = threads per CTA, out[2] = CTAs,
  * out[3] = values per thread slot (vectors per thread), out[4] = vector width
  * in elements, out[5] = ring stages (staged path, else 0),
- * out[6] = dynamic shared memory bytes.  `chain` is 0 for the LayerNorm
- * chain, 1 for the TorchInductor chain; `aligned` says whether every pointer
- * is 16-byte aligned.  Queries the current device (SM count, shared memory).
+ * out[6] = dynamic shared memory bytes.  `chain`: 0 residual + LayerNorm +
+ * GeLU, 1 the TorchInductor chain, 2 the LayerNorm family with a residual,
+ * 3 without, 4 row softmax.  `aligned` says whether every pointer is 16-byte
+ * aligned.  Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,
                       int aligned, int32_t out[7]);

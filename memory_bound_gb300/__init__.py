@@ -10,13 +10,15 @@ fallback of any kind, and calling a chain without the built library raises.
     fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None)
     fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta,
                                          x_scale=1.1, branch_scale=0.1, out=None)
+    fused_layernorm_act(x, w, b, r=None, eps=1e-5, act="gelu_tanh", want_h=False)
+    fused_row_softmax(x, out=None)
 
 ``raw`` exposes the C entry points themselves (plain integers for pointers
 and streams) for callers that manage their own memory.
 """
 from ._binding import (  # noqa: F401
-    MB_BF16, MB_F32, MB_MAX_COLS, MBError, ROW_PATHS, device_error,
-    fused_add_relu_scale, fused_bias_relu_branch_mean_epilogue,
-    fused_residual_layernorm_gelu, library_path, load_library, raw, row_plan,
+    ACTIVATIONS, MB_BF16, MB_F32, MB_MAX_COLS, MBError, ROW_PATHS, device_error,
+    fused_add_relu_scale, fused_bias_relu_branch_mean_epilogue, fused_layernorm_act,
+    fused_residual_layernorm_gelu, fused_row_softmax, library_path, load_library, raw, row_plan,
     set_pointwise_shape, set_row_path, status_string,
 )

@@ -8,6 +8,7 @@ _LIB_PATH = os.path.join(HERE, "libmemory_bound.so")
 MB_F32, MB_BF16 = 0, 1
 MB_MAX_COLS = 32768
 ROW_PATHS = {"auto": 0, "warp": 1, "direct": 2, "staged": 3}
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu_tanh": 2}
 
 STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_NULL", 2: "MB_ERR_SHAPE", 3: "MB_ERR_DTYPE",
                 4: "MB_ERR_OVERLAP", 5: "MB_ERR_ALIGN", 6: "MB_ERR_VALUE",
@@ -21,6 +22,9 @@ SIGNATURES = {
     "fused_add_relu_scale": (_I, [_P, _P, _P, _P, _I64, _F, _I, _P]),
     "fused_bias_relu_branch_mean_epilogue": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _F, _P]),
     "fused_residual_layernorm_gelu": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]),
+    "fused_bias_relu_branch_mean_epilogue_bf16": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _F, _P]),
+    "fused_layernorm_act": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P]),
+    "fused_row_softmax": (_I, [_P, _P, _I64, _I64, _I, _P]),
     "mb_status_string": (ctypes.c_char_p, [_I]),
     "mb_abi_version": (_I, []),
     "mb_last_cuda_error": (_I, []),
@@ -145,13 +149,16 @@ def fused_add_relu_scale(x, b1, b2, scale=0.5, out=None):
 
 def fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
                                          branch_scale=0.1, out=None):
-    """The TorchInductor example chain on a 2-D float32 x (rows x cols)."""
+    """The TorchInductor example chain on a 2-D x (rows x cols), float32 or
+    bfloat16 (all tensors one dtype)."""
     torch = _torch()
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, cols)")
     if out is None:
         out = torch.empty_like(x)
-    _require([x, bias, gamma, beta, out], torch.float32)
+    _require([x, bias, gamma, beta, out], x.dtype)
+    fn_name = ("fused_bias_relu_branch_mean_epilogue" if _dtype_code(x) == MB_F32
+               else "fused_bias_relu_branch_mean_epilogue_bf16")
     rows, cols = x.shape
     for v in (bias, gamma, beta):
         if v.numel() != cols:
@@ -159,11 +166,11 @@ def fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
     if out.numel() != x.numel():
         raise ValueError("out must match x")
     with torch.cuda.device(x.device):
-        st = load_library().fused_bias_relu_branch_mean_epilogue(
+        st = getattr(load_library(), fn_name)(
             x.data_ptr(), bias.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
             out.data_ptr(), rows, cols, float(x_scale), float(branch_scale),
             _stream_handle(x))
-    _check("fused_bias_relu_branch_mean_epilogue", st)
+    _check(fn_name, st)
     return out
 
 
@@ -185,6 +192,54 @@ def fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None):
             x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(),
             rows, hidden, float(eps), _dtype_code(x), _stream_handle(x))
     _check("fused_residual_layernorm_gelu", st)
+    return out
+
+
+def fused_layernorm_act(x, w, b, r=None, eps=1e-5, act="gelu_tanh", out=None, h_out=None,
+                        want_h=False):
+    """act(LayerNorm(x (+ r)) * w + b) over the last dim of a 2-D x.  With
+    ``want_h`` (or an ``h_out`` tensor) also writes h = x + r (or x), the
+    residual stream; returns (out, h) then, else out."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, hidden)")
+    if out is None:
+        out = torch.empty_like(x)
+    if want_h and h_out is None:
+        h_out = torch.empty_like(x)
+    ts = [x, w, b, out] + [t for t in (r, h_out) if t is not None]
+    _require(ts, x.dtype)
+    rows, hidden = x.shape
+    if (r is not None and r.shape != x.shape) or w.numel() != hidden or b.numel() != hidden:
+        raise ValueError("shape mismatch")
+    for t in (out, h_out):
+        if t is not None and t.numel() != x.numel():
+            raise ValueError("outputs must match x")
+    code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    with torch.cuda.device(x.device):
+        st = load_library().fused_layernorm_act(
+            x.data_ptr(), r.data_ptr() if r is not None else None, w.data_ptr(), b.data_ptr(),
+            out.data_ptr(), h_out.data_ptr() if h_out is not None else None, rows, hidden,
+            float(eps), code, _dtype_code(x), _stream_handle(x))
+    _check("fused_layernorm_act", st)
+    return (out, h_out) if h_out is not None else out
+
+
+def fused_row_softmax(x, out=None):
+    """Softmax over the last dim of a 2-D x (float32 or bfloat16)."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, cols)")
+    if out is None:
+        out = torch.empty_like(x)
+    _require([x, out], x.dtype)
+    if out.numel() != x.numel():
+        raise ValueError("out must match x")
+    rows, cols = x.shape
+    with torch.cuda.device(x.device):
+        st = load_library().fused_row_softmax(x.data_ptr(), out.data_ptr(), rows, cols,
+                                              _dtype_code(x), _stream_handle(x))
+    _check("fused_row_softmax", st)
     return out
 
 
@@ -213,9 +268,10 @@ def set_pointwise_shape(blocks_per_sm=0, unroll=0):
 
 def row_plan(chain, dtype, rows, cols, aligned=True):
     """The launch a row chain would use: dict(path, threads, ctas, vpt, vec,
-    stages, smem).  chain: "ln" or "inductor"; dtype: "f32" or "bf16"."""
+    stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact" or
+    "softmax"; dtype: "f32" or "bf16"."""
     out = (ctypes.c_int32 * 7)()
-    code = {"ln": 0, "inductor": 1}[chain]
+    code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4}[chain]
     dt = {"f32": MB_F32, "bf16": MB_BF16}[dtype]
     st = load_library().mb_row_plan(code, dt, rows, cols, int(bool(aligned)), out)
     _check("mb_row_plan", st)

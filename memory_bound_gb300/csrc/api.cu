@@ -175,6 +175,83 @@ mb_status fused_bias_relu_branch_mean_epilogue(const float *x, const float *bias
                              branch_scale, aligned, nullptr, true);
 }
 
+mb_status fused_bias_relu_branch_mean_epilogue_bf16(const void *x, const void *bias,
+                                                    const void *gamma, const void *beta,
+                                                    void *y, int64_t rows, int64_t cols,
+                                                    float x_scale, float branch_scale,
+                                                    cudaStream_t stream) {
+    mb_status st = check_rows(rows, cols);
+    if (st != MB_OK) return st;
+    if (!std::isfinite(x_scale) || !std::isfinite(branch_scale)) return MB_ERR_VALUE;
+    if (rows == 0) return MB_OK;
+    if (!x || !bias || !gamma || !beta || !y) return MB_ERR_NULL;
+    for (const void *p : {x, bias, gamma, beta, static_cast<const void *>(y)})
+        if (!aligned_to(p, 2)) return MB_ERR_ALIGN;
+    const int64_t big = rows * cols * 2, small = cols * 2;
+    if (overlaps(y, big, x, big) || overlaps(y, big, bias, small) ||
+        overlaps(y, big, gamma, small) || overlaps(y, big, beta, small))
+        return MB_ERR_OVERLAP;
+    bool aligned = true;
+    for (const void *p : {x, bias, gamma, beta, static_cast<const void *>(y)})
+        aligned = aligned && aligned_to(p, 16);
+    LaunchCtx ctx;
+    if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
+    return inductor_rows_bf16(ctx, g_tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
+                              branch_scale, aligned, nullptr, true);
+}
+
+mb_status fused_layernorm_act(const void *x, const void *r, const void *w, const void *b,
+                              void *out, void *h_out, int64_t rows, int64_t hidden, float eps,
+                              mb_activation act, mb_dtype dtype, cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
+    mb_status st = check_rows(rows, hidden);
+    if (st != MB_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return MB_ERR_VALUE;
+    if (act != MB_ACT_NONE && act != MB_ACT_RELU && act != MB_ACT_GELU_TANH) return MB_ERR_VALUE;
+    if (rows == 0) return MB_OK;
+    if (!x || !w || !b || !out) return MB_ERR_NULL;
+    const int es = elem_size(dtype);
+    for (const void *p : {x, r, w, b, static_cast<const void *>(out),
+                          static_cast<const void *>(h_out)})
+        if (p && !aligned_to(p, es)) return MB_ERR_ALIGN;
+    const int64_t big = rows * hidden * es, small = hidden * es;
+    for (const void *o : {static_cast<const void *>(out), static_cast<const void *>(h_out)}) {
+        if (!o) continue;
+        if (overlaps(o, big, x, big) || (r && overlaps(o, big, r, big)) ||
+            overlaps(o, big, w, small) || overlaps(o, big, b, small))
+            return MB_ERR_OVERLAP;
+    }
+    if (h_out && overlaps(out, big, h_out, big)) return MB_ERR_OVERLAP;
+    bool aligned = true;
+    for (const void *p : {x, r, w, b, static_cast<const void *>(out),
+                          static_cast<const void *>(h_out)})
+        aligned = aligned && (!p || aligned_to(p, 16));
+    LaunchCtx ctx;
+    if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
+    if (dtype == MB_F32)
+        return lnact_rows_f32(ctx, g_tuning, r != nullptr, x, r, w, b, out, h_out, rows,
+                              (int)hidden, eps, (int)act, aligned, nullptr, true);
+    return lnact_rows_bf16(ctx, g_tuning, r != nullptr, x, r, w, b, out, h_out, rows,
+                           (int)hidden, eps, (int)act, aligned, nullptr, true);
+}
+
+mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols, mb_dtype dtype,
+                            cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
+    mb_status st = check_rows(rows, cols);
+    if (st != MB_OK) return st;
+    if (rows == 0) return MB_OK;
+    if (!x || !y) return MB_ERR_NULL;
+    const int es = elem_size(dtype);
+    if (!aligned_to(x, es) || !aligned_to(y, es)) return MB_ERR_ALIGN;
+    const int64_t big = rows * cols * es;
+    if (overlaps(y, big, x, big)) return MB_ERR_OVERLAP;
+    const bool aligned = aligned_to(x, 16) && aligned_to(y, 16);
+    LaunchCtx ctx;
+    if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
+    return softmax_rows(ctx, g_tuning, dtype, x, y, rows, (int)cols, aligned, nullptr, true);
+}
+
 const char *mb_status_string(mb_status s) {
     switch (s) {
         case MB_OK: return "ok";
@@ -231,16 +308,26 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll) {
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int aligned,
                       int32_t out[7]) {
     if (!out) return MB_ERR_NULL;
-    if (chain != 0 && chain != 1) return MB_ERR_VALUE;
-    if (!valid_dtype(dtype) || (chain == 1 && dtype != MB_F32)) return MB_ERR_DTYPE;
+    if (chain < 0 || chain > 4) return MB_ERR_VALUE;
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
     mb_status st = check_rows(rows, cols);
     if (st != MB_OK) return st;
     LaunchCtx ctx;
     if ((st = device_ctx(0, &ctx)) != MB_OK) return st;
     RowPlan p;
-    if (chain == 1)
+    const bool al = aligned != 0;
+    if (chain == 1 && dtype == MB_F32)
         st = inductor_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
-                               (int)cols, 1.0f, 1.0f, aligned != 0, &p, false);
+                               (int)cols, 1.0f, 1.0f, al, &p, false);
+    else if (chain == 1)
+        st = inductor_rows_bf16(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+                                (int)cols, 1.0f, 1.0f, al, &p, false);
+    else if (chain == 2 || chain == 3)
+        st = (dtype == MB_F32 ? lnact_rows_f32 : lnact_rows_bf16)(
+            ctx, g_tuning, chain == 2, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+            (int)cols, 0.0f, 0, al, &p, false);
+    else if (chain == 4)
+        st = softmax_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, al, &p, false);
     else if (dtype == MB_F32)
         st = ln_gelu_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                               (int)cols, 0.0f, aligned != 0, &p, false);

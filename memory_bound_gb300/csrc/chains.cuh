@@ -16,6 +16,7 @@ template <typename TT> struct LnGeluChain {
     static constexpr int kInputs = 2;     // x, r
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
+    static constexpr bool kStorePre = false;
     struct Args {
         const T *in[2];
         const T *w;
@@ -52,6 +53,8 @@ template <typename TT> struct LnGeluChain {
         return rsqrtf(m2 / (float)cols + a.eps);
     }
     template <int VEC>
+    __device__ __forceinline__ static void store_pre(const float (&)[VEC], const Args &, int64_t) {}
+    template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float rstd,
                                                 const PostPC<VEC> &pc, const Args &,
                                                 float (&o)[VEC]) {
@@ -69,24 +72,26 @@ template <typename TT> struct LnGeluChain {
 //   s = p + q; m = mean(s, dim=1); y = (s - m) * gamma + beta.
 // Each pointwise step is rounded on its own (no contraction), as the fp32
 // eager ops would round it; s is recomputed in registers, never stored, and
-// the row sum never leaves the chip (§08 of the same post).
-struct InductorChain {
-    using T = float;
+// the row sum never leaves the chip (§08 of the same post).  With bf16 I/O
+// the inputs are widened exactly and y is rounded once.
+template <typename TT> struct InductorChainT {
+    using T = TT;
     static constexpr int kInputs = 1;     // x
     static constexpr bool kTwoPass = false;
     static constexpr bool kMaxFirst = false;
+    static constexpr bool kStorePre = false;
     struct Args {
-        const float *in[1];
-        const float *bias;
-        const float *gamma;
-        const float *beta;
-        float *out;
+        const T *in[1];
+        const T *bias;
+        const T *gamma;
+        const T *beta;
+        T *out;
         float x_scale;
         float branch_scale;
     };
     // per-column values of one slot: bias before the reduction, gamma and beta after
-    template <int VEC> struct PrePC { Frag<float, VEC> bias; };
-    template <int VEC> struct PostPC { Frag<float, VEC> gamma, beta; };
+    template <int VEC> struct PrePC { Frag<T, VEC> bias; };
+    template <int VEC> struct PostPC { Frag<T, VEC> gamma, beta; };
     static constexpr int kPostPC = 2;
     template <int VEC>
     __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc) {
@@ -98,7 +103,7 @@ struct InductorChain {
         pc.beta.load_cached(a.beta + col);
     }
     template <int VEC>
-    __device__ __forceinline__ static void pre(const Frag<float, VEC> (&in)[1],
+    __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1],
                                                const PrePC<VEC> &pc, const Args &a,
                                                float (&v)[VEC]) {
 #pragma unroll
@@ -117,12 +122,137 @@ struct InductorChain {
     __device__ __forceinline__ static float p2(float &, float, float acc) { return acc; }
     __device__ __forceinline__ static float stat2(float, int, const Args &) { return 0.0f; }
     template <int VEC>
+    __device__ __forceinline__ static void store_pre(const float (&)[VEC], const Args &, int64_t) {}
+    template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
                                                 const PostPC<VEC> &pc, const Args &,
                                                 float (&o)[VEC]) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
             o[e] = __fadd_rn(__fmul_rn(__fsub_rn(v[e], mean), pc.gamma.f[e]), pc.beta.f[e]);
+    }
+};
+using InductorChain = InductorChainT<float>;
+
+// LayerNorm family: v = x (+ r); optionally h = v written out (the residual
+// stream); out = act((v - mean) * rstd * w + b), act none / relu / gelu-tanh.
+// "Kernel fusion" course chapter 4 (5688vip.com) §4.3 (LayerNorm, two-pass
+// variance); "Operator fusion and kernel optimisation" (plumephp.com) §2.1
+// (LayerNorm -> ReLU in one kernel) and §2.2-2.3 (residual + LayerNorm + GeLU).
+enum { kActNone = 0, kActRelu = 1, kActGelu = 2 };
+template <typename TT, bool RES> struct LnActChain {
+    using T = TT;
+    static constexpr int kInputs = RES ? 2 : 1;
+    static constexpr bool kTwoPass = true;
+    static constexpr bool kMaxFirst = false;
+    static constexpr bool kStorePre = true;
+    struct Args {
+        const T *in[kInputs];
+        const T *w;
+        const T *b;
+        T *out;
+        T *h;          // residual-stream output (NULL: not written)
+        float eps;
+        int act;
+    };
+    template <int VEC> struct PrePC {};
+    template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
+    static constexpr int kPostPC = 2;
+    template <int VEC>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
+    template <int VEC>
+    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
+        pc.w.load_cached(a.w + col);
+        pc.b.load_cached(a.b + col);
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[kInputs],
+                                               const PrePC<VEC> &, const Args &,
+                                               float (&v)[VEC]) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            if constexpr (RES) v[e] = __fadd_rn(in[0].f[e], in[1].f[e]);
+            else v[e] = in[0].f[e];
+        }
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void store_pre(const float (&v)[VEC], const Args &a,
+                                                     int64_t off) {
+        if (a.h) {
+            Frag<T, VEC> f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) f.f[e] = v[e];
+            f.store_stream(a.h + off);
+        }
+    }
+    __device__ __forceinline__ static float stat1(float sum, int cols, const Args &) {
+        return sum / (float)cols;
+    }
+    __device__ __forceinline__ static float p2(float &v, float mean, float acc) {
+        const float d = v - mean;
+        return fmaf(d, d, acc);
+    }
+    __device__ __forceinline__ static float stat2(float m2, int cols, const Args &a) {
+        return rsqrtf(m2 / (float)cols + a.eps);
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float rstd,
+                                                const PostPC<VEC> &pc, const Args &a,
+                                                float (&o)[VEC]) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const float n = fmaf((v[e] - mean) * rstd, pc.w.f[e], pc.b.f[e]);
+            o[e] = a.act == kActGelu ? gelu_tanh_f(n) : (a.act == kActRelu ? relu_f(n) : n);
+        }
+    }
+};
+
+// Row softmax: y = exp(x - max) / sum exp(x - max), the row held in
+// registers (one HBM read, one write).  "PyTorch operator fusion in
+// practice" (0539edu.com) §4.1-4.2 and "Operator fusion and kernel
+// optimisation" (plumephp.com) §3.2: the softmax of a score row, normalised
+// by the row maximum.  exp(d) = 2^(d log2 e) on the SFU.
+template <typename TT> struct SoftmaxChain {
+    using T = TT;
+    static constexpr int kInputs = 1;
+    static constexpr bool kTwoPass = true;
+    static constexpr bool kMaxFirst = true;
+    static constexpr bool kStorePre = false;
+    struct Args {
+        const T *in[1];
+        T *out;
+    };
+    template <int VEC> struct PrePC {};
+    template <int VEC> struct PostPC {};
+    static constexpr int kPostPC = 0;
+    template <int VEC>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
+    template <int VEC>
+    __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
+    template <int VEC>
+    __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1], const PrePC<VEC> &,
+                                               const Args &, float (&v)[VEC]) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[e] = in[0].f[e];
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void store_pre(const float (&)[VEC], const Args &, int64_t) {}
+    __device__ __forceinline__ static float stat1(float mx, int, const Args &) { return mx; }
+    // v <- exp(v - max); the second pass sums these
+    __device__ __forceinline__ static float p2(float &v, float mx, float acc) {
+        constexpr float kLog2e = 1.4426950408889634f;
+        v = ex2_approx((v - mx) * kLog2e);
+        return acc + v;
+    }
+    __device__ __forceinline__ static float stat2(float sum, int, const Args &) {
+        return 1.0f / sum;
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,
+                                                const PostPC<VEC> &, const Args &,
+                                                float (&o)[VEC]) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = v[e] * inv;
     }
 };
 

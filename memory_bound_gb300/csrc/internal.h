@@ -57,6 +57,22 @@ mb_status inductor_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const fl
                             float *y, int64_t rows, int cols, float x_scale,
                             float branch_scale, bool aligned, RowPlan *plan, bool launch);
 
+mb_status inductor_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
+                             const void *bias, const void *gamma, const void *beta, void *y,
+                             int64_t rows, int cols, float x_scale, float branch_scale,
+                             bool aligned, RowPlan *plan, bool launch);
+mb_status lnact_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, bool residual,
+                         const void *x, const void *r, const void *w, const void *b, void *out,
+                         void *h, int64_t rows, int cols, float eps, int act, bool aligned,
+                         RowPlan *plan, bool launch);
+mb_status lnact_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, bool residual,
+                          const void *x, const void *r, const void *w, const void *b, void *out,
+                          void *h, int64_t rows, int cols, float eps, int act, bool aligned,
+                          RowPlan *plan, bool launch);
+mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
+                       const void *x, void *y, int64_t rows, int cols, bool aligned,
+                       RowPlan *plan, bool launch);
+
 // Records a CUDA error for mb_last_cuda_error and returns MB_ERR_CUDA.
 mb_status cuda_fail(cudaError_t e);
 

@@ -8,6 +8,8 @@
 //           C::p2 forms from each v and s1 (p2 may also rewrite v in place)
 //   post  (per element)   the epilogue from v, s1, s2 and its per-column
 //                         values (PostPC)
+// and, with C::kStorePre, store_pre writes the prologue value v out as well
+// (the residual-stream output of a residual + LayerNorm block).
 // The row is read from device memory once and held in registers (v) between
 // the passes; the output is written once.
 //
@@ -89,6 +91,9 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
         for (int k = 0; k < VPL; ++k) {
             C::template pre<VEC>(in[k], pre[k], a, v[k]);
             l1 = fold1<C, VEC>(l1, v[k], lane + 32 * k < nvec);
+            if constexpr (C::kStorePre) {
+                if (lane + 32 * k < nvec) C::template store_pre<VEC>(v[k], a, base + (lane + 32 * k) * VEC);
+            }
         }
         const float mean = C::stat1(C::kMaxFirst ? warp_max(l1) : warp_sum(l1), cols, a);
         float rstd = 0.0f;
@@ -210,6 +215,10 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
         for (int k = 0; k < VPT; ++k) {
             C::template pre<VEC>(in[k], pre[k], a, v[k]);
             l1 = fold1<C, VEC>(l1, v[k], tid + k * (int)blockDim.x < nvec);
+            if constexpr (C::kStorePre) {
+                const int vi = tid + k * (int)blockDim.x;
+                if (vi < nvec) C::template store_pre<VEC>(v[k], a, base + vi * VEC);
+            }
         }
         // Barrier inside: after it every thread has its row slice in registers.
         const float r1 = C::kMaxFirst ? block_max(l1, red + 32 * rb) : block_sum(l1, red + 32 * rb);

@@ -1,4 +1,4 @@
-"""The five synthetic workloads, by name, with their seeds and tensor ids.
+"""The synthetic workloads, by name, with their seeds and tensor ids.
 
 Shapes and distributions are the pages' example workloads:
 
@@ -8,7 +8,10 @@ Shapes and distributions are the pages' example workloads:
 * the TorchInductor example on ``x`` f32[1024, 1024] with f32[1024] ``bias``,
   ``gamma``, ``beta`` ([P4] "model");
 * residual + LayerNorm + GeLU-tanh rows ([P2] §2.3) at hidden 4096 fp32 and
-  hidden 8192 bf16.
+  hidden 8192 bf16;
+* for the further chains (NEXT): row softmax on [P1] §4.1's attention-score
+  matrix, the LayerNorm family with a residual-stream output or a ReLU, and
+  the TorchInductor chain in bf16.
 
 N(mu, s) takes ``s`` as the standard deviation.  Tensor ids are assigned in
 the order each workload lists its tensors.
@@ -33,7 +36,7 @@ class Tensor:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    chain: str         # "add_relu_scale" | "inductor" | "ln_gelu"
+    chain: str         # "add_relu_scale" | "inductor" | "ln_gelu" | "lnact" | "softmax"
     dtype: str         # "f32" | "bf16"
     rows: int          # 1 for the pointwise chain
     cols: int          # n for the pointwise chain
@@ -59,7 +62,8 @@ class Workload:
         eb = self.elem_bytes
         full = sum(1 for t in self.tensors if not t.per_column)
         percol = sum(1 for t in self.tensors if t.per_column)
-        return rows * self.cols * eb * (full + 1) + percol * self.cols * eb
+        outs = 2 if self.params.get("write_h") else 1
+        return rows * self.cols * eb * (full + outs) + percol * self.cols * eb
 
     def generate(self, tensor, rows=None):
         """Host array for one tensor (uint16 bit patterns for bf16).
@@ -105,8 +109,31 @@ def _ln(name, dtype, rows, hidden, seed):
 LN_F32 = _ln("ln_gelu_f32_8192x4096", "f32", 8192, 4096, 3)
 LN_BF16 = _ln("ln_gelu_bf16_32768x8192", "bf16", 32768, 8192, 4)
 
+# Rows marked "next" in the scope table: the same shapes, other chains.
+# Row softmax on the attention-score matrix of "PyTorch operator fusion in
+# practice" §4.1 (batch 1, 32 heads, seq_len 4096: [32*4096, 4096] fp32).
+SOFTMAX_F32 = Workload("softmax_f32_131072x4096", "softmax", "f32", 32 * 4096, 4096, 5, (
+    Tensor("x", 0, "normal", 0.0, 1.0, False),
+), {})
+# Residual + LayerNorm + GeLU that also writes the residual stream h = x + r.
+LNACT_RES_BF16 = Workload("lnact_res_h_bf16_32768x8192", "lnact", "bf16", 32768, 8192, 6, (
+    Tensor("x", 0, "normal", 0.0, 1.0, False),
+    Tensor("r", 1, "normal", 0.0, 1.0, False),
+    Tensor("w", 2, "uniform", 0.5, 1.5, True),
+    Tensor("b", 3, "normal", 0.0, 0.1, True),
+), {"eps": 1e-5, "act": "gelu_tanh", "residual": True, "write_h": True})
+# Plain LayerNorm -> ReLU (no residual), fp32.
+LNACT_RELU_F32 = Workload("lnact_relu_f32_8192x4096", "lnact", "f32", 8192, 4096, 7, (
+    Tensor("x", 0, "normal", 0.0, 1.0, False),
+    Tensor("w", 2, "uniform", 0.5, 1.5, True),
+    Tensor("b", 3, "normal", 0.0, 0.1, True),
+), {"eps": 1e-5, "act": "relu", "residual": False, "write_h": False})
+INDUCTOR_BF16 = Workload("inductor_bf16_1024x1024", "inductor", "bf16", 1024, 1024, 8,
+                         INDUCTOR_1024.tensors, {"x_scale": 1.1, "branch_scale": 0.1})
+NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16)
+
 ALL = (POINTWISE_TINY, POINTWISE_4M, INDUCTOR_1024, LN_F32, LN_BF16)
-BY_NAME = {w.name: w for w in ALL}
+BY_NAME = {w.name: w for w in ALL + NEXT}
 
 
 def sample_rows(rows, count, seed=12345):

@@ -121,3 +121,24 @@ def test_binding_rejects_without_gpu_work():
     x = torch.zeros(8)
     with pytest.raises(ValueError):
         mb.fused_add_relu_scale(x, x, x)          # CPU tensors are refused
+
+
+def test_further_chains_argument_checks(lib):
+    f = lib.fused_layernorm_act
+    assert f(A, None, C, D, E, None, 0, 64, 1e-5, 2, 0, None) == MB_OK
+    assert f(A, None, C, D, E, None, 4, 64, 1e-5, 3, 0, None) == MB_ERR_VALUE   # act
+    assert f(A, None, C, D, E, None, 4, 64, 1e-5, 1, 9, None) == MB_ERR_DTYPE
+    assert f(None, None, C, D, E, None, 4, 64, 1e-5, 1, 0, None) == MB_ERR_NULL
+    assert f(A, B, C, D, E, E + 128, 4, 64, 1e-5, 1, 0, None) == MB_ERR_OVERLAP  # h over out
+    assert f(A, B, C, D, E, B + 64, 4, 64, 1e-5, 1, 0, None) == MB_ERR_OVERLAP   # h over r
+    assert f(A, B + 2, C, D, E, None, 4, 64, 1e-5, 1, 0, None) == MB_ERR_ALIGN
+    s = lib.fused_row_softmax
+    assert s(A, B, 0, 10, 0, None) == MB_OK
+    assert s(A, B, 4, 0, 0, None) == MB_ERR_SHAPE
+    assert s(A, A + 8, 4, 10, 0, None) == MB_ERR_OVERLAP
+    assert s(A, None, 4, 10, 1, None) == MB_ERR_NULL
+    assert s(A + 1, B, 4, 10, 1, None) == MB_ERR_ALIGN
+    g = lib.fused_bias_relu_branch_mean_epilogue_bf16
+    assert g(A, B, C, D, E, 0, 64, 1.1, 0.1, None) == MB_OK
+    assert g(A, B, C, D, A + 2, 2, 64, 1.1, 0.1, None) == MB_ERR_OVERLAP
+    assert g(A + 1, B, C, D, E, 2, 64, 1.1, 0.1, None) == MB_ERR_ALIGN
