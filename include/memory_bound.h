@@ -252,6 +252,15 @@ mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
                           int vec_per_thread);
 
 /*
+ * Launch overlap (default on): calls that move at most 128 MiB are launched
+ * with programmatic stream serialisation, so their launch and prologue overlap
+ * the tail of the previous kernel in the stream.  Every kernel of this library waits
+ * (griddepcontrol.wait) for the previous grid to complete before touching
+ * global memory, so results do not change.  enable 0 / 1; else MB_ERR_VALUE.
+ */
+mb_status mb_set_launch_overlap(int enable);
+
+/*
  * Process-wide override of the pointwise chain's launch shape, for tuning and
  * testing: blocks_per_sm (0 = as many as fit) and unroll, the 16-byte
  * fragments per input each thread keeps in flight (1, 2, 4 or 8; 0 = the

@@ -20,5 +20,5 @@ from ._binding import (  # noqa: F401
     ACTIVATIONS, MB_BF16, MB_F32, MB_MAX_COLS, MBError, ROW_PATHS, device_error,
     fused_add_relu_scale, fused_bias_relu_branch_mean_epilogue, fused_layernorm_act,
     fused_residual_layernorm_gelu, fused_row_softmax, library_path, load_library, raw, row_plan,
-    set_pointwise_shape, set_row_path, status_string,
+    set_launch_overlap, set_pointwise_shape, set_row_path, status_string,
 )

@@ -31,6 +31,7 @@ SIGNATURES = {
     "mb_device_error": (_I, [_U32P]),
     "mb_set_row_path": (_I, [_I, _I, _I, _I]),
     "mb_set_pointwise_shape": (_I, [_I, _I]),
+    "mb_set_launch_overlap": (_I, [_I]),
     "mb_row_plan": (_I, [_I, _I, _I64, _I64, _I, _I32P]),
 }
 
@@ -258,6 +259,11 @@ def set_row_path(path="auto", ctas_per_sm=0, stages=0, vec_per_thread=0):
     code = ROW_PATHS[path] if isinstance(path, str) else int(path)
     _check("mb_set_row_path", load_library().mb_set_row_path(code, ctas_per_sm, stages,
                                                              vec_per_thread))
+
+
+def set_launch_overlap(enable=True):
+    """Process-wide: launch with programmatic stream serialisation (default)."""
+    _check("mb_set_launch_overlap", load_library().mb_set_launch_overlap(int(bool(enable))))
 
 
 def set_pointwise_shape(blocks_per_sm=0, unroll=0):

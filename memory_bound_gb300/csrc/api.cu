@@ -30,6 +30,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 RowTuning g_tuning{MB_ROW_AUTO, 0, 0, 0};
+bool g_pdl = true;
 PointwiseTuning g_pw_tuning{0, 0};
 thread_local int g_last_cuda_error = 0;
 
@@ -53,7 +54,7 @@ mb_status device_ctx(cudaStream_t stream, LaunchCtx *ctx) {
             return cuda_fail(e);
         d.ready = true;
     }
-    *ctx = LaunchCtx{stream, dev, d.sm_count, d.smem_optin, d.smem_per_sm, d.dev_err};
+    *ctx = LaunchCtx{stream, dev, d.sm_count, d.smem_optin, d.smem_per_sm, d.dev_err, g_pdl};
     return MB_OK;
 }
 
@@ -80,6 +81,22 @@ mb_status check_rows(int64_t rows, int64_t cols) {
 }
 
 }  // namespace
+
+cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 block,
+                          void **args, size_t smem) {
+    if (!ctx.pdl) return cudaLaunchKernel(fn, grid, block, args, smem, ctx.stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
 
 mb_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
@@ -293,6 +310,13 @@ mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
         return MB_ERR_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);
     g_tuning = RowTuning{(int)path, ctas_per_sm, stages, vec_per_thread};
+    return MB_OK;
+}
+
+mb_status mb_set_launch_overlap(int enable) {
+    if (enable != 0 && enable != 1) return MB_ERR_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_pdl = enable != 0;
     return MB_OK;
 }
 

@@ -20,6 +20,21 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr unsigned kWaitLimitPolls = 1u << 28;
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Waits until the grid this launch depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) has completed
+// and its memory is visible; returns at once otherwise.  Every kernel calls it
+// before its first global memory access.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream begin launching (its CTAs start as ours
+// retire, and wait in pdl_wait for our completion).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // scalar fp32 helpers
 // ---------------------------------------------------------------------------
 

@@ -17,7 +17,18 @@ struct LaunchCtx {
     int smem_optin;        // max dynamic shared memory per block (opt-in)
     int smem_per_sm;       // shared memory per multiprocessor
     unsigned *dev_err;     // device-side failure flags of this device
+    bool pdl;              // launch with programmatic stream serialisation
 };
+
+// Launch overlap pays for calls whose launch latency is a visible share of
+// their run time; above this many bytes moved it is noise (measured on GB300:
+// +-1%), so those launches keep plain stream order.
+constexpr int64_t kOverlapMaxBytes = 128ll << 20;
+
+// cudaLaunchKernel, or cudaLaunchKernelEx with programmatic stream
+// serialisation when ctx.pdl (the kernels wait for their predecessor).
+cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 block,
+                          void **args, size_t smem);
 
 // Process-wide row-chain override (mb_set_row_path).
 struct RowTuning {

@@ -33,6 +33,8 @@ add_relu_scale_kernel(const T *__restrict__ x, const T *__restrict__ b1,
     using F = Frag<T, VEC>;
     using F1 = Frag<T, 1>;
     const int64_t body_end = head + nvec * VEC;
+    pdl_wait();
+    pdl_launch_dependents();
     if (blockIdx.x == 0) {
         const int t = threadIdx.x;
         const int64_t tail = n - body_end;
@@ -120,7 +122,9 @@ mb_status launch(const LaunchCtx &ctx, const PointwiseTuning &tun, const void *x
             *p2 = static_cast<const T *>(b2);
     T *py = static_cast<T *>(y);
     void *args[] = {&px, &p1, &p2, &py, &n, &head, &nvec, &chunk, &scale};
-    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kThreads), args, 0, ctx.stream);
+    LaunchCtx lctx = ctx;
+    lctx.pdl = ctx.pdl && n * (int64_t)sizeof(T) * 4 <= kOverlapMaxBytes;
+    e = launch_kernel(lctx, fn, dim3((unsigned)grid), dim3(kThreads), args, 0);
     if (e != cudaSuccess) return cuda_fail(e);
     return MB_OK;
 }

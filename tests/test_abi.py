@@ -104,6 +104,12 @@ def test_row_path_setter_validates(lib):
     assert lib.mb_set_row_path(0, 0, 0, 0) == MB_OK
 
 
+def test_launch_overlap_setter_validates(lib):
+    assert lib.mb_set_launch_overlap(2) == MB_ERR_VALUE
+    assert lib.mb_set_launch_overlap(0) == MB_OK
+    assert lib.mb_set_launch_overlap(1) == MB_OK
+
+
 def test_pointwise_shape_setter_validates(lib):
     assert lib.mb_set_pointwise_shape(-1, 0) == MB_ERR_VALUE
     assert lib.mb_set_pointwise_shape(0, 3) == MB_ERR_VALUE
