@@ -69,6 +69,15 @@ __device__ __forceinline__ float gelu_tanh_f(float n) {
     return n * rcp_approx(1.0f + e);
 }
 
+// Pairs of fp32 values through Blackwell's packed fp32x2 instructions: each
+// lane is an ordinary IEEE fp32 operation rounded to nearest, so results are
+// the same as two scalar operations, at half the instruction issue.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 relu2(float2 a) { return make_float2(relu_f(a.x), relu_f(a.y)); }
+
 // ---------------------------------------------------------------------------
 // bf16 packing (raw 16-bit patterns, little-endian pairs in 32-bit words)
 // ---------------------------------------------------------------------------

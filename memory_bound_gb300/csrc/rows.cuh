@@ -4,8 +4,8 @@
 //   pre   (per element)   the pointwise prologue, giving v from the row inputs
 //                         and the per-column values it needs (PrePC)
 //   s1    = C::stat1(R1, cols, args), R1 = sum(v), or max(v) with C::kMaxFirst
-//   s2    = C::stat2(R2, cols, args) with C::kTwoPass, where R2 sums the terms
-//           C::p2 forms from each v and s1 (p2 may also rewrite v in place)
+//   s2    = C::stat2(R2, cols, args) with C::kTwoPass, where R2 sums the
+//           per-slot partials C::p2 forms from v and s1 (p2 may rewrite v)
 //   post  (per element)   the epilogue from v, s1, s2 and its per-column
 //                         values (PostPC)
 // and, with C::kStorePre, store_pre writes the prologue value v out as well
@@ -49,11 +49,13 @@ __device__ __forceinline__ float fold1(float acc, const float (&v)[VEC], bool va
 #pragma unroll
         for (int e = 1; e < VEC; ++e) m = fmaxf(m, v[e]);
         return valid ? fmaxf(acc, m) : acc;
+    } else if constexpr (VEC == 1) {
+        return acc + (valid ? v[0] : 0.0f);
     } else {
-        float part = 0.0f;
+        float2 p = make_float2(v[0], v[1]);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) part += v[e];
-        return acc + (valid ? part : 0.0f);
+        for (int e = 2; e < VEC; e += 2) p = add2(p, make_float2(v[e], v[e + 1]));
+        return acc + (valid ? p.x + p.y : 0.0f);
     }
 }
 
@@ -103,9 +105,7 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             float l2 = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
-                float part = 0.0f;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) part = C::p2(v[k][e], mean, part);
+                const float part = C::template p2<VEC>(v[k], mean);
                 l2 += lane + 32 * k < nvec ? part : 0.0f;
             }
             rstd = C::stat2(warp_sum(l2), cols, a);
@@ -237,9 +237,7 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             float l2 = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                float part = 0.0f;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) part = C::p2(v[k][e], mean, part);
+                const float part = C::template p2<VEC>(v[k], mean);
                 l2 += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
             }
             rstd = C::stat2(block_sum(l2, red + 32 * rb), cols, a);
