@@ -2,7 +2,8 @@
 
     python -m memory_bound_gb300.profile_case ln_bf16 8192 8192 --iters 3
 
-Chains: pointwise_f32, pointwise_bf16, inductor_f32, ln_f32, ln_bf16.
+Chains: pointwise_f32, pointwise_bf16, inductor_f32, ln_f32, ln_bf16,
+softmax_f32, softmax_bf16.
 Inputs are seeded synthetic tensors from synth; nothing is checked here (the
 tests do that).  Keep ncu captures small: a few hundred MB on the device.
 """
@@ -53,6 +54,10 @@ def main(argv=None):
         bias, gamma, beta = t(1, (a.cols,), 0, 0.1), t(2, (a.cols,), 0.5, 1.5, True), t(3, (a.cols,), 0, 0.1)
         out = torch.empty_like(x)
         run = lambda: mb.fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, 1.1, 0.1, out=out)
+    elif a.chain.startswith("softmax"):
+        x = t(0, (a.rows, a.cols))
+        out = torch.empty_like(x)
+        run = lambda: mb.fused_row_softmax(x, out=out)
     else:
         x, r = t(0, (a.rows, a.cols)), t(1, (a.rows, a.cols))
         w, b = t(2, (a.cols,), 0.5, 1.5, True), t(3, (a.cols,), 0, 0.1)
@@ -61,7 +66,9 @@ def main(argv=None):
     for _ in range(a.iters):
         run()
     torch.cuda.synchronize()
-    print("plan:", mb.row_plan("ln" if a.chain.startswith("ln") else "inductor", dt, a.rows, a.cols)
+    kind = ("ln" if a.chain.startswith("ln") else
+            "softmax" if a.chain.startswith("softmax") else "inductor")
+    print("plan:", mb.row_plan(kind, dt, a.rows, a.cols)
           if not a.chain.startswith("pointwise") else "pointwise")
 
 
