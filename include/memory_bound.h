@@ -68,8 +68,10 @@ extern "C" {
 
 #define MB_ABI_VERSION 1
 
-/* Longest row (cols / hidden) the row chains accept. */
-#define MB_MAX_COLS 32768
+/* Longest row (cols / hidden) the row chains accept.  Rows longer than one
+ * CTA can hold (32768 elements) are spread over a thread-block cluster of up
+ * to 16 CTAs. */
+#define MB_MAX_COLS 524288
 
 typedef enum mb_status {
     MB_OK = 0,
@@ -234,19 +236,23 @@ typedef enum mb_row_path {
     MB_ROW_AUTO = 0,     /* choose by shape and alignment (default)            */
     MB_ROW_WARP = 1,     /* one warp per row, row in registers                */
     MB_ROW_DIRECT = 2,   /* one CTA per row, vector loads into registers      */
-    MB_ROW_STAGED = 3    /* one CTA per row, rows staged into shared memory by
+    MB_ROW_STAGED = 3,   /* one CTA per row, rows staged into shared memory by
                             bulk async copies in a multi-stage ring            */
+    MB_ROW_CLUSTER = 4   /* one thread-block cluster per row: each CTA holds a
+                            slice, statistics combined through distributed
+                            shared memory (automatic above 32768 elements)    */
 } mb_row_path;
 
 /*
  * Process-wide override of the row-chain path and launch shape, for tuning
  * and testing.  ctas_per_sm (CTAs resident per SM), stages (ring depth of the
- * staged path) and vec_per_thread (16-byte vectors each thread holds per row
+ * staged path; CTAs per row, 2..16, on the cluster path) and vec_per_thread (16-byte vectors each thread holds per row
  * on the CTA paths; a power of two) of 0 mean "choose automatically"; a
  * value that cannot serve a shape is ignored.  A forced path that cannot
  * serve a shape (MB_ROW_WARP beyond 256 vectors per row, MB_ROW_STAGED on
- * unaligned rows or rows too long for one stage) falls back to the automatic
- * choice.  Returns MB_ERR_VALUE on a bad code or a negative count.
+ * unaligned rows or rows too long for one stage, one-CTA paths on rows longer
+ * than one CTA holds) falls back to the automatic choice.  Returns
+ * MB_ERR_VALUE on a bad code or a negative count.
  */
 mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
                           int vec_per_thread);
@@ -272,7 +278,8 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * The launch the row chains would use for a shape, without launching:
  * out[0] = path (mb_row_path), out[1] = threads per CTA, out[2] = CTAs,
  * out[3] = values per thread slot (vectors per thread), out[4] = vector width
- * in elements, out[5] = ring stages (staged path, else 0),
+ * in elements, out[5] = ring stages (staged path), CTAs per row (cluster
+ * path), else 0,
  * out[6] = dynamic shared memory bytes.  `chain`: 0 residual + LayerNorm +
  * GeLU, 1 the TorchInductor chain, 2 the LayerNorm family with a residual,
  * 3 without, 4 row softmax.  `aligned` says whether every pointer is 16-byte

@@ -6,8 +6,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(HERE, "libmemory_bound.so")
 
 MB_F32, MB_BF16 = 0, 1
-MB_MAX_COLS = 32768
-ROW_PATHS = {"auto": 0, "warp": 1, "direct": 2, "staged": 3}
+MB_MAX_COLS = 524288
+ROW_PATHS = {"auto": 0, "warp": 1, "direct": 2, "staged": 3, "cluster": 4}
 ACTIVATIONS = {"none": 0, "relu": 1, "gelu_tanh": 2}
 
 STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_NULL", 2: "MB_ERR_SHAPE", 3: "MB_ERR_DTYPE",

@@ -83,18 +83,29 @@ mb_status check_rows(int64_t rows, int64_t cols) {
 }  // namespace
 
 cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 block,
-                          void **args, size_t smem) {
-    if (!ctx.pdl) return cudaLaunchKernel(fn, grid, block, args, smem, ctx.stream);
+                          void **args, size_t smem, int cluster) {
+    if (!ctx.pdl && cluster <= 1) return cudaLaunchKernel(fn, grid, block, args, smem, ctx.stream);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (ctx.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -305,7 +316,7 @@ mb_status mb_device_error(uint32_t *flags) {
 
 mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
                           int vec_per_thread) {
-    if (path < MB_ROW_AUTO || path > MB_ROW_STAGED || ctas_per_sm < 0 || stages < 0 ||
+    if (path < MB_ROW_AUTO || path > MB_ROW_CLUSTER || ctas_per_sm < 0 || stages < 0 ||
         vec_per_thread < 0)
         return MB_ERR_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);

@@ -28,7 +28,7 @@ constexpr int64_t kOverlapMaxBytes = 128ll << 20;
 // cudaLaunchKernel, or cudaLaunchKernelEx with programmatic stream
 // serialisation when ctx.pdl (the kernels wait for their predecessor).
 cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 block,
-                          void **args, size_t smem);
+                          void **args, size_t smem, int cluster = 1);
 
 // Process-wide row-chain override (mb_set_row_path).
 struct RowTuning {
@@ -47,6 +47,7 @@ struct PointwiseTuning {
 // The launch a row chain uses (mb_row_plan reports it).
 struct RowPlan {
     int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
+    int slice = 0;     // cluster path: vectors of the row each CTA holds
 };
 
 // Chains implemented in their own translation units.  `launch == false`

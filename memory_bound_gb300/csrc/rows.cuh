@@ -29,6 +29,8 @@
 // loads overlap the others' reductions and epilogues.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -39,6 +41,7 @@ constexpr int kWarpBlock = 256;
 constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
 constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
+constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
 
 // Folds one slot's VEC values into the running first-pass partial (a sum, or a
 // maximum with C::kMaxFirst); slots past the row end leave it unchanged.
@@ -282,6 +285,128 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
 }
 
 // ---------------------------------------------------------------------------
+// one thread-block cluster per row (rows longer than one CTA can hold)
+// ---------------------------------------------------------------------------
+
+// Sum (or maximum) of one value per CTA over the cluster.  `xch` is this
+// CTA's pair of exchange slots (alternated between reductions, as block_sum's
+// buffers are); thread 0 publishes, the cluster barrier orders it, and every
+// thread reads the cluster's slots in rank order, so all CTAs get the
+// bitwise-same result.
+template <bool MAX>
+__device__ __forceinline__ float cluster_reduce(float v, float *xch,
+                                                cooperative_groups::cluster_group &cl) {
+    if (threadIdx.x == 0) *xch = v;
+    cl.sync();
+    const unsigned n = cl.num_blocks();
+    float r = MAX ? -INFINITY : 0.0f;
+    for (unsigned j = 0; j < n; ++j) {
+        const float p = *cl.map_shared_rank(xch, j);
+        r = MAX ? fmaxf(r, p) : r + p;
+    }
+    return r;
+}
+
+// The cluster of CS CTAs owns rows c, c + nclusters, ...; CTA `rank` holds the
+// columns [rank * slice, (rank + 1) * slice) of each of them in registers.
+// Direct vector loads, the next row's issued as soon as the current row has
+// left the input registers; the two statistics combine CTA partials through
+// distributed shared memory.
+template <class C, int VPT, int VEC>
+__global__ void __launch_bounds__(kCtaMaxThreads, 1)
+rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *) {
+    namespace cg = cooperative_groups;
+    using T = typename C::T;
+    constexpr int NIN = C::kInputs;
+    constexpr bool kEarlyPost = VPT * VEC * C::kPostPC <= 8;
+    using PrePC = typename C::template PrePC<VEC>;
+    using PostPC = typename C::template PostPC<VEC>;
+    __shared__ float red[2][32];
+    __shared__ float xch[2];
+    cg::cluster_group cl = cg::this_cluster();
+    const int tid = threadIdx.x;
+    const int rank = (int)cl.block_rank();
+    const int64_t nclusters = gridDim.x / cl.num_blocks();
+    const int64_t cid = blockIdx.x / cl.num_blocks();
+    const int lo = rank * slice;                               // first column of this CTA
+    const int hi = lo + slice < cols ? lo + slice : cols;
+    const int nvec = hi > lo ? (hi - lo) / VEC : 0;            // vectors this CTA holds
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // Loads of one row's slice (and of its per-column values); the planner
+    // leaves no rank empty, and indices stay in bounds regardless.
+    PrePC pre[VPT];
+    PostPC post[kEarlyPost ? VPT : 1];
+    Frag<T, VEC> in[VPT][NIN];
+    auto load_row = [&](int64_t r) {
+        if (nvec == 0) return;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
+            C::template load_pre<VEC>(a, lo + vc * VEC, pre[k]);
+            if constexpr (kEarlyPost) C::template load_post<VEC>(a, lo + vc * VEC, post[k]);
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) in[k][i].load_stream(a.in[i] + r * cols + lo + vc * VEC);
+        }
+    };
+    if (cid < rows) load_row(cid);
+
+    int rb = 0, xb = 0;
+    for (int64_t row = cid; row < rows; row += nclusters) {
+        const int64_t base = row * cols + lo;
+        float v[VPT][VEC];
+        float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vi = tid + k * (int)blockDim.x;
+            C::template pre<VEC>(in[k], pre[k], a, v[k]);
+            l1 = fold1<C, VEC>(l1, v[k], vi < nvec);
+            if constexpr (C::kStorePre) {
+                if (vi < nvec) C::template store_pre<VEC>(v[k], a, base + vi * VEC);
+            }
+        }
+        // The input registers are free now: the next row's loads stay in
+        // flight through this row's reductions, cluster barriers and epilogue.
+        if (row + nclusters < rows) load_row(row + nclusters);
+        const float c1 = C::kMaxFirst ? block_max(l1, red[rb]) : block_sum(l1, red[rb]);
+        rb ^= 1;
+        const float r1 = cluster_reduce<C::kMaxFirst>(c1, &xch[xb], cl);
+        xb ^= 1;
+        const float mean = C::stat1(r1, cols, a);
+        float rstd = 0.0f;
+        if constexpr (C::kTwoPass) {
+            float l2 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const float part = C::template p2<VEC>(v[k], mean);
+                l2 += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
+            }
+            const float c2 = block_sum(l2, red[rb]);
+            rb ^= 1;
+            rstd = C::stat2(cluster_reduce<false>(c2, &xch[xb], cl), cols, a);
+            xb ^= 1;
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vi = tid + k * blockDim.x;
+            if (vi < nvec) {
+                Frag<T, VEC> o;
+                if constexpr (kEarlyPost) {
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, o.f);
+                } else {
+                    PostPC pc;
+                    C::template load_post<VEC>(a, lo + vi * VEC, pc);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, o.f);
+                }
+                o.store_stream(a.out + base + vi * VEC);
+            }
+        }
+    }
+    cl.sync();     // no CTA leaves while another may still read its slots
+}
+
+// ---------------------------------------------------------------------------
 // host-side planning and launch
 // ---------------------------------------------------------------------------
 
@@ -351,6 +476,100 @@ template <class C> struct RowEngine {
         return nullptr;
     }
 
+    static const void *cluster_fn(int vpt, bool vec) {
+        if (vec) {
+            switch (vpt) {
+                case 1: return (const void *)rows_cluster_kernel<C, 1, kVecN>;
+                case 2: return (const void *)rows_cluster_kernel<C, 2, kVecN>;
+                case 4: return (const void *)rows_cluster_kernel<C, 4, kVecN>;
+                case 8: if constexpr (kVecN == 4) return (const void *)rows_cluster_kernel<C, 8, kVecN>;
+                        break;
+            }
+        } else {
+            switch (vpt) {
+                case 1: return (const void *)rows_cluster_kernel<C, 1, 1>;
+                case 2: return (const void *)rows_cluster_kernel<C, 2, 1>;
+                case 4: return (const void *)rows_cluster_kernel<C, 4, 1>;
+                case 8: return (const void *)rows_cluster_kernel<C, 8, 1>;
+                case 16: return (const void *)rows_cluster_kernel<C, 16, 1>;
+                case 32: return (const void *)rows_cluster_kernel<C, 32, 1>;
+            }
+        }
+        return nullptr;
+    }
+
+    // Resident clusters of `fn` with `cs` CTAs of `threads` threads (0 if none fit).
+    static mb_status active_clusters(const LaunchCtx &ctx, const void *fn, int cs, int threads,
+                                     int *n) {
+        cudaError_t e = cudaSuccess;
+        if (cs > 8)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs * ctx.sm_count);
+        cfg.blockDim = dim3(threads);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(n, fn, &cfg);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();   // an unplaceable shape is not an error here
+            *n = 0;
+        }
+        return MB_OK;
+    }
+
+    // One cluster of `cs` CTAs per row.  Each resident cluster keeps one row
+    // in flight, so among cluster sizes 2, 4, 8, 16 (or the requested one) and
+    // the vectors-per-thread that fit a slice in one CTA, take the launch with
+    // the most resident clusters (ties: the larger cluster); no rank is empty.
+    static mb_status plan_cluster(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows,
+                                  int nvec, bool vec, RowPlan *p, const void **fn) {
+        int best_n = 0, best_cs = 0, best_vpt = 0, best_threads = 0, best_slice = 0;
+        for (int cs0 : {2, 4, 8, 16}) {
+            int cs = cs0;
+            if (tun.stages >= 2 && tun.stages <= kMaxCluster) {
+                if (cs0 != 2) continue;
+                cs = tun.stages;
+            }
+            if (cs > nvec) cs = nvec;
+            const int slice_v = ceil_div(nvec, cs);
+            cs = ceil_div(nvec, slice_v);                  // no empty rank
+            if (cs < 2) continue;
+            for (int vpt = 1; vpt <= max_vpt(vec); vpt *= 2) {
+                if (tun.vpt > 0 && vpt != tun.vpt) continue;
+                if (ceil_div(slice_v, vpt) > kCtaMaxThreads) continue;
+                const int threads = round_up32(ceil_div(slice_v, vpt));
+                const void *f = cluster_fn(vpt, vec);
+                if (!f) continue;
+                int n = 0;
+                mb_status st = active_clusters(ctx, f, cs, threads, &n);
+                if (st != MB_OK) return st;
+                if (n > best_n || (n == best_n && n > 0 && cs > best_cs)) {
+                    best_n = n; best_cs = cs; best_vpt = vpt; best_threads = threads;
+                    best_slice = slice_v;
+                }
+            }
+        }
+        if (!best_n && tun.vpt > 0) {
+            RowTuning t2 = tun;
+            t2.vpt = 0;
+            return plan_cluster(ctx, t2, rows, nvec, vec, p, fn);
+        }
+        if (!best_n) return MB_ERR_SHAPE;
+        *fn = cluster_fn(best_vpt, vec);
+        const int64_t ncl = rows < best_n ? rows : best_n;
+        p->path = MB_ROW_CLUSTER; p->threads = best_threads; p->vpt = best_vpt;
+        p->stages = best_cs; p->smem = 0;
+        p->ctas = (int)(ncl * best_cs);
+        p->slice = best_slice;
+        return MB_OK;
+    }
+
     // CTAs of `fn` resident per SM with `threads` threads and `smem` bytes.
     static mb_status occupancy(const LaunchCtx &ctx, const void *fn, int threads, int smem,
                                int *occ) {
@@ -369,13 +588,18 @@ template <class C> struct RowEngine {
         const int stage_bytes = C::kInputs * cols * (int)sizeof(T);
         const bool stage_fits = kHdrBytes + stage_bytes <= ctx.smem_optin;
 
+        const bool one_cta = nvec <= kCtaMaxThreads * max_vpt(vec);
         int path = tun.path;
         if (path == MB_ROW_WARP && !warp_ok) path = MB_ROW_AUTO;
-        if (path == MB_ROW_STAGED && (!vec || !stage_fits)) path = MB_ROW_AUTO;
+        if (path == MB_ROW_STAGED && (!vec || !stage_fits || !one_cta)) path = MB_ROW_AUTO;
+        if (path == MB_ROW_DIRECT && !one_cta) path = MB_ROW_AUTO;
+        if (path == MB_ROW_CLUSTER && nvec < 2) path = MB_ROW_AUTO;
         if (path == MB_ROW_AUTO)
-            path = warp_ok ? MB_ROW_WARP : (vec && stage_fits ? MB_ROW_STAGED : MB_ROW_DIRECT);
+            path = !one_cta ? MB_ROW_CLUSTER
+                 : warp_ok ? MB_ROW_WARP : (vec && stage_fits ? MB_ROW_STAGED : MB_ROW_DIRECT);
 
         p->vec = VEC;
+        if (path == MB_ROW_CLUSTER) return plan_cluster(ctx, tun, rows, nvec, vec, p, fn);
         if (path == MB_ROW_WARP) {
             int vpl = 1;
             while (vpl * 32 < nvec) vpl *= 2;
@@ -479,10 +703,12 @@ template <class C> struct RowEngine {
         typename C::Args args = a;
         int64_t rows_arg = rows;
         int cols_arg = cols;
-        int stages_arg = p.stages > 0 ? p.stages : 1;
+        // the fourth kernel argument: ring depth, or the cluster's slice length
+        int stages_arg = p.path == MB_ROW_CLUSTER ? p.slice * p.vec : (p.stages > 0 ? p.stages : 1);
         unsigned *err = ctx.dev_err;
         void *kargs[] = {&args, &rows_arg, &cols_arg, &stages_arg, &err};
-        cudaError_t e = launch_kernel(lctx, fn, dim3(p.ctas), dim3(p.threads), kargs, p.smem);
+        cudaError_t e = launch_kernel(lctx, fn, dim3(p.ctas), dim3(p.threads), kargs, p.smem,
+                                      p.path == MB_ROW_CLUSTER ? p.stages : 1);
         if (e != cudaSuccess) return cuda_fail(e);
         return MB_OK;
     }

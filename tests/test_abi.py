@@ -98,6 +98,8 @@ def test_inductor_argument_checks(lib):
 
 def test_row_path_setter_validates(lib):
     assert lib.mb_set_row_path(9, 0, 0, 0) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(5, 0, 0, 0) == MB_ERR_VALUE
+    assert lib.mb_set_row_path(4, 0, 8, 0) == MB_OK          # cluster path
     assert lib.mb_set_row_path(0, -1, 0, 0) == MB_ERR_VALUE
     assert lib.mb_set_row_path(0, 0, 0, -2) == MB_ERR_VALUE
     assert lib.mb_set_row_path(3, 2, 4, 1) == MB_OK

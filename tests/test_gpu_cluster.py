@@ -1,0 +1,92 @@
+"""Rows longer than one CTA holds (more than 32768 elements), spread over a
+thread-block cluster whose CTAs combine their partial statistics through
+distributed shared memory; and the cluster path forced on ordinary rows with
+explicit cluster sizes.  Every chain, against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_gb300 as mb
+import oracle
+import synth
+
+from gpu_util import assert_bitexact, assert_close, check_guard, guarded_empty, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    from memory_bound_gb300 import build as lib_build
+    lib_build.build()
+    torch.cuda.set_device(0)
+    mb.set_row_path("auto")
+    yield
+    mb.set_row_path("auto")
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+
+
+@pytest.fixture
+def row_path():
+    yield mb.set_row_path
+    mb.set_row_path("auto")
+
+
+def _ln(rows, cols, seed, bf16):
+    dt = "bf16" if bf16 else "f32"
+    return (synth.normal(seed, 0, (rows, cols), dtype=dt), synth.normal(seed, 1, (rows, cols), dtype=dt),
+            synth.uniform(seed, 2, (cols,), 0.5, 1.5, dtype=dt),
+            synth.normal(seed, 3, (cols,), 0.0, 0.1, dtype=dt))
+
+
+def _check_chains(rows, cols, seed, bf16):
+    dt = torch.bfloat16 if bf16 else torch.float32
+    x, r, w, b = _ln(rows, cols, seed, bf16)
+    buf, out = guarded_empty((rows, cols), dt)
+    mb.fused_residual_layernorm_gelu(to_dev(x, bf16), to_dev(r, bf16), to_dev(w, bf16),
+                                     to_dev(b, bf16), 1e-5, out=out)
+    assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5), bf16=bf16,
+                 what=f"LN {rows}x{cols}")
+    check_guard(buf)
+    out, h = mb.fused_layernorm_act(to_dev(x, bf16), to_dev(w, bf16), to_dev(b, bf16),
+                                    r=to_dev(r, bf16), act="relu", want_h=True)
+    want, want_h = oracle.layernorm_act(x, r, w, b, 1e-5, oracle.ACT_RELU, want_h=True)
+    assert_close(to_host(out), want, bf16=bf16, what="LN relu")
+    assert_bitexact(to_host(h), want_h, "h")
+    y = to_host(mb.fused_row_softmax(to_dev(x, bf16)))
+    ws = oracle.row_softmax(x)
+    g = (y.astype(np.uint32) << 16).view(np.float32) if bf16 else y
+    wf = (ws.astype(np.uint32) << 16).view(np.float32) if bf16 else ws
+    rtol = 1e-2 if bf16 else 1e-5
+    assert np.all(np.abs(g.astype(np.float64) - wf) <= rtol * np.abs(wf) + 2.0 ** -126), "softmax"
+    bias = synth.normal(seed, 4, (cols,), 0.0, 0.1, dtype="bf16" if bf16 else "f32")
+    yi = mb.fused_bias_relu_branch_mean_epilogue(to_dev(x, bf16), to_dev(bias, bf16), to_dev(w, bf16),
+                                                 to_dev(b, bf16), 1.1, 0.1)
+    want = (oracle.bias_relu_branch_mean_epilogue_bf16 if bf16 else
+            oracle.bias_relu_branch_mean_epilogue)(x, bias, w, b, 1.1, 0.1)
+    assert_close(to_host(yi), want, bf16=bf16, what="inductor")
+
+
+@pytest.mark.parametrize("cols", [32769, 40000, 65536, 131072, 262144, 524288])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_long_rows(cols, bf16):
+    rows = 3 if cols > 131072 else 5
+    assert mb.row_plan("ln", "bf16" if bf16 else "f32", rows, cols)["path"] == "cluster"
+    _check_chains(rows, cols, 3000 + cols % 997, bf16)
+
+
+@pytest.mark.parametrize("cs", [2, 3, 5, 8, 16])
+@pytest.mark.parametrize("shape", [(7, 4096), (4, 1000), (9, 33), (300, 2048)])
+def test_forced_cluster_sizes(cs, shape, row_path):
+    row_path("cluster", 0, cs)
+    rows, cols = shape
+    _check_chains(rows, cols, 4000 + cs * 31 + cols, False)
+
+
+def test_long_rows_many_rows_and_unaligned():
+    """More rows than clusters fit at once (each cluster loops over rows), and
+    an unaligned scalar row length."""
+    _check_chains(700, 40000, 5001, True)
+    _check_chains(6, 33333, 5002, False)
