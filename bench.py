@@ -222,7 +222,7 @@ class Case:
         elif self.w.chain == "softmax":
             mb.fused_row_softmax(d["x"], out=out)
         elif self.w.chain == "lnact":
-            mb.fused_layernorm_act(d["x"], d["w"], d["b"], r=d.get("r"), eps=p["eps"],
+            mb.fused_layernorm_act(d["x"], d.get("r"), d["w"], d["b"], eps=p["eps"],
                                    act=p["act"], out=out,
                                    h_out=self.houts[k % self.nsets] if p["write_h"] else None)
         else:

@@ -10,7 +10,7 @@ fallback of any kind, and calling a chain without the built library raises.
     fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None)
     fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta,
                                          x_scale=1.1, branch_scale=0.1, out=None)
-    fused_layernorm_act(x, w, b, r=None, eps=1e-5, act="gelu_tanh", want_h=False)
+    fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", want_h=False)   # r may be None
     fused_row_softmax(x, out=None)
 
 ``raw`` exposes the C entry points themselves (plain integers for pointers

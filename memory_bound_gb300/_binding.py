@@ -120,6 +120,25 @@ def _stream_handle(t):
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
+class _NoSwitch:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NO_SWITCH = _NoSwitch()
+
+
+def _on_device(t):
+    """Make t's device current for the call (a no-op when it already is)."""
+    torch = _torch()
+    if t.device.index == torch.cuda.current_device():
+        return _NO_SWITCH
+    return torch.cuda.device(t.device)
+
+
 def _require(tensors, dtype):
     for t in tensors:
         if not t.is_cuda:
@@ -140,7 +159,7 @@ def fused_add_relu_scale(x, b1, b2, scale=0.5, out=None):
     _require([x, b1, b2, out], x.dtype)
     if not (x.numel() == b1.numel() == b2.numel() == out.numel()):
         raise ValueError("x, b1, b2 and out must have one size")
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = load_library().fused_add_relu_scale(
             x.data_ptr(), b1.data_ptr(), b2.data_ptr(), out.data_ptr(), x.numel(),
             float(scale), _dtype_code(x), _stream_handle(x))
@@ -166,7 +185,7 @@ def fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
             raise ValueError("per-column vectors must have cols elements")
     if out.numel() != x.numel():
         raise ValueError("out must match x")
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = getattr(load_library(), fn_name)(
             x.data_ptr(), bias.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
             out.data_ptr(), rows, cols, float(x_scale), float(branch_scale),
@@ -188,7 +207,7 @@ def fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None):
         raise ValueError("shape mismatch")
     if out.numel() != x.numel():
         raise ValueError("out must match x")
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = load_library().fused_residual_layernorm_gelu(
             x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(),
             rows, hidden, float(eps), _dtype_code(x), _stream_handle(x))
@@ -196,9 +215,10 @@ def fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None):
     return out
 
 
-def fused_layernorm_act(x, w, b, r=None, eps=1e-5, act="gelu_tanh", out=None, h_out=None,
+def fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", out=None, h_out=None,
                         want_h=False):
-    """act(LayerNorm(x (+ r)) * w + b) over the last dim of a 2-D x.  With
+    """act(LayerNorm(x (+ r)) * w + b) over the last dim of a 2-D x; r may be
+    None (no residual).  With
     ``want_h`` (or an ``h_out`` tensor) also writes h = x + r (or x), the
     residual stream; returns (out, h) then, else out."""
     torch = _torch()
@@ -217,7 +237,7 @@ def fused_layernorm_act(x, w, b, r=None, eps=1e-5, act="gelu_tanh", out=None, h_
         if t is not None and t.numel() != x.numel():
             raise ValueError("outputs must match x")
     code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = load_library().fused_layernorm_act(
             x.data_ptr(), r.data_ptr() if r is not None else None, w.data_ptr(), b.data_ptr(),
             out.data_ptr(), h_out.data_ptr() if h_out is not None else None, rows, hidden,
@@ -237,7 +257,7 @@ def fused_row_softmax(x, out=None):
     if out.numel() != x.numel():
         raise ValueError("out must match x")
     rows, cols = x.shape
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = load_library().fused_row_softmax(x.data_ptr(), out.data_ptr(), rows, cols,
                                               _dtype_code(x), _stream_handle(x))
     _check("fused_row_softmax", st)

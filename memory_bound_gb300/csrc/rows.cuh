@@ -29,6 +29,8 @@
 // loads overlap the others' reductions and epilogues.
 #pragma once
 
+#include <mutex>
+
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -42,6 +44,7 @@ constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
 constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
+constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
 // Folds one slot's VEC values into the running first-pass partial (a sum, or a
 // maximum with C::kMaxFirst); slots past the row end leave it unchanged.
@@ -567,6 +570,7 @@ template <class C> struct RowEngine {
         p->stages = best_cs; p->smem = 0;
         p->ctas = (int)(ncl * best_cs);
         p->slice = best_slice;
+        p->cap = best_n;
         return MB_OK;
     }
 
@@ -579,8 +583,84 @@ template <class C> struct RowEngine {
         return MB_OK;
     }
 
+    // The occupancy-derived part of a plan depends on the device, the row
+    // length, the alignment and the tuning, not on the row count: it is
+    // computed once (for an unbounded row count) and kept here; each call
+    // only sizes the grid for its rows.
+    struct CacheEntry {
+        bool used;
+        int device, cols, aligned, path, ctas_per_sm, stages, vpt;
+        RowPlan core;
+        const void *fn;
+    };
+    static constexpr int kCacheSize = 64;
+    struct PlanCache {
+        std::mutex mu;
+        CacheEntry entries[kCacheSize] = {};
+        int next = 0;
+    };
+    static PlanCache &plan_cache() {
+        static PlanCache c;      // one per chain type, built on first use
+        return c;
+    }
+
     static mb_status plan(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows, int cols,
                           bool aligned, RowPlan *p, const void **fn) {
+        RowPlan core;
+        const void *f = nullptr;
+        bool hit = false;
+        PlanCache &pc = plan_cache();
+        {
+            std::lock_guard<std::mutex> lock(pc.mu);
+            for (const CacheEntry &e : pc.entries) {
+                if (e.used && e.device == ctx.device && e.cols == cols && e.aligned == (int)aligned &&
+                    e.path == tun.path && e.ctas_per_sm == tun.ctas_per_sm &&
+                    e.stages == tun.stages && e.vpt == tun.vpt) {
+                    core = e.core;
+                    f = e.fn;
+                    hit = true;
+                    break;
+                }
+            }
+        }
+        if (!hit) {
+            mb_status st = plan_full(ctx, tun, kUnboundedRows, cols, aligned, &core, &f);
+            if (st != MB_OK) return st;
+            std::lock_guard<std::mutex> lock(pc.mu);
+            pc.entries[pc.next] = CacheEntry{true, ctx.device, cols, (int)aligned, tun.path,
+                                             tun.ctas_per_sm, tun.stages, tun.vpt, core, f};
+            pc.next = (pc.next + 1) % kCacheSize;
+        }
+        *p = core;
+        *fn = f;
+        if (core.path == MB_ROW_WARP) {
+            // Few rows: smaller blocks, so the rows spread over every SM
+            // (at least two blocks per SM when the rows allow it).
+            int threads = kWarpBlock;
+            while (threads > 32 && (rows + threads / 32 - 1) / (threads / 32) < 2 * ctx.sm_count)
+                threads /= 2;
+            const int64_t cap = core.cap * (kWarpBlock / threads);
+            const int64_t want = (rows + threads / 32 - 1) / (threads / 32);
+            p->threads = threads;
+            p->ctas = (int)(want < cap ? want : cap);
+        } else if (core.path == MB_ROW_CLUSTER) {
+            const int64_t ncl = rows < core.cap ? rows : core.cap;
+            p->ctas = (int)(ncl * core.stages);
+        } else {
+            // Balanced grid: as many row rounds as the full grid needs, but
+            // only as many CTAs as those rounds need.
+            int64_t grid = rows < core.cap ? rows : core.cap;
+            if (grid > 0) {
+                const int64_t rounds = (rows + grid - 1) / grid;
+                grid = (rows + rounds - 1) / rounds;
+            }
+            p->ctas = (int)grid;
+        }
+        return MB_OK;
+    }
+
+    static mb_status plan_full(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows, int cols,
+                               bool aligned, RowPlan *p, const void **fn) {
         const bool vec = aligned && (cols % kVecN) == 0;
         const int VEC = vec ? kVecN : 1;
         const int nvec = cols / VEC;
@@ -609,6 +689,7 @@ template <class C> struct RowEngine {
             if (st != MB_OK) return st;
             if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
             if (occ < 1) occ = 1;
+            p->cap = (int64_t)occ * ctx.sm_count;
             // Few rows: smaller blocks, so the rows spread over every SM
             // (at least two blocks per SM when the rows allow it).
             int threads = kWarpBlock;
@@ -676,6 +757,7 @@ template <class C> struct RowEngine {
         if (occ2 < occ) occ = occ2;
         if (occ < 1) occ = 1;
         const int64_t cap = (int64_t)occ * ctx.sm_count;
+        p->cap = cap;
         // Balanced grid: as many row rounds as the full grid needs, but only
         // as many CTAs as those rounds need, so the last round is not mostly
         // idle (8192 rows on 608 slots: 14 rounds on 586 CTAs, not 13.5 on 608).

@@ -50,8 +50,8 @@ def _check_chains(rows, cols, seed, bf16):
     assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5), bf16=bf16,
                  what=f"LN {rows}x{cols}")
     check_guard(buf)
-    out, h = mb.fused_layernorm_act(to_dev(x, bf16), to_dev(w, bf16), to_dev(b, bf16),
-                                    r=to_dev(r, bf16), act="relu", want_h=True)
+    out, h = mb.fused_layernorm_act(to_dev(x, bf16), to_dev(r, bf16), to_dev(w, bf16),
+                                    to_dev(b, bf16), act="relu", want_h=True)
     want, want_h = oracle.layernorm_act(x, r, w, b, 1e-5, oracle.ACT_RELU, want_h=True)
     assert_close(to_host(out), want, bf16=bf16, what="LN relu")
     assert_bitexact(to_host(h), want_h, "h")

@@ -79,8 +79,8 @@ def test_layernorm_act(shape, path, res, bf16, row_path):
     for act in ("none", "relu", "gelu_tanh"):
         obuf, out = guarded_empty(shape, dt)
         hbuf, h = guarded_empty(shape, dt)
-        mb.fused_layernorm_act(to_dev(x, bf16), to_dev(w, bf16), to_dev(b, bf16),
-                               r=to_dev(r, bf16) if res else None, eps=1e-5, act=act,
+        mb.fused_layernorm_act(to_dev(x, bf16), to_dev(r, bf16) if res else None,
+                               to_dev(w, bf16), to_dev(b, bf16), eps=1e-5, act=act,
                                out=out, h_out=h)
         want, want_h = oracle.layernorm_act(x, r if res else None, w, b, 1e-5, ACTS[act],
                                             want_h=True)
@@ -94,7 +94,7 @@ def test_layernorm_act_without_h_matches_the_gelu_entry_point():
     """fused_layernorm_act(r, gelu) is the same chain as
     fused_residual_layernorm_gelu: both within the bar of one oracle."""
     x, r, w, b = _ln_inputs(64, 4096, 77, False)
-    out = mb.fused_layernorm_act(to_dev(x), to_dev(w), to_dev(b), r=to_dev(r))
+    out = mb.fused_layernorm_act(to_dev(x), to_dev(r), to_dev(w), to_dev(b))
     ref = mb.fused_residual_layernorm_gelu(to_dev(x), to_dev(r), to_dev(w), to_dev(b))
     want = oracle.residual_layernorm_gelu(x, r, w, b, 1e-5)
     assert_close(to_host(out), want)
@@ -107,7 +107,7 @@ def test_layernorm_act_workload_full_size(w):
     t = w.generate_all()
     res = w.params["residual"]
     d = {k: to_dev(v, bf16) for k, v in t.items()}
-    out, h = mb.fused_layernorm_act(d["x"], d["w"], d["b"], r=d.get("r"), eps=1e-5,
+    out, h = mb.fused_layernorm_act(d["x"], d.get("r"), d["w"], d["b"], eps=1e-5,
                                     act=w.params["act"], want_h=True)
     torch.cuda.synchronize()
     rows = W.sample_rows(w.rows, 32)
