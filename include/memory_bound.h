@@ -231,7 +231,17 @@ int mb_last_cuda_error(void);
  */
 mb_status mb_device_error(uint32_t *flags);
 
-/* Row-chain execution paths (both row chains). */
+/*
+ * Self-test of the failure path: launches one thread that waits, with a limit
+ * of limit_us microseconds (1 .. 1000000), on a shared-memory barrier that
+ * nothing completes -- the same bounded wait the staged row kernels use.  The
+ * wait runs out, the kernel records bit 0 in the device flags and ends
+ * normally, so a following mb_device_error() reports MB_ERR_DEVICE and the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+mb_status mb_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
+/* Row-chain execution paths (all row chains). */
 typedef enum mb_row_path {
     MB_ROW_AUTO = 0,     /* choose by shape and alignment (default)            */
     MB_ROW_WARP = 1,     /* one warp per row, row in registers                */

@@ -244,14 +244,15 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after kWaitLimitNs
-// (or kWaitLimitPolls polls).  Returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// of %globaltimer (or kWaitLimitPolls polls).  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (unsigned i = 0; i < kWaitLimitPolls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

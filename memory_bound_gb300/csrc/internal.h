@@ -86,6 +86,8 @@ mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtyp
                        const void *x, void *y, int64_t rows, int cols, bool aligned,
                        RowPlan *plan, bool launch);
 
+mb_status selftest_wait_timeout(const LaunchCtx &ctx, uint32_t limit_us);
+
 // Records a CUDA error for mb_last_cuda_error and returns MB_ERR_CUDA.
 mb_status cuda_fail(cudaError_t e);
 
