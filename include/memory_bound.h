@@ -22,10 +22,17 @@
  *
  * Conventions shared by every entry point:
  *
- *   Pointers    Device pointers (or any pointer the current device can
- *               dereference).  The caller owns every buffer, outputs
- *               included: the library never allocates, frees or copies
- *               buffers and never synchronises the stream.
+ *   Pointers    Device pointers, or any pointer the current device can
+ *               dereference at the same address: page-locked host memory
+ *               (cudaHostAlloc / cudaMallocHost, mapped into the device's
+ *               address space) included.  The kernels then read and write
+ *               that memory directly over the host link ("zero copy"); row
+ *               inputs that are not device memory never go through the
+ *               bulk-async staged path (each call checks them with
+ *               cudaPointerGetAttributes when that path is planned), so
+ *               host rows take a plain-load path.  The caller owns every
+ *               buffer, outputs included: the library never allocates,
+ *               frees or copies buffers and never synchronises the stream.
  *   Layout      Contiguous, row-major.  Per-column vectors (length cols /
  *               hidden) are broadcast over all rows (a stride-0 row view).
  *   dtype       MB_F32 (IEEE binary32) or MB_BF16 (bfloat16, raw 16-bit

@@ -116,9 +116,30 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
 
 
-def _stream_handle(t):
+def _call_device(tensors):
+    """The CUDA device a call runs on: that of its CUDA tensors, else (all
+    tensors in pinned host memory) the current device."""
     torch = _torch()
-    return torch.cuda.current_stream(t.device).cuda_stream
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _stream_handle(dev):
+    torch = _torch()
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _empty_like(x):
+    """An output like x: on x's device, or in pinned host memory when x is
+    there (the kernels then write it over the host link)."""
+    torch = _torch()
+    if x.is_cuda:
+        return torch.empty_like(x)
+    if not (x.device.type == "cpu" and x.is_pinned()):
+        raise ValueError("tensors must be CUDA tensors or pinned host tensors")
+    return torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
 
 
 class _NoSwitch:
@@ -132,38 +153,41 @@ class _NoSwitch:
 _NO_SWITCH = _NoSwitch()
 
 
-def _on_device(t):
-    """Make t's device current for the call (a no-op when it already is)."""
+def _on_device(dev):
+    """Make dev current for the call (a no-op when it already is)."""
     torch = _torch()
-    if t.device.index == torch.cuda.current_device():
+    if dev.index == torch.cuda.current_device():
         return _NO_SWITCH
-    return torch.cuda.device(t.device)
+    return torch.cuda.device(dev)
 
 
 def _require(tensors, dtype):
+    """Contiguous tensors of one dtype, each either on one CUDA device or in
+    pinned (page-locked) host memory; returns the device the call runs on."""
     for t in tensors:
-        if not t.is_cuda:
-            raise ValueError("tensors must be CUDA tensors")
+        if not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+            raise ValueError("tensors must be CUDA tensors or pinned host tensors")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous (row-major)")
         if t.dtype != dtype:
             raise TypeError("all tensors of a call must share one dtype")
-        if t.device != tensors[0].device:
-            raise ValueError("all tensors of a call must be on one device")
+    dev = _call_device(tensors)
+    if any(t.is_cuda and t.device != dev for t in tensors):
+        raise ValueError("all CUDA tensors of a call must be on one device")
+    return dev
 
 
 def fused_add_relu_scale(x, b1, b2, scale=0.5, out=None):
     """y = relu(x + b1) * scale + b2, elementwise (float32 or bfloat16)."""
-    torch = _torch()
     if out is None:
-        out = torch.empty_like(x)
-    _require([x, b1, b2, out], x.dtype)
+        out = _empty_like(x)
+    dev = _require([x, b1, b2, out], x.dtype)
     if not (x.numel() == b1.numel() == b2.numel() == out.numel()):
         raise ValueError("x, b1, b2 and out must have one size")
-    with _on_device(x):
+    with _on_device(dev):
         st = load_library().fused_add_relu_scale(
             x.data_ptr(), b1.data_ptr(), b2.data_ptr(), out.data_ptr(), x.numel(),
-            float(scale), _dtype_code(x), _stream_handle(x))
+            float(scale), _dtype_code(x), _stream_handle(dev))
     _check("fused_add_relu_scale", st)
     return out
 
@@ -172,12 +196,11 @@ def fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
                                          branch_scale=0.1, out=None):
     """The TorchInductor example chain on a 2-D x (rows x cols), float32 or
     bfloat16 (all tensors one dtype)."""
-    torch = _torch()
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, cols)")
     if out is None:
-        out = torch.empty_like(x)
-    _require([x, bias, gamma, beta, out], x.dtype)
+        out = _empty_like(x)
+    dev = _require([x, bias, gamma, beta, out], x.dtype)
     fn_name = ("fused_bias_relu_branch_mean_epilogue" if _dtype_code(x) == MB_F32
                else "fused_bias_relu_branch_mean_epilogue_bf16")
     rows, cols = x.shape
@@ -186,32 +209,31 @@ def fused_bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
             raise ValueError("per-column vectors must have cols elements")
     if out.numel() != x.numel():
         raise ValueError("out must match x")
-    with _on_device(x):
+    with _on_device(dev):
         st = getattr(load_library(), fn_name)(
             x.data_ptr(), bias.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
             out.data_ptr(), rows, cols, float(x_scale), float(branch_scale),
-            _stream_handle(x))
+            _stream_handle(dev))
     _check(fn_name, st)
     return out
 
 
 def fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None):
     """GeLU_tanh(LayerNorm(x + r) * w + b) over the last dim of a 2-D x."""
-    torch = _torch()
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, hidden)")
     if out is None:
-        out = torch.empty_like(x)
-    _require([x, r, w, b, out], x.dtype)
+        out = _empty_like(x)
+    dev = _require([x, r, w, b, out], x.dtype)
     rows, hidden = x.shape
     if r.shape != x.shape or w.numel() != hidden or b.numel() != hidden:
         raise ValueError("shape mismatch")
     if out.numel() != x.numel():
         raise ValueError("out must match x")
-    with _on_device(x):
+    with _on_device(dev):
         st = load_library().fused_residual_layernorm_gelu(
             x.data_ptr(), r.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(),
-            rows, hidden, float(eps), _dtype_code(x), _stream_handle(x))
+            rows, hidden, float(eps), _dtype_code(x), _stream_handle(dev))
     _check("fused_residual_layernorm_gelu", st)
     return out
 
@@ -222,15 +244,14 @@ def fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", out=None, h_out=N
     None (no residual).  With
     ``want_h`` (or an ``h_out`` tensor) also writes h = x + r (or x), the
     residual stream; returns (out, h) then, else out."""
-    torch = _torch()
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, hidden)")
     if out is None:
-        out = torch.empty_like(x)
+        out = _empty_like(x)
     if want_h and h_out is None:
-        h_out = torch.empty_like(x)
+        h_out = _empty_like(x)
     ts = [x, w, b, out] + [t for t in (r, h_out) if t is not None]
-    _require(ts, x.dtype)
+    dev = _require(ts, x.dtype)
     rows, hidden = x.shape
     if (r is not None and r.shape != x.shape) or w.numel() != hidden or b.numel() != hidden:
         raise ValueError("shape mismatch")
@@ -238,29 +259,28 @@ def fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", out=None, h_out=N
         if t is not None and t.numel() != x.numel():
             raise ValueError("outputs must match x")
     code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
-    with _on_device(x):
+    with _on_device(dev):
         st = load_library().fused_layernorm_act(
             x.data_ptr(), r.data_ptr() if r is not None else None, w.data_ptr(), b.data_ptr(),
             out.data_ptr(), h_out.data_ptr() if h_out is not None else None, rows, hidden,
-            float(eps), code, _dtype_code(x), _stream_handle(x))
+            float(eps), code, _dtype_code(x), _stream_handle(dev))
     _check("fused_layernorm_act", st)
     return (out, h_out) if h_out is not None else out
 
 
 def fused_row_softmax(x, out=None):
     """Softmax over the last dim of a 2-D x (float32 or bfloat16)."""
-    torch = _torch()
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, cols)")
     if out is None:
-        out = torch.empty_like(x)
-    _require([x, out], x.dtype)
+        out = _empty_like(x)
+    dev = _require([x, out], x.dtype)
     if out.numel() != x.numel():
         raise ValueError("out must match x")
     rows, cols = x.shape
-    with _on_device(x):
+    with _on_device(dev):
         st = load_library().fused_row_softmax(x.data_ptr(), out.data_ptr(), rows, cols,
-                                              _dtype_code(x), _stream_handle(x))
+                                              _dtype_code(x), _stream_handle(dev))
     _check("fused_row_softmax", st)
     return out
 

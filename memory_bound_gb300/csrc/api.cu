@@ -114,6 +114,15 @@ mb_status cuda_fail(cudaError_t e) {
     return MB_ERR_CUDA;
 }
 
+bool device_resident(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();           // an unknown pointer is not an error here
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice;
+}
+
 }  // namespace mb
 
 using namespace mb;

@@ -36,6 +36,8 @@ struct RowTuning {
     int ctas_per_sm;       // 0 = automatic
     int stages;            // 0 = automatic
     int vpt;               // vector slots per thread, 0 = automatic
+    int no_bulk = 0;       // 1: some row input is not device memory, so no
+                           // bulk-async copies (the STAGED path) are planned
 };
 
 // Process-wide pointwise override (mb_set_pointwise_shape).
@@ -90,5 +92,10 @@ mb_status selftest_wait_timeout(const LaunchCtx &ctx, uint32_t limit_us);
 
 // Records a CUDA error for mb_last_cuda_error and returns MB_ERR_CUDA.
 mb_status cuda_fail(cudaError_t e);
+
+// True when p lies in device memory (cudaMalloc, stream-ordered or virtual
+// memory allocations); false for pinned or other host memory, managed memory
+// and pointers CUDA does not know.  Only device memory is bulk-copied.
+bool device_resident(const void *p);
 
 }  // namespace mb

@@ -589,7 +589,7 @@ template <class C> struct RowEngine {
     // only sizes the grid for its rows.
     struct CacheEntry {
         bool used;
-        int device, cols, aligned, path, ctas_per_sm, stages, vpt;
+        int device, cols, aligned, path, ctas_per_sm, stages, vpt, no_bulk;
         RowPlan core;
         const void *fn;
     };
@@ -615,7 +615,7 @@ template <class C> struct RowEngine {
             for (const CacheEntry &e : pc.entries) {
                 if (e.used && e.device == ctx.device && e.cols == cols && e.aligned == (int)aligned &&
                     e.path == tun.path && e.ctas_per_sm == tun.ctas_per_sm &&
-                    e.stages == tun.stages && e.vpt == tun.vpt) {
+                    e.stages == tun.stages && e.vpt == tun.vpt && e.no_bulk == tun.no_bulk) {
                     core = e.core;
                     f = e.fn;
                     hit = true;
@@ -628,7 +628,8 @@ template <class C> struct RowEngine {
             if (st != MB_OK) return st;
             std::lock_guard<std::mutex> lock(pc.mu);
             pc.entries[pc.next] = CacheEntry{true, ctx.device, cols, (int)aligned, tun.path,
-                                             tun.ctas_per_sm, tun.stages, tun.vpt, core, f};
+                                             tun.ctas_per_sm, tun.stages, tun.vpt, tun.no_bulk,
+                                             core, f};
             pc.next = (pc.next + 1) % kCacheSize;
         }
         *p = core;
@@ -666,7 +667,7 @@ template <class C> struct RowEngine {
         const int nvec = cols / VEC;
         const bool warp_ok = nvec <= 32 * 8;
         const int stage_bytes = C::kInputs * cols * (int)sizeof(T);
-        const bool stage_fits = kHdrBytes + stage_bytes <= ctx.smem_optin;
+        const bool stage_fits = !tun.no_bulk && kHdrBytes + stage_bytes <= ctx.smem_optin;
 
         const bool one_cta = nvec <= kCtaMaxThreads * max_vpt(vec);
         int path = tun.path;
@@ -778,6 +779,17 @@ template <class C> struct RowEngine {
         const void *fn = nullptr;
         mb_status st = plan(ctx, tun, rows, cols, aligned, &p, &fn);
         if (st != MB_OK) return st;
+        if (launch && p.path == MB_ROW_STAGED) {
+            // Bulk-async copies read device memory only: rows held in host
+            // memory (pinned, read over the host link) take a plain-load path.
+            bool dev = true;
+            for (int i = 0; i < C::kInputs; ++i) dev = dev && device_resident(a.in[i]);
+            if (!dev) {
+                RowTuning t2 = tun;
+                t2.no_bulk = 1;
+                if ((st = plan(ctx, t2, rows, cols, aligned, &p, &fn)) != MB_OK) return st;
+            }
+        }
         if (plan_out) *plan_out = p;
         if (!launch || rows == 0) return MB_OK;
         LaunchCtx lctx = ctx;
