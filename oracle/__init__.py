@@ -85,6 +85,25 @@ def load(path=None):
     lib.oracle_layernorm_act_bf16.argtypes = [
         U16P, U16P, U16P, U16P, U16P, U16P, i64, i64, f32, ctypes.c_int]
     lib.oracle_layernorm_act_bf16.restype = None
+    u64 = ctypes.c_uint64
+    lib.oracle_layernorm_act_ex_f32.argtypes = [
+        F32P, F32P, F32P, F32P, F32P, F32P, F64P, F64P, i64, i64, f32, ctypes.c_int, f32,
+        u64, u64]
+    lib.oracle_layernorm_act_ex_f32.restype = None
+    lib.oracle_layernorm_act_ex_bf16.argtypes = [
+        U16P, U16P, U16P, U16P, U16P, U16P, F64P, F64P, i64, i64, f32, ctypes.c_int, f32,
+        u64, u64]
+    lib.oracle_layernorm_act_ex_bf16.restype = None
+    U32P = ctypes.POINTER(ctypes.c_uint32)
+    U64P = ctypes.POINTER(ctypes.c_uint64)
+    lib.oracle_philox4x32_10.argtypes = [U32P, U32P, U32P]
+    lib.oracle_philox4x32_10.restype = None
+    lib.oracle_philox4x64_10.argtypes = [U64P, U64P, U64P]
+    lib.oracle_philox4x64_10.restype = None
+    lib.oracle_dropout_keep.argtypes = [u64, u64, i64, f32]
+    lib.oracle_dropout_keep.restype = ctypes.c_int
+    lib.oracle_dropout_mask.argtypes = [u64, u64, i64, i64, f32, ctypes.POINTER(ctypes.c_uint8)]
+    lib.oracle_dropout_mask.restype = None
     lib.oracle_row_softmax_f32.argtypes = [F32P, F32P, i64, i64]
     lib.oracle_row_softmax_f32.restype = None
     lib.oracle_row_softmax_bf16.argtypes = [U16P, U16P, i64, i64]
@@ -256,6 +275,73 @@ def layernorm_act(x, r, w, b, eps=1e-5, act=ACT_GELU, want_h=False, lib=None):
     fn(p(x), p(r) if r is not None else nullp, p(w), p(b), p(out),
        p(h) if h is not None else nullp, rows, hidden, eps, int(act))
     return (out, h) if want_h else out
+
+
+def layernorm_act_ex(x, r, w, b, eps=1e-5, act=ACT_GELU, p=0.0, seed=0, offset=0,
+                     want_h=False, want_stats=False, lib=None):
+    """o4 with its extras: dropout with probability ``p`` keyed by (seed,
+    offset) on the activation output, and the per-row statistics.  Returns
+    (out, h, mean, rstd); h is None without ``want_h``, mean and rstd (float64
+    per row) None without ``want_stats``."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    rows, hidden = x.shape
+    if x.dtype == np.float32:
+        cv, fn, ptr, nullp = np.float32, lib.oracle_layernorm_act_ex_f32, _f32p, ctypes.POINTER(ctypes.c_float)()
+    elif x.dtype == np.uint16:
+        cv, fn, ptr, nullp = np.uint16, lib.oracle_layernorm_act_ex_bf16, _u16p, ctypes.POINTER(ctypes.c_uint16)()
+    else:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    w, b = _c(w, cv), _c(b, cv)
+    if r is not None:
+        r = _c(r, cv)
+        if r.shape != x.shape:
+            raise ValueError("shape mismatch")
+    if w.shape != (hidden,) or b.shape != (hidden,):
+        raise ValueError("shape mismatch")
+    out = np.empty_like(x)
+    h = np.empty_like(x) if want_h else None
+    mean = np.empty(rows, np.float64) if want_stats else None
+    rstd = np.empty(rows, np.float64) if want_stats else None
+    fn(ptr(x), ptr(r) if r is not None else nullp, ptr(w), ptr(b), ptr(out),
+       ptr(h) if h is not None else nullp, _f64p(mean), _f64p(rstd), rows, hidden, eps,
+       int(act), float(p), int(seed), int(offset))
+    return out, h, mean, rstd
+
+
+# --------------------------------------------------------------------------
+# o6: Philox counter-based generator and the dropout decision
+# --------------------------------------------------------------------------
+
+def philox4x32_10(ctr, key, lib=None):
+    """Philox-4x32-10 of a 4-word counter and a 2-word key (uint32 words)."""
+    lib = lib or load()
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    o = np.empty(4, np.uint32)
+    P = ctypes.POINTER(ctypes.c_uint32)
+    lib.oracle_philox4x32_10(c.ctypes.data_as(P), k.ctypes.data_as(P), o.ctypes.data_as(P))
+    return o
+
+
+def philox4x64_10(ctr, key, lib=None):
+    """Philox-4x64-10 (uint64 words): the same rounds with 64-bit words."""
+    lib = lib or load()
+    c = np.ascontiguousarray(ctr, np.uint64)
+    k = np.ascontiguousarray(key, np.uint64)
+    o = np.empty(4, np.uint64)
+    P = ctypes.POINTER(ctypes.c_uint64)
+    lib.oracle_philox4x64_10(c.ctypes.data_as(P), k.ctypes.data_as(P), o.ctypes.data_as(P))
+    return o
+
+
+def dropout_mask(seed, offset, start, n, p, lib=None):
+    """Keep decisions (bool) of elements start .. start + n - 1."""
+    lib = lib or load()
+    keep = np.empty(n, np.uint8)
+    lib.oracle_dropout_mask(int(seed), int(offset), int(start), int(n), float(p),
+                            keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    return keep.astype(bool)
 
 
 # --------------------------------------------------------------------------

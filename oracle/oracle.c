@@ -25,6 +25,11 @@
  *       residual sum optionally written out (rounded once to the I/O type) and
  *       the activation chosen (none, relu, gelu-tanh).
  *   o5  Row softmax in double, relative to the row maximum, rounded once.
+ *   o6  Dropout ([P2] §2.1 LayerNorm -> ReLU -> Dropout): the pages fix no
+ *       random number generator, so the decision of element i comes from the
+ *       published Philox-4x32-10 counter-based generator at a counter fixed by
+ *       (offset, i) and a key fixed by seed; kept elements are scaled by
+ *       1 / (1 - p) in double, dropped ones are the product with 0.
  */
 #include "oracle.h"
 
@@ -283,6 +288,95 @@ void oracle_bias_relu_branch_mean_epilogue_bf16(const uint16_t *x, const uint16_
 }
 
 /* ------------------------------------------------------------------------ */
+/* o6: counter-based random numbers and the dropout decision                */
+/* "Parallel random numbers: as easy as 1, 2, 3" (Salmon, Moraes, Dror and */
+/* Shaw, SC'11), the Philox-4xW-10 generator: a counter of four W-bit words */
+/* and a key of two; each of ten rounds multiplies counter words 0 and 2 by */
+/* the round multipliers M0 and M1 (full 2W-bit products) and forms         */
+/*   (hi(M1 c2) ^ c1 ^ k0,  lo(M1 c2),  hi(M0 c0) ^ c3 ^ k1,  lo(M0 c0)),     */
+/* and before every round but the first the key words are bumped by the    */
+/* Weyl constants W0, W1 (the leading W bits of the golden ratio's fraction */
+/* and of sqrt(3) - 1).  The pages use dropout but fix no generator.        */
+/* ------------------------------------------------------------------------ */
+
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        uint64_t p0 = (uint64_t)M0 * c0;
+        uint64_t p1 = (uint64_t)M1 * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        unsigned __int128 p0 = (unsigned __int128)M0 * c0;
+        unsigned __int128 p1 = (unsigned __int128)M1 * c2;
+        uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k0;
+        uint64_t n1 = (uint64_t)p1;
+        uint64_t n2 = (uint64_t)(p0 >> 64) ^ c3 ^ k1;
+        uint64_t n3 = (uint64_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+int oracle_dropout_keep(uint64_t seed, uint64_t offset, int64_t i, float p)
+{
+    /* element i takes word i mod 4 of the block at counter
+     * (0, 0, lo(g), hi(g)), g = offset + floor(i / 4), key (lo, hi) of seed */
+    uint64_t g = offset + (uint64_t)i / 4u;
+    uint32_t ctr[4] = {0u, 0u, (uint32_t)g, (uint32_t)(g >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    /* u = the word's top 24 bits as a fraction in [0, 1): exact in fp32 */
+    float u = (float)(w[i % 4] >> 8) * 0x1p-24f;
+    return u >= p;
+}
+
+void oracle_dropout_mask(uint64_t seed, uint64_t offset, int64_t start, int64_t n, float p,
+                         uint8_t *keep)
+{
+    for (int64_t k = 0; k < n; ++k)
+        keep[k] = (uint8_t)oracle_dropout_keep(seed, offset, start + k, p);
+}
+
+/* ------------------------------------------------------------------------ */
 /* o4: LayerNorm family                                                     */
 /* [P3] §4.3 (mean, var = sum((x - mean)^2)/cols, (x - mean)/sqrt(var + eps) */
 /* * gamma + beta); [P2] §2.1 (LayerNorm -> ReLU fused) and §2.2-2.3         */
@@ -298,9 +392,17 @@ static double o4_act(double n, int act)
     return n;
 }
 
+/* The optional extras of the LayerNorm family: dropout on the activation
+ * (p = 0: none) and the per-row statistics written out (NULL: not written). */
+struct o4_extras {
+    float p;
+    uint64_t seed, offset;
+    double *mean_out, *rstd_out;
+};
+
 static void o4_rows(const void *x, const void *r, const void *w, const void *b,
                     o3_load_fn load, void *out, void *h_out, int bf16, int64_t rows,
-                    int64_t hidden, float eps, int act)
+                    int64_t hidden, float eps, int act, const struct o4_extras *ex)
 {
     for (int64_t i = 0; i < rows; ++i) {
         int64_t base = i * hidden;
@@ -321,6 +423,10 @@ static void o4_rows(const void *x, const void *r, const void *w, const void *b,
             sq += d * d;
         }
         double rstd = 1.0 / sqrt(sq / (double)hidden + (double)eps);
+        if (ex->mean_out)
+            ex->mean_out[i] = mean;
+        if (ex->rstd_out)
+            ex->rstd_out[i] = rstd;
         for (int64_t j = 0; j < hidden; ++j) {
             float v = load(x, base + j);
             if (r)
@@ -333,6 +439,15 @@ static void o4_rows(const void *x, const void *r, const void *w, const void *b,
             }
             double n = ((double)v - mean) * rstd * (double)load(w, j) + (double)load(b, j);
             double g = o4_act(n, act);
+            if (ex->p > 0.0f) {
+                /* dropout: a kept element is scaled by 1 / (1 - p); a dropped
+                 * one is the product g * 0 (a signed zero, as the scaled
+                 * mask product of eager dropout gives) */
+                if (oracle_dropout_keep(ex->seed, ex->offset, base + j, ex->p))
+                    g = g / (1.0 - (double)ex->p);
+                else
+                    g = g * 0.0;
+            }
             if (bf16)
                 ((uint16_t *)out)[base + j] = oracle_bf16_from_double(g);
             else
@@ -345,14 +460,35 @@ void oracle_layernorm_act_f32(const float *x, const float *r, const float *w,
                               const float *b, float *out, float *h_out, int64_t rows,
                               int64_t hidden, float eps, int act)
 {
-    o4_rows(x, r, w, b, load_f32, out, h_out, 0, rows, hidden, eps, act);
+    struct o4_extras none = {0.0f, 0, 0, NULL, NULL};
+    o4_rows(x, r, w, b, load_f32, out, h_out, 0, rows, hidden, eps, act, &none);
 }
 
 void oracle_layernorm_act_bf16(const uint16_t *x, const uint16_t *r, const uint16_t *w,
                                const uint16_t *b, uint16_t *out, uint16_t *h_out,
                                int64_t rows, int64_t hidden, float eps, int act)
 {
-    o4_rows(x, r, w, b, load_bf16, out, h_out, 1, rows, hidden, eps, act);
+    struct o4_extras none = {0.0f, 0, 0, NULL, NULL};
+    o4_rows(x, r, w, b, load_bf16, out, h_out, 1, rows, hidden, eps, act, &none);
+}
+
+void oracle_layernorm_act_ex_f32(const float *x, const float *r, const float *w,
+                                 const float *b, float *out, float *h_out, double *mean_out,
+                                 double *rstd_out, int64_t rows, int64_t hidden, float eps,
+                                 int act, float p, uint64_t seed, uint64_t offset)
+{
+    struct o4_extras ex = {p, seed, offset, mean_out, rstd_out};
+    o4_rows(x, r, w, b, load_f32, out, h_out, 0, rows, hidden, eps, act, &ex);
+}
+
+void oracle_layernorm_act_ex_bf16(const uint16_t *x, const uint16_t *r, const uint16_t *w,
+                                  const uint16_t *b, uint16_t *out, uint16_t *h_out,
+                                  double *mean_out, double *rstd_out, int64_t rows,
+                                  int64_t hidden, float eps, int act, float p, uint64_t seed,
+                                  uint64_t offset)
+{
+    struct o4_extras ex = {p, seed, offset, mean_out, rstd_out};
+    o4_rows(x, r, w, b, load_bf16, out, h_out, 1, rows, hidden, eps, act, &ex);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -98,6 +98,34 @@ void oracle_layernorm_act_bf16(const uint16_t *x, const uint16_t *r, const uint1
                                const uint16_t *b, uint16_t *out, uint16_t *h_out,
                                int64_t rows, int64_t hidden, float eps, int act);
 
+/* ---- o4 with the optional extras: per-row statistics written out (mean and
+ * rstd in double; NULL: not written) and dropout on the activation output
+ * ([P2] §2.1 LayerNorm -> ReLU -> Dropout; p = 0: none), the decision of
+ * element i (its index in the whole tensor) as in oracle_dropout_keep; kept
+ * values become act / (1 - p) (in double, then rounded once), dropped ones
+ * act * 0. */
+void oracle_layernorm_act_ex_f32(const float *x, const float *r, const float *w,
+                                 const float *b, float *out, float *h_out, double *mean_out,
+                                 double *rstd_out, int64_t rows, int64_t hidden, float eps,
+                                 int act, float p, uint64_t seed, uint64_t offset);
+void oracle_layernorm_act_ex_bf16(const uint16_t *x, const uint16_t *r, const uint16_t *w,
+                                  const uint16_t *b, uint16_t *out, uint16_t *h_out,
+                                  double *mean_out, double *rstd_out, int64_t rows,
+                                  int64_t hidden, float eps, int act, float p, uint64_t seed,
+                                  uint64_t offset);
+
+/* ---- o6: Philox-4xW-10 ("Parallel random numbers: as easy as 1, 2, 3",
+ * SC'11) for W = 32 (the dropout generator) and W = 64 (the same round
+ * structure, checkable against numpy's Philox), and the dropout decision:
+ *   element i of a call keyed by (seed, offset) takes word i mod 4 of
+ *   Philox-4x32-10 at counter (0, 0, lo(g), hi(g)), g = offset + floor(i/4),
+ *   key (lo(seed), hi(seed)); u = (word >> 8) * 2^-24; kept iff u >= p. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+int oracle_dropout_keep(uint64_t seed, uint64_t offset, int64_t i, float p);
+void oracle_dropout_mask(uint64_t seed, uint64_t offset, int64_t start, int64_t n, float p,
+                         uint8_t *keep);
+
 /* ---- o5: row softmax ([P1] §4.1-4.2, [P2] §3.2: the softmax of each score
  * row, taken relative to the row maximum):
  *   m = max_j x_j;  e_j = exp(x_j - m);  y_j = e_j / sum_k e_k   (in double) */

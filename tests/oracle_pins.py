@@ -450,4 +450,163 @@ def pin_softmax_bf16(lib):
     assert np.all(np.abs(g - want) <= 2.0 ** -8 * want * 1.0001 + 1e-40)
 
 
+# --------------------------------------------------------------------------
+# o4 extras and o6: row statistics, the Philox generator, dropout
+# --------------------------------------------------------------------------
+
+def pin_layernorm_stats_library(lib):
+    """The per-row statistics o4 writes out: torch float64 mean and
+    1/sqrt(biased variance + eps) of v = x + r ([P3] §4.3)."""
+    x, r, w, b = _ln_inputs(7, 300, 71)
+    _, _, mean, rstd = oracle.layernorm_act_ex(x, r, w, b, 1e-5, oracle.ACT_RELU,
+                                               want_stats=True, lib=lib)
+    v = torch.from_numpy(x).double() + torch.from_numpy(r).double()
+    v = v.float().double()                              # v = x + r in fp32
+    want_mean = v.mean(dim=1).numpy()
+    want_rstd = (1.0 / torch.sqrt(v.var(dim=1, unbiased=False) + 1e-5)).numpy()
+    assert np.all(np.abs(mean - want_mean) <= 1e-13)
+    assert np.all(np.abs(rstd - want_rstd) <= 1e-13 * want_rstd)
+
+
+def _numpy_philox64(ctr, key, blocks=1):
+    """numpy's Philox (4x64-10) bit generator: it advances its counter before
+    each block, so a generator set to ctr - 1 yields the block at ctr."""
+    prev = np.array(ctr, np.uint64)
+    assert prev[0] >= 1
+    prev[0] -= np.uint64(1)
+    bg = np.random.Philox(key=np.array(key, np.uint64), counter=prev)
+    return bg.random_raw(4 * blocks).astype(np.uint64)
+
+
+def pin_philox64_numpy(lib):
+    """Philox-4x64-10 against numpy's Philox bit generator (a library routine)
+    on counters and keys with every word in play: the round structure (which
+    words are multiplied, what each new word is, the key schedule) that the
+    32-bit generator shares."""
+    rng = np.random.default_rng(2024)
+    cases = [([1, 0, 0, 0], [0, 0]), ([1, 2, 3, 4], [5, 6]),
+             ([2 ** 64 - 1, 2 ** 64 - 1, 2 ** 64 - 1, 2 ** 64 - 1], [2 ** 64 - 1, 2 ** 64 - 1])]
+    for _ in range(6):
+        cases.append((list(rng.integers(1, 2 ** 63, 4, dtype=np.uint64) * np.uint64(2) - np.uint64(1)),
+                      list(rng.integers(0, 2 ** 63, 2, dtype=np.uint64) * np.uint64(2))))
+    for ctr, key in cases:
+        got = oracle.philox4x64_10(ctr, key, lib=lib)
+        want = _numpy_philox64(ctr, key)
+        assert np.array_equal(got, want), (ctr, key)
+
+
+def _curand():
+    """cuRAND's host-side generator API (runs on the CPU), or None."""
+    import ctypes
+    import ctypes.util
+    cands = [ctypes.util.find_library("curand"), "libcurand.so", "libcurand.so.10"]
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    cands += [os.path.join(home, d, "libcurand.so") for d in ("lib64", "lib")]
+    for c in cands:
+        if not c:
+            continue
+        try:
+            return ctypes.CDLL(c)
+        except OSError:
+            continue
+    return None
+
+
+def _curand_philox_words(seed, n, offset=0):
+    """n raw 32-bit outputs of cuRAND's host Philox4_32_10 generator."""
+    import ctypes
+    lib = _curand()
+    if lib is None:
+        import pytest
+        pytest.skip("libcurand not found")
+    g = ctypes.c_void_p()
+    assert lib.curandCreateGeneratorHost(ctypes.byref(g), 161) == 0  # PHILOX4_32_10
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(g, ctypes.c_ulonglong(seed)) == 0
+        if offset:
+            assert lib.curandSetGeneratorOffset(g, ctypes.c_ulonglong(offset)) == 0
+        buf = (ctypes.c_uint32 * n)()
+        assert lib.curandGenerate(g, buf, ctypes.c_size_t(n)) == 0
+        return np.frombuffer(buf, np.uint32).copy()
+    finally:
+        lib.curandDestroyGenerator(g)
+
+
+def pin_philox32_curand(lib):
+    """Philox-4x32-10 against cuRAND's Philox4_32_10 host generator (a library
+    routine): with seed s its output block b is the generator at counter
+    (0, 0, b, 0) under key (lo(s), hi(s)), and a generator offset of 4k starts
+    at counter (0, 0, k, 0)."""
+    for seed in (0, 1, 0x0123456789ABCDEF, 2 ** 64 - 1):
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        words = _curand_philox_words(seed, 4 * 64)
+        for blk in range(64):
+            got = oracle.philox4x32_10([0, 0, blk, 0], key, lib=lib)
+            assert np.array_equal(got, words[4 * blk:4 * blk + 4]), (seed, blk)
+        k = 3 * 4096 + 5
+        words = _curand_philox_words(seed, 4, offset=4 * k)
+        assert np.array_equal(oracle.philox4x32_10([0, 0, k, 0], key, lib=lib), words)
+
+
+def pin_dropout_decision(lib):
+    """Element i of a call (seed, offset 0) takes word i mod 4 of block i // 4,
+    which is cuRAND's output i; kept iff (word >> 8) * 2^-24 >= p.  p is also
+    set to the exact u of chosen elements (u >= p keeps them), p = 0 keeps
+    everything, and masks nest as p grows."""
+    seed = 0x5EED0F0D
+    words = _curand_philox_words(seed, 4 * 256)
+    u = (words >> np.uint32(8)).astype(np.float32) * np.float32(2.0 ** -24)
+    for p in (0.1, 0.5, 0.9, float(u[17]), float(u[300])):
+        keep = oracle.dropout_mask(seed, 0, 0, u.size, p, lib=lib)
+        assert np.array_equal(keep, u >= np.float32(p)), p
+    assert oracle.dropout_mask(seed, 0, 0, 1000, 0.0, lib=lib).all()
+    lo = oracle.dropout_mask(seed, 9, 40, 4000, 0.2, lib=lib)
+    hi = oracle.dropout_mask(seed, 9, 40, 4000, 0.6, lib=lib)
+    assert np.all(hi <= lo)
+
+
+def pin_dropout_counter_and_rate(lib):
+    """Counter arithmetic: offset + 1 is the same stream as element index + 4;
+    the keep rate over 2^20 elements is within 5 sigma of 1 - p; another seed
+    gives another mask."""
+    a = oracle.dropout_mask(11, 5, 8, 4096, 0.3, lib=lib)
+    b = oracle.dropout_mask(11, 4, 12, 4096, 0.3, lib=lib)
+    assert np.array_equal(a, b)
+    n = 1 << 20
+    for p in (0.1, 0.5):
+        keep = oracle.dropout_mask(12345, 0, 0, n, p, lib=lib)
+        sigma = math.sqrt(n * p * (1 - p))
+        assert abs(keep.sum() - n * (1 - p)) <= 5 * sigma, p
+    other = oracle.dropout_mask(12346, 0, 0, n, 0.5, lib=lib)
+    same = np.mean(other == oracle.dropout_mask(12345, 0, 0, n, 0.5, lib=lib))
+    assert abs(same - 0.5) < 0.01
+
+
+def pin_layernorm_dropout(lib):
+    """[P2] §2.1's LayerNorm -> ReLU -> Dropout: kept elements are the
+    undropped output / (1 - p) (within a rounding of each), dropped ones are
+    the product with 0 (+0 after a ReLU), by the mask of element index
+    row * hidden + col; p = 0 is the undropped chain bit for bit."""
+    x, r, w, b = _ln_inputs(9, 257, 72)
+    for dt in ("f32", "bf16"):
+        if dt == "bf16":
+            x, r, w, b = (synth.f32_to_bf16_bits(a) for a in (x, r, w, b))
+        base = oracle.layernorm_act(x, None, w, b, 1e-5, oracle.ACT_RELU, lib=lib)
+        same, _, _, _ = oracle.layernorm_act_ex(x, None, w, b, 1e-5, oracle.ACT_RELU, p=0.0,
+                                                lib=lib)
+        assert np.array_equal(base, same)
+        p = 0.25
+        out, _, _, _ = oracle.layernorm_act_ex(x, None, w, b, 1e-5, oracle.ACT_RELU, p=p,
+                                               seed=99, offset=3, lib=lib)
+        keep = oracle.dropout_mask(99, 3, 0, x.size, p, lib=lib).reshape(x.shape)
+        if dt == "bf16":
+            g, o, tol = synth.bf16_bits_to_f32(base), synth.bf16_bits_to_f32(out), 2.0 ** -7
+        else:
+            g, o, tol = base, out, 2.0 ** -22
+        g64, o64 = g.astype(np.float64), o.astype(np.float64)
+        assert np.all(np.abs(o64[keep] - g64[keep] / (1 - p)) <= tol * np.abs(g64[keep]) / (1 - p))
+        assert np.all(o[~keep] == 0) and not np.any(np.signbit(o[~keep]))
+        assert 0.6 < keep.mean() < 0.9
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

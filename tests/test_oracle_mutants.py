@@ -73,6 +73,30 @@ MUTANTS = {
                          "sum += exp((double)load(x, base + j));"),
     "o5_divide_by_cols": ("double p = exp((double)load(x, base + j) - m) / sum;",
                           "double p = exp((double)load(x, base + j) - m) / (double)cols;"),
+    # o4 extras and o6: statistics out, Philox, dropout
+    "stats_mean_is_sum": ("ex->mean_out[i] = mean;", "ex->mean_out[i] = sum;"),
+    "stats_rstd_is_var": ("ex->rstd_out[i] = rstd;", "ex->rstd_out[i] = 1.0 / (rstd * rstd);"),
+    "philox32_multiplier": ("0xD2511F53u", "0xD2511F55u"),
+    "philox32_no_key_bump": ("            k0 += W0;\n            k1 += W1;\n        }\n        uint64_t p0",
+                             "        }\n        uint64_t p0"),
+    "philox32_nine_rounds": ("uint32_t k0 = key[0], k1 = key[1];\n    for (int round = 0; round < 10;",
+                             "uint32_t k0 = key[0], k1 = key[1];\n    for (int round = 0; round < 9;"),
+    "philox32_words_swapped": ("uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;",
+                               "uint32_t n0 = (uint32_t)(p1 >> 32) ^ c3 ^ k0;"),
+    "philox64_hi_word": ("uint64_t n2 = (uint64_t)(p0 >> 64) ^ c3 ^ k1;",
+                         "uint64_t n2 = (uint64_t)(p0 >> 64) ^ c1 ^ k1;"),
+    "philox64_key_order": ("uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k0;",
+                           "uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k1;"),
+    "dropout_lane": ("float u = (float)(w[i % 4] >> 8)", "float u = (float)(w[(i + 1) % 4] >> 8)"),
+    "dropout_counter_word": ("uint32_t ctr[4] = {0u, 0u, (uint32_t)g, (uint32_t)(g >> 32)};",
+                             "uint32_t ctr[4] = {(uint32_t)g, 0u, 0u, (uint32_t)(g >> 32)};"),
+    "dropout_block_per_element": ("uint64_t g = offset + (uint64_t)i / 4u;",
+                                  "uint64_t g = offset + (uint64_t)i;"),
+    "dropout_strict_threshold": ("return u >= p;", "return u > p;"),
+    "dropout_low_bits": ("(w[i % 4] >> 8) * 0x1p-24f", "(w[i % 4] & 0xFFFFFFu) * 0x1p-24f"),
+    "dropout_scale_inverted": ("g = g / (1.0 - (double)ex->p);", "g = g * (1.0 - (double)ex->p);"),
+    "dropout_dropped_kept": ("                else\n                    g = g * 0.0;",
+                             "                else\n                    g = g * 1.0;"),
     "o5_min_not_max": ("if (v > m)\n                m = v;", "if (v < m || m == -INFINITY)\n                m = v;"),
 }
 
