@@ -226,7 +226,9 @@ class Case:
         elif self.w.chain == "lnact":
             mb.fused_layernorm_act(d["x"], d.get("r"), d["w"], d["b"], eps=p["eps"],
                                    act=p["act"], out=out,
-                                   h_out=self.houts[k % self.nsets] if p["write_h"] else None)
+                                   h_out=self.houts[k % self.nsets] if p["write_h"] else None,
+                                   p=p.get("p", 0.0), seed=p.get("seed", 0),
+                                   offset=p.get("offset", 0))
         else:
             mb.fused_residual_layernorm_gelu(d["x"], d["r"], d["w"], d["b"], p["eps"], out=out)
 
@@ -256,7 +258,8 @@ class Case:
         if self.w.chain == "lnact":
             v = d["x"] + d["r"] if "r" in d else d["x"]
             n = F.layer_norm(v, (self.w.cols,), d["w"], d["b"], p["eps"])
-            return torch.relu(n) if p["act"] == "relu" else F.gelu(n, approximate="tanh")
+            a = torch.relu(n) if p["act"] == "relu" else F.gelu(n, approximate="tanh")
+            return F.dropout(a, p["p"]) if p.get("p") else a
         if self.w.chain == "inductor":
             t = d["x"] * p["x_scale"] + d["bias"]
             a = torch.relu(t)

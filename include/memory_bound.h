@@ -10,7 +10,8 @@
  *   fused_residual_layernorm_gelu         GeLU_tanh(LayerNorm(x + r) * w + b)
  *
  * and, built on the same row engines: fused_layernorm_act (LayerNorm with an
- * optional residual, residual-stream output and activation), fused_row_softmax
+ * optional residual, residual-stream output and activation) and its extended
+ * form fused_layernorm_act_ex (dropout, per-row statistics), fused_row_softmax
  * and the bf16 variant of the TorchInductor chain.
  *
  * Sources (the pages these chains come from):
@@ -195,6 +196,37 @@ mb_status fused_layernorm_act(const void *x, const void *r, const void *w, const
                               cudaStream_t stream);
 
 /*
+ * fused_layernorm_act with its optional extras, in the same single pass:
+ *
+ *   dropout  [P2] §2.1 fuses LayerNorm -> ReLU -> Dropout (p = 0.1 there)
+ *            into one kernel.  With 0 < p < 1 each element of `out` is kept
+ *            with probability 1 - p and scaled by 1 / (1 - p) (fp32, rounded
+ *            once), or multiplied by 0.  The pages fix no random number
+ *            generator; the decision is the counter-based Philox-4x32-10
+ *            ("Parallel random numbers: as easy as 1, 2, 3", SC'11): element
+ *            i = row * hidden + col takes word i mod 4 of the block at counter
+ *            (0, 0, lo(g), hi(g)), g = offset + floor(i / 4), under the key
+ *            (lo(seed), hi(seed)), and is kept iff (word >> 8) * 2^-24 >= p.
+ *            The decisions depend only on (seed, offset, i, p), never on the
+ *            launch; a later call takes fresh ones with offset advanced by
+ *            ceil(rows * hidden / 4).  p = 0: no dropout (out is bit-identical
+ *            to fused_layernorm_act).  p outside [0, 1) (or NaN) gives
+ *            MB_ERR_VALUE.  h_out (the residual stream) is never dropped.
+ *   stats    mean_out / rstd_out (fp32, `rows` values each; NULL: not
+ *            written) receive each row's mean and 1/sqrt(var + eps), the
+ *            statistics the normalisation used (what a LayerNorm backward
+ *            pass reads).  4-byte aligned, else MB_ERR_ALIGN.
+ *
+ * No output (out, h_out, mean_out, rstd_out) may overlap an input or another
+ * output (MB_ERR_OVERLAP).
+ */
+mb_status fused_layernorm_act_ex(const void *x, const void *r, const void *w, const void *b,
+                                 void *out, void *h_out, float *mean_out, float *rstd_out,
+                                 int64_t rows, int64_t hidden, float eps, mb_activation act,
+                                 float p, uint64_t seed, uint64_t offset, mb_dtype dtype,
+                                 cudaStream_t stream);
+
+/*
  * Row softmax over rows x cols:  y[i, j] = exp(x[i, j] - m_i) / sum_k exp(x[i, k] - m_i),
  * m_i the row maximum.  [P1] §4.1-4.2 and [P2] §3.2 (the softmax of a score
  * row, normalised by the row maximum; here the row is held on chip, so it is
@@ -299,7 +331,8 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * path), else 0,
  * out[6] = dynamic shared memory bytes.  `chain`: 0 residual + LayerNorm +
  * GeLU, 1 the TorchInductor chain, 2 the LayerNorm family with a residual,
- * 3 without, 4 row softmax.  `aligned` says whether every pointer is 16-byte
+ * 3 without, 4 row softmax, 5 and 6 the LayerNorm family with dropout (with
+ * a residual, without).  `aligned` says whether every pointer is 16-byte
  * aligned.  Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,

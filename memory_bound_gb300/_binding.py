@@ -24,6 +24,8 @@ SIGNATURES = {
     "fused_residual_layernorm_gelu": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]),
     "fused_bias_relu_branch_mean_epilogue_bf16": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _F, _P]),
     "fused_layernorm_act": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P]),
+    "fused_layernorm_act_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _F,
+                                    ctypes.c_uint64, ctypes.c_uint64, _I, _P]),
     "fused_row_softmax": (_I, [_P, _P, _I64, _I64, _I, _P]),
     "mb_status_string": (ctypes.c_char_p, [_I]),
     "mb_abi_version": (_I, []),
@@ -239,32 +241,64 @@ def fused_residual_layernorm_gelu(x, r, w, b, eps=1e-5, out=None):
 
 
 def fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", out=None, h_out=None,
-                        want_h=False):
+                        want_h=False, p=0.0, seed=0, offset=0, mean_out=None, rstd_out=None,
+                        want_stats=False):
     """act(LayerNorm(x (+ r)) * w + b) over the last dim of a 2-D x; r may be
-    None (no residual).  With
-    ``want_h`` (or an ``h_out`` tensor) also writes h = x + r (or x), the
-    residual stream; returns (out, h) then, else out."""
+    None (no residual).
+
+    With ``want_h`` (or an ``h_out`` tensor) also writes h = x + r (or x), the
+    residual stream.  With ``p`` > 0, dropout on the output keyed by
+    (``seed``, ``offset``) (Philox-4x32-10; see fused_layernorm_act_ex in the
+    C header).  With ``want_stats`` (or ``mean_out`` / ``rstd_out`` float32
+    tensors of ``rows`` values) also writes each row's mean and rstd.
+
+    Returns out; (out, h) when h is written; (out, h or None, mean, rstd) when
+    the statistics are."""
+    torch = _torch()
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, hidden)")
+    rows, hidden = x.shape
     if out is None:
         out = _empty_like(x)
     if want_h and h_out is None:
         h_out = _empty_like(x)
+    stats = want_stats or mean_out is not None or rstd_out is not None
+    if stats:
+        like = x if x.is_cuda else None
+        for name, t in (("mean_out", mean_out), ("rstd_out", rstd_out)):
+            if t is None:
+                t = (torch.empty(rows, dtype=torch.float32, device=like.device) if like is not None
+                     else torch.empty(rows, dtype=torch.float32, pin_memory=True))
+            elif t.dtype != torch.float32 or t.numel() != rows:
+                raise ValueError(f"{name} must be float32 with rows elements")
+            if name == "mean_out":
+                mean_out = t
+            else:
+                rstd_out = t
     ts = [x, w, b, out] + [t for t in (r, h_out) if t is not None]
     dev = _require(ts, x.dtype)
-    rows, hidden = x.shape
+    if stats:
+        _require([mean_out, rstd_out], torch.float32)
     if (r is not None and r.shape != x.shape) or w.numel() != hidden or b.numel() != hidden:
         raise ValueError("shape mismatch")
     for t in (out, h_out):
         if t is not None and t.numel() != x.numel():
             raise ValueError("outputs must match x")
     code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    ptr = (lambda t: t.data_ptr() if t is not None else None)
     with _on_device(dev):
-        st = load_library().fused_layernorm_act(
-            x.data_ptr(), r.data_ptr() if r is not None else None, w.data_ptr(), b.data_ptr(),
-            out.data_ptr(), h_out.data_ptr() if h_out is not None else None, rows, hidden,
-            float(eps), code, _dtype_code(x), _stream_handle(dev))
+        if p == 0.0 and not stats:
+            st = load_library().fused_layernorm_act(
+                x.data_ptr(), ptr(r), w.data_ptr(), b.data_ptr(), out.data_ptr(), ptr(h_out),
+                rows, hidden, float(eps), code, _dtype_code(x), _stream_handle(dev))
+        else:
+            st = load_library().fused_layernorm_act_ex(
+                x.data_ptr(), ptr(r), w.data_ptr(), b.data_ptr(), out.data_ptr(), ptr(h_out),
+                ptr(mean_out), ptr(rstd_out), rows, hidden, float(eps), code, float(p),
+                int(seed), int(offset), _dtype_code(x), _stream_handle(dev))
     _check("fused_layernorm_act", st)
+    if stats:
+        return out, h_out, mean_out, rstd_out
     return (out, h_out) if h_out is not None else out
 
 
@@ -315,10 +349,11 @@ def set_pointwise_shape(blocks_per_sm=0, unroll=0):
 
 def row_plan(chain, dtype, rows, cols, aligned=True):
     """The launch a row chain would use: dict(path, threads, ctas, vpt, vec,
-    stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact" or
-    "softmax"; dtype: "f32" or "bf16"."""
+    stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact", "softmax",
+    "lnact_res_dropout" or "lnact_dropout"; dtype: "f32" or "bf16"."""
     out = (ctypes.c_int32 * 7)()
-    code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4}[chain]
+    code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4,
+            "lnact_res_dropout": 5, "lnact_dropout": 6}[chain]
     dt = {"f32": MB_F32, "bf16": MB_BF16}[dtype]
     st = load_library().mb_row_plan(code, dt, rows, cols, int(bool(aligned)), out)
     _check("mb_row_plan", st)

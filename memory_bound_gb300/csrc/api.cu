@@ -240,36 +240,62 @@ mb_status fused_bias_relu_branch_mean_epilogue_bf16(const void *x, const void *b
 mb_status fused_layernorm_act(const void *x, const void *r, const void *w, const void *b,
                               void *out, void *h_out, int64_t rows, int64_t hidden, float eps,
                               mb_activation act, mb_dtype dtype, cudaStream_t stream) {
+    return fused_layernorm_act_ex(x, r, w, b, out, h_out, nullptr, nullptr, rows, hidden, eps,
+                                  act, 0.0f, 0, 0, dtype, stream);
+}
+
+mb_status fused_layernorm_act_ex(const void *x, const void *r, const void *w, const void *b,
+                                 void *out, void *h_out, float *mean_out, float *rstd_out,
+                                 int64_t rows, int64_t hidden, float eps, mb_activation act,
+                                 float p, uint64_t seed, uint64_t offset, mb_dtype dtype,
+                                 cudaStream_t stream) {
     if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
     mb_status st = check_rows(rows, hidden);
     if (st != MB_OK) return st;
     if (!std::isfinite(eps) || eps < 0.0f) return MB_ERR_VALUE;
     if (act != MB_ACT_NONE && act != MB_ACT_RELU && act != MB_ACT_GELU_TANH) return MB_ERR_VALUE;
+    if (!(p >= 0.0f && p < 1.0f)) return MB_ERR_VALUE;     // NaN fails too
     if (rows == 0) return MB_OK;
     if (!x || !w || !b || !out) return MB_ERR_NULL;
     const int es = elem_size(dtype);
-    for (const void *p : {x, r, w, b, static_cast<const void *>(out),
+    for (const void *q : {x, r, w, b, static_cast<const void *>(out),
                           static_cast<const void *>(h_out)})
-        if (p && !aligned_to(p, es)) return MB_ERR_ALIGN;
-    const int64_t big = rows * hidden * es, small = hidden * es;
-    for (const void *o : {static_cast<const void *>(out), static_cast<const void *>(h_out)}) {
+        if (q && !aligned_to(q, es)) return MB_ERR_ALIGN;
+    for (const void *q : {static_cast<const void *>(mean_out),
+                          static_cast<const void *>(rstd_out)})
+        if (q && !aligned_to(q, 4)) return MB_ERR_ALIGN;
+    const int64_t big = rows * hidden * es, small = hidden * es, stat = rows * 4;
+    // every output (out, h_out, mean_out, rstd_out) against every input and
+    // against the other outputs
+    const void *outs[4] = {out, h_out, mean_out, rstd_out};
+    const int64_t out_bytes[4] = {big, big, stat, stat};
+    for (int i = 0; i < 4; ++i) {
+        const void *o = outs[i];
+        const int64_t n = out_bytes[i];
         if (!o) continue;
-        if (overlaps(o, big, x, big) || (r && overlaps(o, big, r, big)) ||
-            overlaps(o, big, w, small) || overlaps(o, big, b, small))
+        if (overlaps(o, n, x, big) || (r && overlaps(o, n, r, big)) ||
+            overlaps(o, n, w, small) || overlaps(o, n, b, small))
             return MB_ERR_OVERLAP;
+        for (int j = i + 1; j < 4; ++j)
+            if (outs[j] && overlaps(o, n, outs[j], out_bytes[j])) return MB_ERR_OVERLAP;
     }
-    if (h_out && overlaps(out, big, h_out, big)) return MB_ERR_OVERLAP;
     bool aligned = true;
-    for (const void *p : {x, r, w, b, static_cast<const void *>(out),
+    for (const void *q : {x, r, w, b, static_cast<const void *>(out),
                           static_cast<const void *>(h_out)})
-        aligned = aligned && (!p || aligned_to(p, 16));
+        aligned = aligned && (!q || aligned_to(q, 16));
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
-    if (dtype == MB_F32)
-        return lnact_rows_f32(ctx, g_tuning, r != nullptr, x, r, w, b, out, h_out, rows,
-                              (int)hidden, eps, (int)act, aligned, nullptr, true);
-    return lnact_rows_bf16(ctx, g_tuning, r != nullptr, x, r, w, b, out, h_out, rows,
-                           (int)hidden, eps, (int)act, aligned, nullptr, true);
+    LnExtras ex;
+    ex.mean = mean_out;
+    ex.rstd = rstd_out;
+    ex.p = p;
+    ex.seed = seed;
+    ex.offset = offset;
+    const bool drop = p > 0.0f;
+    auto fn = dtype == MB_F32 ? (drop ? lnact_drop_rows_f32 : lnact_rows_f32)
+                              : (drop ? lnact_drop_rows_bf16 : lnact_rows_bf16);
+    return fn(ctx, g_tuning, r != nullptr, x, r, w, b, out, h_out, rows, (int)hidden, eps,
+              (int)act, ex, aligned, nullptr, true);
 }
 
 mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols, mb_dtype dtype,
@@ -360,7 +386,7 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll) {
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int aligned,
                       int32_t out[7]) {
     if (!out) return MB_ERR_NULL;
-    if (chain < 0 || chain > 4) return MB_ERR_VALUE;
+    if (chain < 0 || chain > 6) return MB_ERR_VALUE;
     if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
     mb_status st = check_rows(rows, cols);
     if (st != MB_OK) return st;
@@ -377,7 +403,11 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
     else if (chain == 2 || chain == 3)
         st = (dtype == MB_F32 ? lnact_rows_f32 : lnact_rows_bf16)(
             ctx, g_tuning, chain == 2, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
-            (int)cols, 0.0f, 0, al, &p, false);
+            (int)cols, 0.0f, 0, LnExtras{}, al, &p, false);
+    else if (chain == 5 || chain == 6)
+        st = (dtype == MB_F32 ? lnact_drop_rows_f32 : lnact_drop_rows_bf16)(
+            ctx, g_tuning, chain == 5, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+            (int)cols, 0.0f, 0, LnExtras{}, al, &p, false);
     else if (chain == 4)
         st = softmax_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, al, &p, false);
     else if (dtype == MB_F32)

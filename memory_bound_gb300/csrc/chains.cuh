@@ -119,9 +119,10 @@ template <typename TT> struct LnGeluChain {
     __device__ __forceinline__ static float stat2(float m2, int cols, const Args &a) {
         return rsqrtf(m2 / (float)cols + a.eps);
     }
+    __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,
-                                                const PostPC<VEC> &pc, const Args &,
+                                                const PostPC<VEC> &pc, const Args &, int64_t,
                                                 float (&o)[VEC]) {
         ln_affine_act<T, VEC, 2>(v, rstd, pc.w, pc.b, o);
     }
@@ -192,9 +193,10 @@ template <typename TT> struct InductorChainT {
     template <int VEC>
     __device__ __forceinline__ static float p2(float (&)[VEC], float) { return 0.0f; }
     __device__ __forceinline__ static float stat2(float, int, const Args &) { return 0.0f; }
+    __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
-                                                const PostPC<VEC> &pc, const Args &,
+                                                const PostPC<VEC> &pc, const Args &, int64_t,
                                                 float (&o)[VEC]) {
         if constexpr (VEC == 1) {
             o[0] = __fadd_rn(__fmul_rn(__fsub_rn(v[0], mean), pc.gamma.f[0]), pc.beta.f[0]);
@@ -214,12 +216,14 @@ template <typename TT> struct InductorChainT {
 using InductorChain = InductorChainT<float>;
 
 // LayerNorm family: v = x (+ r); optionally h = v written out (the residual
-// stream); out = act((v - mean) * rstd * w + b), act none / relu / gelu-tanh.
+// stream); out = act((v - mean) * rstd * w + b), act none / relu / gelu-tanh;
+// with DROP, dropout on out (§2.1 of the same page: LayerNorm -> ReLU ->
+// Dropout in one kernel); optionally the per-row mean and rstd written out.
 // "Kernel fusion" course chapter 4 (5688vip.com) §4.3 (LayerNorm, two-pass
 // variance); "Operator fusion and kernel optimisation" (plumephp.com) §2.1
 // (LayerNorm -> ReLU in one kernel) and §2.2-2.3 (residual + LayerNorm + GeLU).
 enum { kActNone = 0, kActRelu = 1, kActGelu = 2 };
-template <typename TT, bool RES> struct LnActChain {
+template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     using T = TT;
     static constexpr int kInputs = RES ? 2 : 1;
     static constexpr bool kTwoPass = true;
@@ -233,6 +237,9 @@ template <typename TT, bool RES> struct LnActChain {
         T *h;          // residual-stream output (NULL: not written)
         float eps;
         int act;
+        float *mean_out;   // per-row mean (NULL: not written)
+        float *rstd_out;   // per-row 1/sqrt(var + eps) (NULL: not written)
+        DropoutArgs drop;  // used with DROP only
     };
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
@@ -278,10 +285,17 @@ template <typename TT, bool RES> struct LnActChain {
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,
                                                 const PostPC<VEC> &pc, const Args &a,
-                                                float (&o)[VEC]) {
+                                                int64_t off, float (&o)[VEC]) {
         if (a.act == kActGelu) ln_affine_act<T, VEC, 2>(v, rstd, pc.w, pc.b, o);
         else if (a.act == kActRelu) ln_affine_act<T, VEC, 1>(v, rstd, pc.w, pc.b, o);
         else ln_affine_act<T, VEC, 0>(v, rstd, pc.w, pc.b, o);
+        if constexpr (DROP) dropout_slot<VEC>(o, off, a.drop);
+    }
+    // the row's mean and rstd, written by one thread per row when asked for
+    __device__ __forceinline__ static void store_stats(const Args &a, int64_t row, float mean,
+                                                       float rstd) {
+        if (a.mean_out) a.mean_out[row] = mean;
+        if (a.rstd_out) a.rstd_out[row] = rstd;
     }
 };
 
@@ -339,9 +353,10 @@ template <typename TT> struct SoftmaxChain {
     __device__ __forceinline__ static float stat2(float sum, int, const Args &) {
         return 1.0f / sum;
     }
+    __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,
-                                                const PostPC<VEC> &, const Args &,
+                                                const PostPC<VEC> &, const Args &, int64_t,
                                                 float (&o)[VEC]) {
         if constexpr (VEC == 1) {
             o[0] = v[0] * inv;

@@ -79,6 +79,78 @@ __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 relu2(float2 a) { return make_float2(relu_f(a.x), relu_f(a.y)); }
 
 // ---------------------------------------------------------------------------
+// counter-based random numbers for dropout
+// ---------------------------------------------------------------------------
+
+// Philox-4x32-10 ("Parallel random numbers: as easy as 1, 2, 3", Salmon,
+// Moraes, Dror and Shaw, SC'11): ten rounds over a 4-word counter; each round
+// takes the full 64-bit products of words 0 and 2 with the two multipliers and
+// forms (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)),
+// with the key bumped by the Weyl constants (golden ratio and sqrt(3) - 1)
+// before every round but the first.
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
+// Dropout parameters, prepared on the host.  The round keys are the key
+// schedule written out (rk[2r], rk[2r + 1] = key + r (W0, W1)), so the kernel
+// reads them as launch constants.  Element i takes word i mod 4 of the block at
+// counter (0, 0, lo(g), hi(g)), g = offset + i / 4, and is kept iff its top 24
+// bits, as a fraction of 2^24, are >= p: iff word >= thr = ceil(p 2^24) 2^8
+// (the same decision, taken exactly in integers).  Kept values are scaled by
+// inv_keep = 1 / (1 - p); dropped ones are multiplied by 0.
+struct DropoutArgs {
+    uint32_t rk[20];
+    uint64_t offset;
+    uint32_t thr;
+    float inv_keep;
+};
+
+// The block at counter (0, 0, lo(g), hi(g)).
+__device__ __forceinline__ uint4 philox_block(uint64_t g, const DropoutArgs &d) {
+    uint32_t c0 = 0u, c1 = 0u, c2 = (uint32_t)g, c3 = (uint32_t)(g >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)kPhiloxM0 * c0;
+        const uint64_t p1 = (uint64_t)kPhiloxM1 * c2;
+        c0 = (uint32_t)(p1 >> 32) ^ c1 ^ d.rk[2 * r];
+        c1 = (uint32_t)p1;
+        c2 = (uint32_t)(p0 >> 32) ^ c3 ^ d.rk[2 * r + 1];
+        c3 = (uint32_t)p0;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+__device__ __forceinline__ float keep_scale(uint32_t word, const DropoutArgs &d) {
+    return word >= d.thr ? d.inv_keep : 0.0f;
+}
+
+// Dropout over one slot of VEC values whose first element has index `off`
+// in the whole tensor.  Vector slots start at a multiple of 4 (rows hold a
+// multiple of VEC elements), so each group of four takes one block.
+template <int VEC>
+__device__ __forceinline__ void dropout_slot(float (&o)[VEC], int64_t off, const DropoutArgs &d) {
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const uint4 w = philox_block(d.offset + (uint64_t)(off >> 2) + (uint64_t)q, d);
+            o[4 * q + 0] *= keep_scale(w.x, d);
+            o[4 * q + 1] *= keep_scale(w.y, d);
+            o[4 * q + 2] *= keep_scale(w.z, d);
+            o[4 * q + 3] *= keep_scale(w.w, d);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int64_t i = off + e;
+            const uint4 w = philox_block(d.offset + (uint64_t)(i >> 2), d);
+            const int lane = (int)(i & 3);
+            const uint32_t word = lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
+            o[e] *= keep_scale(word, d);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // bf16 packing (raw 16-bit patterns, little-endian pairs in 32-bit words)
 // ---------------------------------------------------------------------------
 

@@ -76,14 +76,28 @@ mb_status inductor_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const v
                              const void *bias, const void *gamma, const void *beta, void *y,
                              int64_t rows, int cols, float x_scale, float branch_scale,
                              bool aligned, RowPlan *plan, bool launch);
-mb_status lnact_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, bool residual,
-                         const void *x, const void *r, const void *w, const void *b, void *out,
-                         void *h, int64_t rows, int cols, float eps, int act, bool aligned,
-                         RowPlan *plan, bool launch);
-mb_status lnact_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, bool residual,
-                          const void *x, const void *r, const void *w, const void *b, void *out,
-                          void *h, int64_t rows, int cols, float eps, int act, bool aligned,
-                          RowPlan *plan, bool launch);
+// Optional extras of the LayerNorm family: per-row statistics out (NULL: not
+// written) and dropout with probability p (0: none) keyed by (seed, offset).
+struct LnExtras {
+    float *mean = nullptr;
+    float *rstd = nullptr;
+    float p = 0.0f;
+    uint64_t seed = 0;
+    uint64_t offset = 0;
+};
+
+// LayerNorm family launches: fp32 / bf16 I/O, without dropout (lnact_rows_*)
+// and with it (lnact_drop_rows_*, p > 0).
+#define MB_LNACT_DECL(name)                                                              \
+    mb_status name(const LaunchCtx &ctx, const RowTuning &tun, bool residual, const void *x, \
+                   const void *r, const void *w, const void *b, void *out, void *h,          \
+                   int64_t rows, int cols, float eps, int act, const LnExtras &ex,           \
+                   bool aligned, RowPlan *plan, bool launch)
+MB_LNACT_DECL(lnact_rows_f32);
+MB_LNACT_DECL(lnact_rows_bf16);
+MB_LNACT_DECL(lnact_drop_rows_f32);
+MB_LNACT_DECL(lnact_drop_rows_bf16);
+#undef MB_LNACT_DECL
 mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
                        const void *x, void *y, int64_t rows, int cols, bool aligned,
                        RowPlan *plan, bool launch);

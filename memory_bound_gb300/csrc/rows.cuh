@@ -6,8 +6,10 @@
 //   s1    = C::stat1(R1, cols, args), R1 = sum(v), or max(v) with C::kMaxFirst
 //   s2    = C::stat2(R2, cols, args) with C::kTwoPass, where R2 sums the
 //           per-slot partials C::p2 forms from v and s1 (p2 may rewrite v)
-//   post  (per element)   the epilogue from v, s1, s2 and its per-column
-//                         values (PostPC)
+//   post  (per element)   the epilogue from v, s1, s2, its per-column
+//                         values (PostPC) and the index of the slot's first
+//                         element in the whole tensor
+//   store_stats           one thread per row may write s1 and s2 out
 // and, with C::kStorePre, store_pre writes the prologue value v out as well
 // (the residual-stream output of a residual + LayerNorm block).
 // The row is read from device memory once and held in registers (v) between
@@ -116,12 +118,13 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             }
             rstd = C::stat2(warp_sum(l2), cols, a);
         }
+        if (lane == 0) C::store_stats(a, row, mean, rstd);
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int vi = lane + 32 * k;
             if (vi < nvec) {
                 Frag<T, VEC> o;
-                C::template post<VEC>(v[k], mean, rstd, post[k], a, o.f);
+                C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, o.f);
                 o.store_stream(a.out + base + vi * VEC);
             }
         }
@@ -249,17 +252,18 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             rstd = C::stat2(block_sum(l2, red + 32 * rb), cols, a);
             rb ^= 1;
         }
+        if (tid == 0) C::store_stats(a, row, mean, rstd);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vi = tid + k * blockDim.x;
             if (vi < nvec) {
                 Frag<T, VEC> o;
                 if constexpr (kEarlyPost) {
-                    C::template post<VEC>(v[k], mean, rstd, post[k], a, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, o.f);
                 } else {
                     PostPC pc;
                     C::template load_post<VEC>(a, vi * VEC, pc);
-                    C::template post<VEC>(v[k], mean, rstd, pc, a, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, o.f);
                 }
                 o.store_stream(a.out + base + vi * VEC);
             }
@@ -390,17 +394,18 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
             rstd = C::stat2(cluster_reduce<false>(c2, &xch[xb], cl), cols, a);
             xb ^= 1;
         }
+        if (rank == 0 && tid == 0) C::store_stats(a, row, mean, rstd);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vi = tid + k * blockDim.x;
             if (vi < nvec) {
                 Frag<T, VEC> o;
                 if constexpr (kEarlyPost) {
-                    C::template post<VEC>(v[k], mean, rstd, post[k], a, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, o.f);
                 } else {
                     PostPC pc;
                     C::template load_post<VEC>(a, lo + vi * VEC, pc);
-                    C::template post<VEC>(v[k], mean, rstd, pc, a, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, o.f);
                 }
                 o.store_stream(a.out + base + vi * VEC);
             }

@@ -10,8 +10,8 @@ Shapes and distributions are the pages' example workloads:
 * residual + LayerNorm + GeLU-tanh rows ([P2] §2.3) at hidden 4096 fp32 and
   hidden 8192 bf16;
 * for the further chains (NEXT): row softmax on [P1] §4.1's attention-score
-  matrix, the LayerNorm family with a residual-stream output or a ReLU, and
-  the TorchInductor chain in bf16.
+  matrix, the LayerNorm family with a residual-stream output or a ReLU, the
+  TorchInductor chain in bf16, and [P2] §2.1's LayerNorm -> ReLU -> Dropout.
 
 N(mu, s) takes ``s`` as the standard deviation.  Tensor ids are assigned in
 the order each workload lists its tensors.
@@ -130,7 +130,13 @@ LNACT_RELU_F32 = Workload("lnact_relu_f32_8192x4096", "lnact", "f32", 8192, 4096
 ), {"eps": 1e-5, "act": "relu", "residual": False, "write_h": False})
 INDUCTOR_BF16 = Workload("inductor_bf16_1024x1024", "inductor", "bf16", 1024, 1024, 8,
                          INDUCTOR_1024.tensors, {"x_scale": 1.1, "branch_scale": 0.1})
-NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16)
+# "Operator fusion and kernel optimisation" §2.1: LayerNorm -> ReLU ->
+# Dropout(p = 0.1) in one kernel, fp32, on the same rows as the plain chain.
+LNACT_RELU_DROP_F32 = Workload("lnact_relu_dropout_f32_8192x4096", "lnact", "f32", 8192, 4096, 9,
+                               LNACT_RELU_F32.tensors,
+                               {"eps": 1e-5, "act": "relu", "residual": False, "write_h": False,
+                                "p": 0.1, "seed": 2024, "offset": 0})
+NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16, LNACT_RELU_DROP_F32)
 
 ALL = (POINTWISE_TINY, POINTWISE_4M, INDUCTOR_1024, LN_F32, LN_BF16)
 BY_NAME = {w.name: w for w in ALL + NEXT}

@@ -150,3 +150,24 @@ def test_further_chains_argument_checks(lib):
     assert g(A, B, C, D, E, 0, 64, 1.1, 0.1, None) == MB_OK
     assert g(A, B, C, D, A + 2, 2, 64, 1.1, 0.1, None) == MB_ERR_OVERLAP
     assert g(A + 1, B, C, D, E, 2, 64, 1.1, 0.1, None) == MB_ERR_ALIGN
+
+
+def test_layernorm_ex_argument_checks(lib):
+    """Dropout probability, statistics pointers and their overlaps are all
+    checked on the host."""
+    f = lib.fused_layernorm_act_ex
+    F = 0x60000000                                  # statistics buffers
+    G = F + 0x1000
+    nan = float("nan")
+    assert f(A, B, C, D, E, None, F, G, 0, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_OK
+    for p in (-0.1, 1.0, 1.5, nan):
+        assert f(A, B, C, D, E, None, None, None, 4, 64, 1e-5, 1, p, 1, 0, 0, None) == MB_ERR_VALUE
+    assert f(A, B, C, D, E, None, F + 2, None, 4, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_ERR_ALIGN
+    assert f(A, B, C, D, E, None, None, G + 1, 4, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_ERR_ALIGN
+    assert f(A, B, C, D, E, None, A + 8, None, 4, 64, 1e-5, 1, 0.0, 1, 0, 0, None) == MB_ERR_OVERLAP
+    assert f(A, B, C, D, E, None, E + 16, None, 4, 64, 1e-5, 1, 0.0, 1, 0, 0, None) == MB_ERR_OVERLAP
+    assert f(A, B, C, D, E, None, F, F + 8, 4, 64, 1e-5, 1, 0.0, 1, 0, 0, None) == MB_ERR_OVERLAP
+    assert f(A, B, C, D, E, F, None, F + 64, 4, 64, 1e-5, 1, 0.0, 1, 0, 0, None) == MB_ERR_OVERLAP
+    assert f(A, B, C, D, E, None, None, None, 4, 64, 1e-5, 7, 0.1, 1, 0, 0, None) == MB_ERR_VALUE
+    assert f(None, B, C, D, E, None, F, G, 4, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_ERR_NULL
+    assert lib.mb_row_plan(7, 0, 4, 64, 1, (ctypes.c_int32 * 7)()) == MB_ERR_VALUE

@@ -114,3 +114,26 @@ def test_softmax_rows_beyond_2_31():
     got = to_host(y[torch.from_numpy(rows_s).cuda()]).astype(np.float64)
     want = oracle.row_softmax(x_b[rows_s % B]).astype(np.float64)
     assert np.all(np.abs(got - want) <= 1e-5 * want + 2.0 ** -126)
+
+
+def test_layernorm_dropout_rows_beyond_2_31():
+    """Dropout decisions keyed by element indices past 2^31 (the Philox
+    counter takes the 64-bit index): sampled rows' masks and values."""
+    cols = 4096
+    rows = TWO31 // cols + 3
+    B = 991
+    x_b = synth.normal(1005, 0, (B, cols))
+    w = synth.uniform(1005, 2, (cols,), 0.5, 1.5)
+    b = synth.normal(1005, 3, (cols,), 0.0, 0.1)
+    x = _tile(x_b, rows)
+    p, seed, offset = 0.1, 31337, 12
+    out = mb.fused_layernorm_act(x, None, to_dev(w), to_dev(b), act="relu", p=p, seed=seed,
+                                 offset=offset)
+    rows_s = np.unique(np.r_[_sample(rows, 16), [TWO31 // cols - 1, TWO31 // cols]])
+    got = to_host(out[torch.from_numpy(rows_s).cuda()]).astype(np.float64)
+    plain = oracle.layernorm_act(x_b[rows_s % B], None, w, b, 1e-5, oracle.ACT_RELU)
+    for k, row in enumerate(rows_s):
+        keep = oracle.dropout_mask(seed, offset, int(row) * cols, cols, p)
+        want = np.where(keep, plain[k].astype(np.float64) / (1 - p), 0.0)
+        assert np.all(got[k][~keep] == 0), row
+        assert np.all(np.abs(got[k] - want) <= 2e-5 * np.maximum(np.abs(want), 1.0)), row

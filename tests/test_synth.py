@@ -82,7 +82,7 @@ def test_golden_first_values():
             assert got == gold[w.name][t.name], (w.name, t.name)
 
 
-@pytest.mark.parametrize("w", W.ALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", W.ALL + W.NEXT, ids=lambda w: w.name)
 def test_workload_ideal_bytes(w):
     # read-once / write-once bytes of one call, from the workload shapes
     want = {
@@ -91,5 +91,10 @@ def test_workload_ideal_bytes(w):
         "inductor_f32_1024x1024": 2 * 1024 * 1024 * 4 + 3 * 1024 * 4,
         "ln_gelu_f32_8192x4096": 3 * 8192 * 4096 * 4 + 2 * 4096 * 4,
         "ln_gelu_bf16_32768x8192": 3 * 32768 * 8192 * 2 + 2 * 8192 * 2,
+        "softmax_f32_131072x4096": 2 * 131072 * 4096 * 4,
+        "lnact_res_h_bf16_32768x8192": 4 * 32768 * 8192 * 2 + 2 * 8192 * 2,
+        "lnact_relu_f32_8192x4096": 2 * 8192 * 4096 * 4 + 2 * 4096 * 4,
+        "inductor_bf16_1024x1024": 2 * 1024 * 1024 * 2 + 3 * 1024 * 2,
+        "lnact_relu_dropout_f32_8192x4096": 2 * 8192 * 4096 * 4 + 2 * 4096 * 4,
     }[w.name]
     assert w.ideal_bytes() == want
