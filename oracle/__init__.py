@@ -85,6 +85,12 @@ def load(path=None):
     lib.oracle_layernorm_act_bf16.argtypes = [
         U16P, U16P, U16P, U16P, U16P, U16P, i64, i64, f32, ctypes.c_int]
     lib.oracle_layernorm_act_bf16.restype = None
+    lib.oracle_add_relu_scale_bcast_f32.argtypes = [
+        F32P, F32P, F32P, F32P, i64, i64, ctypes.c_int, ctypes.c_int, f32]
+    lib.oracle_add_relu_scale_bcast_f32.restype = None
+    lib.oracle_add_relu_scale_bcast_bf16.argtypes = [
+        U16P, U16P, U16P, U16P, i64, i64, ctypes.c_int, ctypes.c_int, f32]
+    lib.oracle_add_relu_scale_bcast_bf16.restype = None
     u64 = ctypes.c_uint64
     lib.oracle_layernorm_act_ex_f32.argtypes = [
         F32P, F32P, F32P, F32P, F32P, F32P, F64P, F64P, i64, i64, f32, ctypes.c_int, f32,
@@ -169,6 +175,32 @@ def add_relu_scale(x, b1, b2, scale=0.5, lib=None):
 # --------------------------------------------------------------------------
 # o2: TorchInductor example chain   ([P4] "model", Figure 1)
 # --------------------------------------------------------------------------
+
+def add_relu_scale_bcast(x, b1, b2, scale=0.5, lib=None):
+    """The pointwise chain on a 2-D x (rows, cols); b1 and b2 each either the
+    shape of x or a length-cols vector broadcast over the rows."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    if x.dtype == np.float32:
+        cv, fn, ptr = np.float32, lib.oracle_add_relu_scale_bcast_f32, _f32p
+    elif x.dtype == np.uint16:
+        cv, fn, ptr = np.uint16, lib.oracle_add_relu_scale_bcast_bf16, _u16p
+    else:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    b1, b2 = _c(b1, cv), _c(b2, cv)
+    flags = []
+    for v in (b1, b2):
+        if v.shape == x.shape:
+            flags.append(0)
+        elif v.shape == (cols,):
+            flags.append(1)
+        else:
+            raise ValueError("b1 / b2 must have x's shape or (cols,)")
+    y = np.empty_like(x)
+    fn(ptr(x), ptr(b1), ptr(b2), ptr(y), rows, cols, flags[0], flags[1], scale)
+    return y
+
 
 def bias_relu_branch_mean_epilogue(x, bias, gamma, beta, x_scale=1.1,
                                    branch_scale=0.1, intermediates=False,

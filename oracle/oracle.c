@@ -135,6 +135,45 @@ void oracle_add_relu_scale_bf16(const uint16_t *x, const uint16_t *b1,
     }
 }
 
+/* o1 over rows x cols with b1 and/or b2 given per column (a length-cols
+ * vector broadcast over the rows, as a bias is) */
+static float o1_operand(const void *v, int bf16, int per_col, int64_t i, int64_t j,
+                        int64_t cols)
+{
+    int64_t k = per_col ? j : i * cols + j;
+    return bf16 ? widen_bf16(((const uint16_t *)v)[k]) : ((const float *)v)[k];
+}
+
+static void o1_bcast(const void *x, const void *b1, const void *b2, void *y, int bf16,
+                     int64_t rows, int64_t cols, int b1_per_col, int b2_per_col, float scale)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < cols; ++j) {
+            float xv = o1_operand(x, bf16, 0, i, j, cols);
+            float r = o1_element(xv, o1_operand(b1, bf16, b1_per_col, i, j, cols),
+                                 o1_operand(b2, bf16, b2_per_col, i, j, cols), scale);
+            if (bf16)
+                ((uint16_t *)y)[i * cols + j] = oracle_bf16_from_double((double)r);
+            else
+                ((float *)y)[i * cols + j] = r;
+        }
+    }
+}
+
+void oracle_add_relu_scale_bcast_f32(const float *x, const float *b1, const float *b2,
+                                     float *y, int64_t rows, int64_t cols, int b1_per_col,
+                                     int b2_per_col, float scale)
+{
+    o1_bcast(x, b1, b2, y, 0, rows, cols, b1_per_col, b2_per_col, scale);
+}
+
+void oracle_add_relu_scale_bcast_bf16(const uint16_t *x, const uint16_t *b1,
+                                      const uint16_t *b2, uint16_t *y, int64_t rows,
+                                      int64_t cols, int b1_per_col, int b2_per_col, float scale)
+{
+    o1_bcast(x, b1, b2, y, 1, rows, cols, b1_per_col, b2_per_col, scale);
+}
+
 /* ------------------------------------------------------------------------ */
 /* o2: TorchInductor example chain, [P4] "model" and Figure 1               */
 /* ------------------------------------------------------------------------ */

@@ -52,6 +52,17 @@ void oracle_add_relu_scale_bf16(const uint16_t *x, const uint16_t *b1,
                                 const uint16_t *b2, uint16_t *y, int64_t n,
                                 float scale);
 
+/* ---- o1 over rows x cols with b1 and/or b2 per column: a length-cols vector
+ * broadcast over the rows when the flag is set, else a full rows x cols
+ * tensor; the same four fp32 steps per element (bf16: widened inputs, y
+ * rounded once). */
+void oracle_add_relu_scale_bcast_f32(const float *x, const float *b1, const float *b2,
+                                     float *y, int64_t rows, int64_t cols, int b1_per_col,
+                                     int b2_per_col, float scale);
+void oracle_add_relu_scale_bcast_bf16(const uint16_t *x, const uint16_t *b1,
+                                      const uint16_t *b2, uint16_t *y, int64_t rows,
+                                      int64_t cols, int b1_per_col, int b2_per_col, float scale);
+
 /* ---- o2: TorchInductor example chain ([P4] "model", Figure 1, §6.4) ----
  *   t = x*x_scale + bias; a = relu(t); p = a*a; q = a*branch_scale;
  *   s = p + q; m = mean(s, dim=1); y = (s - m)*gamma + beta

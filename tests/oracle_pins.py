@@ -450,6 +450,28 @@ def pin_softmax_bf16(lib):
     assert np.all(np.abs(g - want) <= 2.0 ** -8 * want * 1.0001 + 1e-40)
 
 
+def pin_pointwise_bcast_library(lib):
+    """Per-column b1 / b2 ([P1]'s chain with bias-like operands): torch CPU
+    eager fp32 with broadcasting, bit for bit, for every flag combination;
+    bf16 against torch's widen / fp32 ops / round-to-nearest-even."""
+    rows, cols = 37, 129
+    x = synth.normal(81, 0, (rows, cols))
+    full = [synth.normal(81, 1, (rows, cols)), synth.normal(81, 2, (rows, cols))]
+    vec = [synth.normal(81, 3, (cols,)), synth.normal(81, 4, (cols,))]
+    for f1 in (0, 1):
+        for f2 in (0, 1):
+            b1 = vec[0] if f1 else full[0]
+            b2 = vec[1] if f2 else full[1]
+            t = torch.relu(torch.from_numpy(x) + torch.from_numpy(b1)) * 0.75 + torch.from_numpy(b2)
+            got = oracle.add_relu_scale_bcast(x, b1, b2, 0.75, lib=lib)
+            assert np.array_equal(_bits(got), _bits(t.numpy())), (f1, f2)
+    xb, v1, v2 = (synth.f32_to_bf16_bits(a) for a in (x, vec[0], vec[1]))
+    wide = [torch.from_numpy(synth.bf16_bits_to_f32(a)) for a in (xb, v1, v2)]
+    t = (torch.relu(wide[0] + wide[1]) * 0.5 + wide[2]).to(torch.bfloat16)
+    got = oracle.add_relu_scale_bcast(xb, v1, v2, 0.5, lib=lib)
+    assert np.array_equal(got, t.view(torch.int16).numpy().view(np.uint16))
+
+
 # --------------------------------------------------------------------------
 # o4 extras and o6: row statistics, the Philox generator, dropout
 # --------------------------------------------------------------------------

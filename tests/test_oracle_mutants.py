@@ -27,6 +27,10 @@ MUTANTS = {
                "    tmp = tmp + b2;",
                "tmp = fmaf(tmp, scale, b2);"),
     "relu_keeps_neg_zero": ("if (v > 0.0f)", "if (v >= 0.0f)"),
+    "o1_bcast_row_index": ("int64_t k = per_col ? j : i * cols + j;",
+                           "int64_t k = per_col ? i % cols : i * cols + j;"),
+    "o1_bcast_flags_swapped": ("o1_operand(b1, bf16, b1_per_col, i, j, cols)",
+                               "o1_operand(b1, bf16, b2_per_col, i, j, cols)"),
     # o2: TorchInductor example chain
     "o2_mean_divisor": ("float m = (float)(sum / (double)cols);",
                         "float m = (float)(sum / (double)(cols + 1));"),
