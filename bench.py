@@ -216,7 +216,7 @@ class Case:
         import memory_bound_gb300 as mb
         d, out = self.sets[k % self.nsets], self.outs[k % self.nsets]
         p = self.w.params
-        if self.w.chain == "add_relu_scale":
+        if self.w.chain in ("add_relu_scale", "add_relu_scale_bcast"):
             mb.fused_add_relu_scale(d["x"], d["b1"], d["b2"], p["scale"], out=out)
         elif self.w.chain == "inductor":
             mb.fused_bias_relu_branch_mean_epilogue(d["x"], d["bias"], d["gamma"], d["beta"],
@@ -251,7 +251,7 @@ class Case:
         import torch
         import torch.nn.functional as F
         d, p = self.sets[k % self.nsets], self.w.params
-        if self.w.chain == "add_relu_scale":
+        if self.w.chain in ("add_relu_scale", "add_relu_scale_bcast"):
             return torch.relu(d["x"] + d["b1"]) * p["scale"] + d["b2"]
         if self.w.chain == "softmax":
             return torch.softmax(d["x"], dim=1)

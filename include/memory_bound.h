@@ -9,10 +9,12 @@
  *   fused_bias_relu_branch_mean_epilogue  the TorchInductor example chain
  *   fused_residual_layernorm_gelu         GeLU_tanh(LayerNorm(x + r) * w + b)
  *
- * and, built on the same row engines: fused_layernorm_act (LayerNorm with an
- * optional residual, residual-stream output and activation) and its extended
- * form fused_layernorm_act_ex (dropout, per-row statistics), fused_row_softmax
- * and the bf16 variant of the TorchInductor chain.
+ * with the broadcast form of the first, fused_add_relu_scale_bcast
+ * (per-column b1 / b2), and, built on the same row engines,
+ * fused_layernorm_act (LayerNorm with an optional residual, residual-stream
+ * output and activation) and its extended form fused_layernorm_act_ex
+ * (dropout, per-row statistics), fused_row_softmax and the bf16 variant of the
+ * TorchInductor chain.
  *
  * Sources (the pages these chains come from):
  *   [P1] "PyTorch operator fusion in practice", www.0539edu.com/news/5489619
@@ -140,6 +142,27 @@ mb_status fused_bias_relu_branch_mean_epilogue(const float *x, const float *bias
                                                int64_t rows, int64_t cols,
                                                float x_scale, float branch_scale,
                                                cudaStream_t stream);
+
+/*
+ * The pointwise chain over rows x cols with b1 and / or b2 given per column:
+ *   y[i, j] = relu(x[i, j] + B1(i, j)) * scale + B2(i, j),
+ *   Bk(i, j) = bk[j] when bk_per_col (a length-cols vector broadcast over the
+ *   rows, as a bias is), else bk[i * cols + j].
+ * [P1] §3.1's chain with bias-like operands; the same four fp32 steps per
+ * element, each rounded on its own, so fp32 results are bit-identical to the
+ * eager ops with broadcasting (bf16: inputs widened exactly, y rounded once).
+ *
+ *   x, y        rows x cols
+ *   b1, b2      cols values when the flag is 1, rows x cols when it is 0
+ *   b1_per_col, b2_per_col   0 or 1, else MB_ERR_VALUE; with both 0 this is
+ *               fused_add_relu_scale over rows * cols elements
+ *   rows >= 0 (0: no-op), 1 <= cols <= INT32_MAX, else MB_ERR_SHAPE
+ *   y may not overlap x, b1 or b2 (MB_ERR_OVERLAP).
+ */
+mb_status fused_add_relu_scale_bcast(const void *x, const void *b1, const void *b2, void *y,
+                                     int64_t rows, int64_t cols, int b1_per_col,
+                                     int b2_per_col, float scale, mb_dtype dtype,
+                                     cudaStream_t stream);
 
 /*
  * out = GeLU_tanh(LayerNorm(x + r) * w + b), row by row over rows x hidden:

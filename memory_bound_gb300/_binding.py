@@ -20,6 +20,7 @@ _P, _I64, _F, _I, _U32P, _I32P = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_floa
                                   ctypes.POINTER(ctypes.c_int32))
 SIGNATURES = {
     "fused_add_relu_scale": (_I, [_P, _P, _P, _P, _I64, _F, _I, _P]),
+    "fused_add_relu_scale_bcast": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _F, _I, _P]),
     "fused_bias_relu_branch_mean_epilogue": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _F, _P]),
     "fused_residual_layernorm_gelu": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]),
     "fused_bias_relu_branch_mean_epilogue_bf16": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _F, _F, _P]),
@@ -180,17 +181,38 @@ def _require(tensors, dtype):
 
 
 def fused_add_relu_scale(x, b1, b2, scale=0.5, out=None):
-    """y = relu(x + b1) * scale + b2, elementwise (float32 or bfloat16)."""
+    """y = relu(x + b1) * scale + b2, elementwise (float32 or bfloat16).
+
+    b1 and b2 each have x's size, or (bias-like) the size of x's last
+    dimension, broadcast over the leading ones."""
     if out is None:
         out = _empty_like(x)
     dev = _require([x, b1, b2, out], x.dtype)
-    if not (x.numel() == b1.numel() == b2.numel() == out.numel()):
-        raise ValueError("x, b1, b2 and out must have one size")
+    n = x.numel()
+    if out.numel() != n:
+        raise ValueError("out must have x's size")
+    if b1.numel() == n and b2.numel() == n:
+        with _on_device(dev):
+            st = load_library().fused_add_relu_scale(
+                x.data_ptr(), b1.data_ptr(), b2.data_ptr(), out.data_ptr(), n,
+                float(scale), _dtype_code(x), _stream_handle(dev))
+        _check("fused_add_relu_scale", st)
+        return out
+    cols = x.shape[-1] if x.dim() > 0 else 1
+    flags = []
+    for v in (b1, b2):
+        if v.numel() == n:
+            flags.append(0)
+        elif v.numel() == cols:
+            flags.append(1)
+        else:
+            raise ValueError("b1 / b2 must have x's size or its last dimension's")
+    rows = n // cols if cols else 0
     with _on_device(dev):
-        st = load_library().fused_add_relu_scale(
-            x.data_ptr(), b1.data_ptr(), b2.data_ptr(), out.data_ptr(), x.numel(),
-            float(scale), _dtype_code(x), _stream_handle(dev))
-    _check("fused_add_relu_scale", st)
+        st = load_library().fused_add_relu_scale_bcast(
+            x.data_ptr(), b1.data_ptr(), b2.data_ptr(), out.data_ptr(), rows, cols, flags[0],
+            flags[1], float(scale), _dtype_code(x), _stream_handle(dev))
+    _check("fused_add_relu_scale_bcast", st)
     return out
 
 

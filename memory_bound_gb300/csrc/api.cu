@@ -155,6 +155,37 @@ mb_status fused_add_relu_scale(const void *x, const void *b1, const void *b2, vo
     return add_relu_scale_run(ctx, g_pw_tuning, dtype, x, b1, b2, y, n, scale, vec, (int)head);
 }
 
+mb_status fused_add_relu_scale_bcast(const void *x, const void *b1, const void *b2, void *y,
+                                     int64_t rows, int64_t cols, int b1_per_col,
+                                     int b2_per_col, float scale, mb_dtype dtype,
+                                     cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
+    if (rows < 0 || cols < 1 || cols > INT32_MAX || rows > INT64_MAX / 8 / cols)
+        return MB_ERR_SHAPE;
+    if ((b1_per_col != 0 && b1_per_col != 1) || (b2_per_col != 0 && b2_per_col != 1))
+        return MB_ERR_VALUE;
+    if (!std::isfinite(scale)) return MB_ERR_VALUE;
+    if (rows == 0) return MB_OK;
+    if (!x || !b1 || !b2 || !y) return MB_ERR_NULL;
+    const int es = elem_size(dtype);
+    for (const void *p : {x, b1, b2, static_cast<const void *>(y)})
+        if (!aligned_to(p, es)) return MB_ERR_ALIGN;
+    const int64_t big = rows * cols * es, small = cols * es;
+    if (overlaps(y, big, x, big) || overlaps(y, big, b1, b1_per_col ? small : big) ||
+        overlaps(y, big, b2, b2_per_col ? small : big))
+        return MB_ERR_OVERLAP;
+    if (!b1_per_col && !b2_per_col)       // no broadcast: the plain chain
+        return fused_add_relu_scale(x, b1, b2, y, rows * cols, scale, dtype, stream);
+    bool vec = cols % (16 / es) == 0;
+    for (const void *p : {x, b1, b2, static_cast<const void *>(y)})
+        vec = vec && aligned_to(p, 16);
+    LaunchCtx ctx;
+    mb_status st = device_ctx(stream, &ctx);
+    if (st != MB_OK) return st;
+    return add_relu_scale_bcast_run(ctx, dtype, x, b1, b2, y, rows, cols, b1_per_col != 0,
+                                    b2_per_col != 0, scale, vec);
+}
+
 mb_status fused_residual_layernorm_gelu(const void *x, const void *r, const void *w,
                                         const void *b, void *out, int64_t rows,
                                         int64_t hidden, float eps, mb_dtype dtype,

@@ -69,6 +69,15 @@ __device__ __forceinline__ float gelu_tanh_f(float n) {
     return n * rcp_approx(1.0f + e);
 }
 
+// The pointwise chain's four fp32 steps, each rounded on its own (no
+// contraction), as the four eager ops round them.
+__device__ __forceinline__ float add_relu_scale_1(float x, float b1, float b2, float scale) {
+    float t = __fadd_rn(x, b1);       // x + b1
+    t = relu_f(t);                    // relu
+    t = __fmul_rn(t, scale);          // * scale
+    return __fadd_rn(t, b2);          // + b2
+}
+
 // Pairs of fp32 values through Blackwell's packed fp32x2 instructions: each
 // lane is an ordinary IEEE fp32 operation rounded to nearest, so results are
 // the same as two scalar operations, at half the instruction issue.

@@ -58,6 +58,12 @@ struct RowPlan {
 mb_status add_relu_scale_run(const LaunchCtx &ctx, const PointwiseTuning &tun, mb_dtype dtype,
                              const void *x, const void *b1, const void *b2, void *y, int64_t n,
                              float scale, bool vec, int head);
+// rows x cols with b1 / b2 per column where flagged; vec: 16-byte fragments
+// (every pointer 16-byte aligned and cols a multiple of the fragment length).
+mb_status add_relu_scale_bcast_run(const LaunchCtx &ctx, mb_dtype dtype, const void *x,
+                                   const void *b1, const void *b2, void *y, int64_t rows,
+                                   int64_t cols, bool b1_per_col, bool b2_per_col, float scale,
+                                   bool vec);
 
 mb_status ln_gelu_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                            const void *r, const void *w, const void *b, void *out,

@@ -14,13 +14,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ float add_relu_scale_1(float x, float b1, float b2, float scale) {
-    float t = __fadd_rn(x, b1);       // x + b1
-    t = relu_f(t);                    // relu
-    t = __fmul_rn(t, scale);          // * scale
-    return __fadd_rn(t, b2);          // + b2
-}
-
 // Elements [0, head) and [head + nvec*VEC, n) are done one by one by the
 // first threads of block 0; [head, head + nvec*VEC) by 16-byte fragments.
 // Block b owns the contiguous fragment range [b*chunk, (b+1)*chunk): every

@@ -11,7 +11,8 @@ Shapes and distributions are the pages' example workloads:
   hidden 8192 bf16;
 * for the further chains (NEXT): row softmax on [P1] §4.1's attention-score
   matrix, the LayerNorm family with a residual-stream output or a ReLU, the
-  TorchInductor chain in bf16, and [P2] §2.1's LayerNorm -> ReLU -> Dropout.
+  TorchInductor chain in bf16, [P2] §2.1's LayerNorm -> ReLU -> Dropout, and
+  the pointwise chain with per-column b1 / b2.
 
 N(mu, s) takes ``s`` as the standard deviation.  Tensor ids are assigned in
 the order each workload lists its tensors.
@@ -36,7 +37,8 @@ class Tensor:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    chain: str         # "add_relu_scale" | "inductor" | "ln_gelu" | "lnact" | "softmax"
+    chain: str         # "add_relu_scale" | "add_relu_scale_bcast" | "inductor" |
+    #                    "ln_gelu" | "lnact" | "softmax"
     dtype: str         # "f32" | "bf16"
     rows: int          # 1 for the pointwise chain
     cols: int          # n for the pointwise chain
@@ -136,7 +138,16 @@ LNACT_RELU_DROP_F32 = Workload("lnact_relu_dropout_f32_8192x4096", "lnact", "f32
                                LNACT_RELU_F32.tensors,
                                {"eps": 1e-5, "act": "relu", "residual": False, "write_h": False,
                                 "p": 0.1, "seed": 2024, "offset": 0})
-NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16, LNACT_RELU_DROP_F32)
+# The pointwise chain with bias-like operands: x [4096, 1024] (4 Mi fp32
+# elements, as the plain chain) and b1, b2 per column.
+POINTWISE_BCAST_F32 = Workload("pointwise_bcast_f32_4096x1024", "add_relu_scale_bcast", "f32",
+                               4096, 1024, 10, (
+                                   Tensor("x", 0, "normal", 0.0, 1.0, False),
+                                   Tensor("b1", 1, "normal", 0.0, 1.0, True),
+                                   Tensor("b2", 2, "normal", 0.0, 1.0, True),
+                               ), {"scale": 0.5})
+NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16, LNACT_RELU_DROP_F32,
+        POINTWISE_BCAST_F32)
 
 ALL = (POINTWISE_TINY, POINTWISE_4M, INDUCTOR_1024, LN_F32, LN_BF16)
 BY_NAME = {w.name: w for w in ALL + NEXT}

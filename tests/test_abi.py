@@ -171,3 +171,19 @@ def test_layernorm_ex_argument_checks(lib):
     assert f(A, B, C, D, E, None, None, None, 4, 64, 1e-5, 7, 0.1, 1, 0, 0, None) == MB_ERR_VALUE
     assert f(None, B, C, D, E, None, F, G, 4, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_ERR_NULL
     assert lib.mb_row_plan(7, 0, 4, 64, 1, (ctypes.c_int32 * 7)()) == MB_ERR_VALUE
+
+
+def test_pointwise_bcast_argument_checks(lib):
+    f = lib.fused_add_relu_scale_bcast
+    assert f(A, B, C, D, 0, 64, 1, 1, 0.5, 0, None) == MB_OK
+    assert f(A, B, C, D, 4, 0, 1, 1, 0.5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, 4, 1 << 31, 1, 1, 0.5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, -1, 64, 1, 1, 0.5, 0, None) == MB_ERR_SHAPE
+    assert f(A, B, C, D, 4, 64, 2, 1, 0.5, 0, None) == MB_ERR_VALUE
+    assert f(A, B, C, D, 4, 64, 1, 1, float("inf"), 0, None) == MB_ERR_VALUE
+    assert f(A, B, C, D, 4, 64, 1, 1, 0.5, 5, None) == MB_ERR_DTYPE
+    assert f(A, None, C, D, 4, 64, 1, 1, 0.5, 0, None) == MB_ERR_NULL
+    assert f(A + 2, B, C, D, 4, 64, 1, 1, 0.5, 0, None) == MB_ERR_ALIGN
+    assert f(A, B, C, A + 64, 4, 64, 1, 1, 0.5, 0, None) == MB_ERR_OVERLAP
+    # a per-column b1 occupies cols elements only; a full one rows * cols
+    assert f(A, D + 4 * 64, C, D, 4, 64, 0, 1, 0.5, 0, None) == MB_ERR_OVERLAP

@@ -96,5 +96,6 @@ def test_workload_ideal_bytes(w):
         "lnact_relu_f32_8192x4096": 2 * 8192 * 4096 * 4 + 2 * 4096 * 4,
         "inductor_bf16_1024x1024": 2 * 1024 * 1024 * 2 + 3 * 1024 * 2,
         "lnact_relu_dropout_f32_8192x4096": 2 * 8192 * 4096 * 4 + 2 * 4096 * 4,
+        "pointwise_bcast_f32_4096x1024": 2 * 4096 * 1024 * 4 + 2 * 1024 * 4,
     }[w.name]
     assert w.ideal_bytes() == want
