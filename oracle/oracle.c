@@ -28,8 +28,9 @@
  *   o6  Dropout ([P2] §2.1 LayerNorm -> ReLU -> Dropout): the pages fix no
  *       random number generator, so the decision of element i comes from the
  *       published Philox-4x32-10 counter-based generator at a counter fixed by
- *       (offset, i) and a key fixed by seed; kept elements are scaled by
- *       1 / (1 - p) in double, dropped ones are the product with 0.
+ *       (offset, i) and a key fixed by seed, one 16-bit uniform per element
+ *       (eight per generator block); kept elements are scaled by 1 / (1 - p)
+ *       in double, dropped ones are the product with 0.
  */
 #include "oracle.h"
 
@@ -396,15 +397,19 @@ void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t
 
 int oracle_dropout_keep(uint64_t seed, uint64_t offset, int64_t i, float p)
 {
-    /* element i takes word i mod 4 of the block at counter
-     * (0, 0, lo(g), hi(g)), g = offset + floor(i / 4), key (lo, hi) of seed */
-    uint64_t g = offset + (uint64_t)i / 4u;
+    /* a block serves eight elements: element i takes the 16-bit half
+     * (i mod 2: 0 the low half, 1 the high half) of word (i mod 8) / 2 of the
+     * block at counter (0, 0, lo(g), hi(g)), g = offset + floor(i / 8), key
+     * (lo, hi) of seed */
+    uint64_t g = offset + (uint64_t)i / 8u;
     uint32_t ctr[4] = {0u, 0u, (uint32_t)g, (uint32_t)(g >> 32)};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t w[4];
     oracle_philox4x32_10(ctr, key, w);
-    /* u = the word's top 24 bits as a fraction in [0, 1): exact in fp32 */
-    float u = (float)(w[i % 4] >> 8) * 0x1p-24f;
+    uint32_t word = w[(i % 8) / 2];
+    uint32_t half = (i % 2) ? (word >> 16) : (word & 0xFFFFu);
+    /* u = the half as a fraction in [0, 1): exact in fp32 */
+    float u = (float)half * 0x1p-16f;
     return u >= p;
 }
 

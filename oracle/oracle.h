@@ -128,9 +128,10 @@ void oracle_layernorm_act_ex_bf16(const uint16_t *x, const uint16_t *r, const ui
 /* ---- o6: Philox-4xW-10 ("Parallel random numbers: as easy as 1, 2, 3",
  * SC'11) for W = 32 (the dropout generator) and W = 64 (the same round
  * structure, checkable against numpy's Philox), and the dropout decision:
- *   element i of a call keyed by (seed, offset) takes word i mod 4 of
- *   Philox-4x32-10 at counter (0, 0, lo(g), hi(g)), g = offset + floor(i/4),
- *   key (lo(seed), hi(seed)); u = (word >> 8) * 2^-24; kept iff u >= p. */
+ *   element i of a call keyed by (seed, offset) takes the 16-bit half h
+ *   (i mod 2: low, high) of word (i mod 8) / 2 of Philox-4x32-10 at counter
+ *   (0, 0, lo(g), hi(g)), g = offset + floor(i / 8), key (lo(seed),
+ *   hi(seed)); u = h * 2^-16; kept iff u >= p. */
 void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
 int oracle_dropout_keep(uint64_t seed, uint64_t offset, int64_t i, float p);

@@ -571,13 +571,15 @@ def pin_philox32_curand(lib):
 
 
 def pin_dropout_decision(lib):
-    """Element i of a call (seed, offset 0) takes word i mod 4 of block i // 4,
-    which is cuRAND's output i; kept iff (word >> 8) * 2^-24 >= p.  p is also
-    set to the exact u of chosen elements (u >= p keeps them), p = 0 keeps
-    everything, and masks nest as p grows."""
+    """Element i of a call (seed, offset 0) takes half i mod 2 (low, high) of
+    word (i mod 8) / 2 of block i // 8, which is cuRAND's output word i // 2;
+    kept iff half * 2^-16 >= p.  p is also set to the exact u of chosen
+    elements (u >= p keeps them), p = 0 keeps everything, and masks nest as p
+    grows."""
     seed = 0x5EED0F0D
     words = _curand_philox_words(seed, 4 * 256)
-    u = (words >> np.uint32(8)).astype(np.float32) * np.float32(2.0 ** -24)
+    halves = np.stack([words & np.uint32(0xFFFF), words >> np.uint32(16)], axis=1).reshape(-1)
+    u = halves.astype(np.float32) * np.float32(2.0 ** -16)
     for p in (0.1, 0.5, 0.9, float(u[17]), float(u[300])):
         keep = oracle.dropout_mask(seed, 0, 0, u.size, p, lib=lib)
         assert np.array_equal(keep, u >= np.float32(p)), p
@@ -588,11 +590,11 @@ def pin_dropout_decision(lib):
 
 
 def pin_dropout_counter_and_rate(lib):
-    """Counter arithmetic: offset + 1 is the same stream as element index + 4;
+    """Counter arithmetic: offset + 1 is the same stream as element index + 8;
     the keep rate over 2^20 elements is within 5 sigma of 1 - p; another seed
     gives another mask."""
     a = oracle.dropout_mask(11, 5, 8, 4096, 0.3, lib=lib)
-    b = oracle.dropout_mask(11, 4, 12, 4096, 0.3, lib=lib)
+    b = oracle.dropout_mask(11, 4, 16, 4096, 0.3, lib=lib)
     assert np.array_equal(a, b)
     n = 1 << 20
     for p in (0.1, 0.5):

@@ -91,13 +91,15 @@ MUTANTS = {
                          "uint64_t n2 = (uint64_t)(p0 >> 64) ^ c1 ^ k1;"),
     "philox64_key_order": ("uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k0;",
                            "uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k1;"),
-    "dropout_lane": ("float u = (float)(w[i % 4] >> 8)", "float u = (float)(w[(i + 1) % 4] >> 8)"),
+    "dropout_word": ("uint32_t word = w[(i % 8) / 2];", "uint32_t word = w[(i % 4)];"),
+    "dropout_halves_swapped": ("uint32_t half = (i % 2) ? (word >> 16) : (word & 0xFFFFu);",
+                               "uint32_t half = (i % 2) ? (word & 0xFFFFu) : (word >> 16);"),
     "dropout_counter_word": ("uint32_t ctr[4] = {0u, 0u, (uint32_t)g, (uint32_t)(g >> 32)};",
                              "uint32_t ctr[4] = {(uint32_t)g, 0u, 0u, (uint32_t)(g >> 32)};"),
-    "dropout_block_per_element": ("uint64_t g = offset + (uint64_t)i / 4u;",
-                                  "uint64_t g = offset + (uint64_t)i;"),
+    "dropout_block_of_four": ("uint64_t g = offset + (uint64_t)i / 8u;",
+                              "uint64_t g = offset + (uint64_t)i / 4u;"),
     "dropout_strict_threshold": ("return u >= p;", "return u > p;"),
-    "dropout_low_bits": ("(w[i % 4] >> 8) * 0x1p-24f", "(w[i % 4] & 0xFFFFFFu) * 0x1p-24f"),
+    "dropout_scale_of_u": ("float u = (float)half * 0x1p-16f;", "float u = (float)half * 0x1p-15f;"),
     "dropout_scale_inverted": ("g = g / (1.0 - (double)ex->p);", "g = g * (1.0 - (double)ex->p);"),
     "dropout_dropped_kept": ("                else\n                    g = g * 0.0;",
                              "                else\n                    g = g * 1.0;"),
