@@ -226,13 +226,15 @@ mb_status fused_layernorm_act(const void *x, const void *r, const void *w, const
  *            with probability 1 - p and scaled by 1 / (1 - p) (fp32, rounded
  *            once), or multiplied by 0.  The pages fix no random number
  *            generator; the decision is the counter-based Philox-4x32-10
- *            ("Parallel random numbers: as easy as 1, 2, 3", SC'11): element
- *            i = row * hidden + col takes word i mod 4 of the block at counter
- *            (0, 0, lo(g), hi(g)), g = offset + floor(i / 4), under the key
- *            (lo(seed), hi(seed)), and is kept iff (word >> 8) * 2^-24 >= p.
- *            The decisions depend only on (seed, offset, i, p), never on the
- *            launch; a later call takes fresh ones with offset advanced by
- *            ceil(rows * hidden / 4).  p = 0: no dropout (out is bit-identical
+ *            ("Parallel random numbers: as easy as 1, 2, 3", SC'11), one
+ *            16-bit uniform per element: element i = row * hidden + col takes
+ *            the half h (i mod 2: low, high) of word (i mod 8) / 2 of the block
+ *            at counter (0, 0, lo(g), hi(g)), g = offset + floor(i / 8), under
+ *            the key (lo(seed), hi(seed)), and is kept iff h * 2^-16 >= p (so
+ *            the drop probability is ceil(p 2^16) / 2^16).  The decisions
+ *            depend only on (seed, offset, i, p), never on the launch; a later
+ *            call takes fresh ones with offset advanced by
+ *            ceil(rows * hidden / 8).  p = 0: no dropout (out is bit-identical
  *            to fused_layernorm_act).  p outside [0, 1) (or NaN) gives
  *            MB_ERR_VALUE.  h_out (the residual stream) is never dropped.
  *   stats    mean_out / rstd_out (fp32, `rows` values each; NULL: not
@@ -355,7 +357,8 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * out[6] = dynamic shared memory bytes.  `chain`: 0 residual + LayerNorm +
  * GeLU, 1 the TorchInductor chain, 2 the LayerNorm family with a residual,
  * 3 without, 4 row softmax, 5 and 6 the LayerNorm family with dropout (with
- * a residual, without).  `aligned` says whether every pointer is 16-byte
+ * a residual, without), 7 the LayerNorm family with a residual that also
+ * writes the residual stream h.  `aligned` says whether every pointer is 16-byte
  * aligned.  Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,

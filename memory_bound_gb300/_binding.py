@@ -372,10 +372,11 @@ def set_pointwise_shape(blocks_per_sm=0, unroll=0):
 def row_plan(chain, dtype, rows, cols, aligned=True):
     """The launch a row chain would use: dict(path, threads, ctas, vpt, vec,
     stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact", "softmax",
-    "lnact_res_dropout" or "lnact_dropout"; dtype: "f32" or "bf16"."""
+    "lnact_res_dropout", "lnact_dropout" or "lnact_res_h" (with the
+    residual-stream output); dtype: "f32" or "bf16"."""
     out = (ctypes.c_int32 * 7)()
     code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4,
-            "lnact_res_dropout": 5, "lnact_dropout": 6}[chain]
+            "lnact_res_dropout": 5, "lnact_dropout": 6, "lnact_res_h": 7}[chain]
     dt = {"f32": MB_F32, "bf16": MB_BF16}[dtype]
     st = load_library().mb_row_plan(code, dt, rows, cols, int(bool(aligned)), out)
     _check("mb_row_plan", st)

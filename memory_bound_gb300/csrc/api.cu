@@ -417,7 +417,7 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll) {
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int aligned,
                       int32_t out[7]) {
     if (!out) return MB_ERR_NULL;
-    if (chain < 0 || chain > 6) return MB_ERR_VALUE;
+    if (chain < 0 || chain > 7) return MB_ERR_VALUE;
     if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
     mb_status st = check_rows(rows, cols);
     if (st != MB_OK) return st;
@@ -431,10 +431,13 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
     else if (chain == 1)
         st = inductor_rows_bf16(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                                 (int)cols, 1.0f, 1.0f, al, &p, false);
-    else if (chain == 2 || chain == 3)
+    else if (chain == 2 || chain == 3 || chain == 7) {
+        RowTuning t = g_tuning;
+        if (chain == 7) t.outs = 2;            // with the residual-stream output
         st = (dtype == MB_F32 ? lnact_rows_f32 : lnact_rows_bf16)(
-            ctx, g_tuning, chain == 2, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+            ctx, t, chain != 3, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
             (int)cols, 0.0f, 0, LnExtras{}, al, &p, false);
+    }
     else if (chain == 5 || chain == 6)
         st = (dtype == MB_F32 ? lnact_drop_rows_f32 : lnact_drop_rows_bf16)(
             ctx, g_tuning, chain == 5, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,

@@ -79,6 +79,7 @@ __device__ __forceinline__ void add_inputs(const Frag<T, VEC> &x, const Frag<T, 
 template <typename TT> struct LnGeluChain {
     using T = TT;
     static constexpr int kInputs = 2;     // x, r
+    static constexpr int kVec = Elem<T>::kVec;   // elements per vector slot (16 bytes)
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = false;
@@ -120,6 +121,7 @@ template <typename TT> struct LnGeluChain {
         return rsqrtf(m2 / (float)cols + a.eps);
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
+    static int outputs(const Args &) { return 1; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,
                                                 const PostPC<VEC> &pc, const Args &, int64_t,
@@ -139,6 +141,7 @@ template <typename TT> struct LnGeluChain {
 template <typename TT> struct InductorChainT {
     using T = TT;
     static constexpr int kInputs = 1;     // x
+    static constexpr int kVec = Elem<T>::kVec;
     static constexpr bool kTwoPass = false;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = false;
@@ -194,6 +197,7 @@ template <typename TT> struct InductorChainT {
     __device__ __forceinline__ static float p2(float (&)[VEC], float) { return 0.0f; }
     __device__ __forceinline__ static float stat2(float, int, const Args &) { return 0.0f; }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
+    static int outputs(const Args &) { return 1; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
                                                 const PostPC<VEC> &pc, const Args &, int64_t,
@@ -226,6 +230,9 @@ enum { kActNone = 0, kActRelu = 1, kActGelu = 2 };
 template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     using T = TT;
     static constexpr int kInputs = RES ? 2 : 1;
+    // with dropout a slot is eight elements (one generator block; 32 bytes
+    // of fp32), else 16 bytes
+    static constexpr int kVec = DROP ? 8 : Elem<T>::kVec;
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = true;
@@ -291,6 +298,8 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
         else ln_affine_act<T, VEC, 0>(v, rstd, pc.w, pc.b, o);
         if constexpr (DROP) dropout_slot<VEC>(o, off, a.drop);
     }
+    // full-size outputs per row: out, and h when it is written
+    static int outputs(const Args &a) { return a.h ? 2 : 1; }
     // the row's mean and rstd, written by one thread per row when asked for
     __device__ __forceinline__ static void store_stats(const Args &a, int64_t row, float mean,
                                                        float rstd) {
@@ -307,6 +316,7 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
 template <typename TT> struct SoftmaxChain {
     using T = TT;
     static constexpr int kInputs = 1;
+    static constexpr int kVec = Elem<T>::kVec;
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = true;
     static constexpr bool kStorePre = false;
@@ -354,6 +364,7 @@ template <typename TT> struct SoftmaxChain {
         return 1.0f / sum;
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
+    static int outputs(const Args &) { return 1; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,
                                                 const PostPC<VEC> &, const Args &, int64_t,

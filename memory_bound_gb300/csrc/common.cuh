@@ -102,10 +102,11 @@ constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
 
 // Dropout parameters, prepared on the host.  The round keys are the key
 // schedule written out (rk[2r], rk[2r + 1] = key + r (W0, W1)), so the kernel
-// reads them as launch constants.  Element i takes word i mod 4 of the block at
-// counter (0, 0, lo(g), hi(g)), g = offset + i / 4, and is kept iff its top 24
-// bits, as a fraction of 2^24, are >= p: iff word >= thr = ceil(p 2^24) 2^8
-// (the same decision, taken exactly in integers).  Kept values are scaled by
+// reads them as launch constants.  One block serves eight elements: element i
+// takes the 16-bit half (i mod 2: low, high) of word (i mod 8) / 2 of the block
+// at counter (0, 0, lo(g), hi(g)), g = offset + i / 8, and is kept iff that
+// half, as a fraction of 2^16, is >= p: iff half >= thr = ceil(p 2^16) (the
+// same decision, taken exactly in integers).  Kept values are scaled by
 // inv_keep = 1 / (1 - p); dropped ones are multiplied by 0.
 struct DropoutArgs {
     uint32_t rk[20];
@@ -119,42 +120,44 @@ __device__ __forceinline__ uint4 philox_block(uint64_t g, const DropoutArgs &d) 
     uint32_t c0 = 0u, c1 = 0u, c2 = (uint32_t)g, c3 = (uint32_t)(g >> 32);
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint64_t p0 = (uint64_t)kPhiloxM0 * c0;
-        const uint64_t p1 = (uint64_t)kPhiloxM1 * c2;
-        c0 = (uint32_t)(p1 >> 32) ^ c1 ^ d.rk[2 * r];
-        c1 = (uint32_t)p1;
-        c2 = (uint32_t)(p0 >> 32) ^ c3 ^ d.rk[2 * r + 1];
-        c3 = (uint32_t)p0;
+        const uint32_t hi0 = __umulhi(kPhiloxM0, c0), lo0 = kPhiloxM0 * c0;
+        const uint32_t hi1 = __umulhi(kPhiloxM1, c2), lo1 = kPhiloxM1 * c2;
+        c0 = hi1 ^ c1 ^ d.rk[2 * r];
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ d.rk[2 * r + 1];
+        c3 = lo0;
     }
     return make_uint4(c0, c1, c2, c3);
 }
 
-__device__ __forceinline__ float keep_scale(uint32_t word, const DropoutArgs &d) {
-    return word >= d.thr ? d.inv_keep : 0.0f;
+__device__ __forceinline__ float keep_scale(uint32_t half, const DropoutArgs &d) {
+    return half >= d.thr ? d.inv_keep : 0.0f;
 }
 
 // Dropout over one slot of VEC values whose first element has index `off`
-// in the whole tensor.  Vector slots start at a multiple of 4 (rows hold a
-// multiple of VEC elements), so each group of four takes one block.
+// in the whole tensor.  Slots of eight or more start at a multiple of 8 (rows
+// hold a whole number of slots), so each group of eight takes one block.
 template <int VEC>
 __device__ __forceinline__ void dropout_slot(float (&o)[VEC], int64_t off, const DropoutArgs &d) {
-    if constexpr (VEC % 4 == 0) {
+    if constexpr (VEC % 8 == 0) {
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-            const uint4 w = philox_block(d.offset + (uint64_t)(off >> 2) + (uint64_t)q, d);
-            o[4 * q + 0] *= keep_scale(w.x, d);
-            o[4 * q + 1] *= keep_scale(w.y, d);
-            o[4 * q + 2] *= keep_scale(w.z, d);
-            o[4 * q + 3] *= keep_scale(w.w, d);
+        for (int q = 0; q < VEC / 8; ++q) {
+            const uint4 w = philox_block(d.offset + (uint64_t)(off >> 3) + (uint64_t)q, d);
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                o[8 * q + 2 * k] *= keep_scale(words[k] & 0xFFFFu, d);
+                o[8 * q + 2 * k + 1] *= keep_scale(words[k] >> 16, d);
+            }
         }
     } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             const int64_t i = off + e;
-            const uint4 w = philox_block(d.offset + (uint64_t)(i >> 2), d);
-            const int lane = (int)(i & 3);
-            const uint32_t word = lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
-            o[e] *= keep_scale(word, d);
+            const uint4 w = philox_block(d.offset + (uint64_t)(i >> 3), d);
+            const int k = (int)((i & 7) >> 1);
+            const uint32_t word = k == 0 ? w.x : k == 1 ? w.y : k == 2 ? w.z : w.w;
+            o[e] *= keep_scale((i & 1) ? (word >> 16) : (word & 0xFFFFu), d);
         }
     }
 }
@@ -177,8 +180,8 @@ __device__ __forceinline__ uint16_t f_to_bf16(float f) {
 
 // ---------------------------------------------------------------------------
 // Fragments: VEC consecutive elements of one tensor as fp32 values.
-// VEC * sizeof(T) == 16 uses one 128-bit access; VEC == 1 is a scalar access.
-// T is float or uint16_t (bf16 bits).
+// VEC * sizeof(T) a multiple of 16 uses that many 128-bit accesses; VEC == 1
+// is a scalar access.  T is float or uint16_t (bf16 bits).
 // ---------------------------------------------------------------------------
 
 template <typename T> struct Elem;
@@ -186,27 +189,34 @@ template <> struct Elem<float> { static constexpr int kVec = 4; };
 template <> struct Elem<uint16_t> { static constexpr int kVec = 8; };
 
 template <typename T, int VEC> struct Frag {
+    // 16-byte accesses per fragment (0: one scalar access)
+    static constexpr int kParts = VEC * (int)sizeof(T) / 16;
+    static constexpr int kPer = 16 / (int)sizeof(T);    // elements per 16 bytes
+    static_assert(VEC == 1 || (kParts >= 1 && kParts * kPer == VEC), "fragment size");
     float f[VEC];
 
-    __device__ __forceinline__ void unpack(const uint4 &u) {
+    // elements [q * kPer, (q + 1) * kPer) from / to one 16-byte word
+    __device__ __forceinline__ void unpack(const uint4 &u, int q) {
+        float *g = f + q * kPer;
         if constexpr (sizeof(T) == 4) {
-            f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
-            f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+            g[0] = __uint_as_float(u.x); g[1] = __uint_as_float(u.y);
+            g[2] = __uint_as_float(u.z); g[3] = __uint_as_float(u.w);
         } else {
-            f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
-            f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-            f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
-            f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+            g[0] = bf16_lo(u.x); g[1] = bf16_hi(u.x);
+            g[2] = bf16_lo(u.y); g[3] = bf16_hi(u.y);
+            g[4] = bf16_lo(u.z); g[5] = bf16_hi(u.z);
+            g[6] = bf16_lo(u.w); g[7] = bf16_hi(u.w);
         }
     }
-    __device__ __forceinline__ uint4 pack() const {
+    __device__ __forceinline__ uint4 pack(int q) const {
+        const float *g = f + q * kPer;
         uint4 u;
         if constexpr (sizeof(T) == 4) {
-            u.x = __float_as_uint(f[0]); u.y = __float_as_uint(f[1]);
-            u.z = __float_as_uint(f[2]); u.w = __float_as_uint(f[3]);
+            u.x = __float_as_uint(g[0]); u.y = __float_as_uint(g[1]);
+            u.z = __float_as_uint(g[2]); u.w = __float_as_uint(g[3]);
         } else {
-            u.x = pack_bf16x2(f[0], f[1]); u.y = pack_bf16x2(f[2], f[3]);
-            u.z = pack_bf16x2(f[4], f[5]); u.w = pack_bf16x2(f[6], f[7]);
+            u.x = pack_bf16x2(g[0], g[1]); u.y = pack_bf16x2(g[2], g[3]);
+            u.z = pack_bf16x2(g[4], g[5]); u.w = pack_bf16x2(g[6], g[7]);
         }
         return u;
     }
@@ -219,21 +229,39 @@ template <typename T, int VEC> struct Frag {
 
     // streaming load of row data (evict-first in cache)
     __device__ __forceinline__ void load_stream(const T *p) {
-        if constexpr (VEC * sizeof(T) == 16) unpack(__ldcs(reinterpret_cast<const uint4 *>(p)));
-        else f[0] = to_f(__ldcs(p));
+        if constexpr (VEC == 1) {
+            f[0] = to_f(__ldcs(p));
+        } else {
+#pragma unroll
+            for (int q = 0; q < kParts; ++q)
+                unpack(__ldcs(reinterpret_cast<const uint4 *>(p) + q), q);
+        }
     }
     // cached read-only load (per-column vectors, reused by every row)
     __device__ __forceinline__ void load_cached(const T *p) {
-        if constexpr (VEC * sizeof(T) == 16) unpack(__ldg(reinterpret_cast<const uint4 *>(p)));
-        else f[0] = to_f(__ldg(p));
+        if constexpr (VEC == 1) {
+            f[0] = to_f(__ldg(p));
+        } else {
+#pragma unroll
+            for (int q = 0; q < kParts; ++q)
+                unpack(__ldg(reinterpret_cast<const uint4 *>(p) + q), q);
+        }
     }
     __device__ __forceinline__ void load_shared(const T *p) {
-        if constexpr (VEC * sizeof(T) == 16) unpack(*reinterpret_cast<const uint4 *>(p));
-        else f[0] = to_f(*p);
+        if constexpr (VEC == 1) {
+            f[0] = to_f(*p);
+        } else {
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) unpack(reinterpret_cast<const uint4 *>(p)[q], q);
+        }
     }
     __device__ __forceinline__ void store_stream(T *p) const {
-        if constexpr (VEC * sizeof(T) == 16) __stcs(reinterpret_cast<uint4 *>(p), pack());
-        else __stcs(p, from_f(f[0]));
+        if constexpr (VEC == 1) {
+            __stcs(p, from_f(f[0]));
+        } else {
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) __stcs(reinterpret_cast<uint4 *>(p) + q, pack(q));
+        }
     }
 };
 

@@ -36,8 +36,11 @@ struct RowTuning {
     int ctas_per_sm;       // 0 = automatic
     int stages;            // 0 = automatic
     int vpt;               // vector slots per thread, 0 = automatic
+    // per-call planning inputs (set by the row engine, not by the override)
     int no_bulk = 0;       // 1: some row input is not device memory, so no
                            // bulk-async copies (the STAGED path) are planned
+    int outs = 1;          // full-size outputs written per row (2 with the
+                           // LayerNorm family's residual-stream output)
 };
 
 // Process-wide pointwise override (mb_set_pointwise_shape).

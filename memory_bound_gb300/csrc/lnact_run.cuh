@@ -21,9 +21,9 @@ inline DropoutArgs make_dropout(float p, uint64_t seed, uint64_t offset) {
         k1 += kPhiloxW1;
     }
     d.offset = offset;
-    // keep iff (word >> 8) * 2^-24 >= p  <=>  word >= ceil(p * 2^24) * 2^8
-    // (p * 2^24 is exact; p < 1 keeps the threshold below 2^32)
-    d.thr = (uint32_t)std::ceil((double)p * 16777216.0) << 8;
+    // keep iff half * 2^-16 >= p  <=>  half >= ceil(p * 2^16) (p * 2^16 is
+    // exact; a threshold of 2^16 keeps nothing)
+    d.thr = (uint32_t)std::ceil((double)p * 65536.0);
     d.inv_keep = 1.0f / (1.0f - p);
     return d;
 }

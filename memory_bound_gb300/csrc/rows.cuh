@@ -45,6 +45,12 @@ constexpr int kWarpBlock = 256;
 constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
 constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
+// Bytes of row reads and writes per SM in flight beyond which more resident
+// rows stop paying (sweeps on GB300: LayerNorm rows of 48 KB in + out run
+// fastest three to an SM in fp32, four in bf16, whose rows carry twice the
+// arithmetic per byte; 64 KB bf16 rows three to an SM).
+constexpr int64_t kFlightBytesF32 = 160 * 1024;
+constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
 constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
@@ -430,7 +436,7 @@ inline cudaError_t allow_smem(const void *fn, const LaunchCtx &ctx, int bytes) {
 
 template <class C> struct RowEngine {
     using T = typename C::T;
-    static constexpr int kVecN = Elem<T>::kVec;
+    static constexpr int kVecN = C::kVec;     // elements per vector slot
 
     static const void *warp_fn(int vpl, bool vec) {
         if (vec) {
@@ -594,7 +600,7 @@ template <class C> struct RowEngine {
     // only sizes the grid for its rows.
     struct CacheEntry {
         bool used;
-        int device, cols, aligned, path, ctas_per_sm, stages, vpt, no_bulk;
+        int device, cols, aligned, path, ctas_per_sm, stages, vpt, no_bulk, outs;
         RowPlan core;
         const void *fn;
     };
@@ -620,7 +626,8 @@ template <class C> struct RowEngine {
             for (const CacheEntry &e : pc.entries) {
                 if (e.used && e.device == ctx.device && e.cols == cols && e.aligned == (int)aligned &&
                     e.path == tun.path && e.ctas_per_sm == tun.ctas_per_sm &&
-                    e.stages == tun.stages && e.vpt == tun.vpt && e.no_bulk == tun.no_bulk) {
+                    e.stages == tun.stages && e.vpt == tun.vpt && e.no_bulk == tun.no_bulk &&
+                    e.outs == tun.outs) {
                     core = e.core;
                     f = e.fn;
                     hit = true;
@@ -634,7 +641,7 @@ template <class C> struct RowEngine {
             std::lock_guard<std::mutex> lock(pc.mu);
             pc.entries[pc.next] = CacheEntry{true, ctx.device, cols, (int)aligned, tun.path,
                                              tun.ctas_per_sm, tun.stages, tun.vpt, tun.no_bulk,
-                                             core, f};
+                                             tun.outs, core, f};
             pc.next = (pc.next + 1) % kCacheSize;
         }
         *p = core;
@@ -712,10 +719,16 @@ template <class C> struct RowEngine {
         // CTA engine.  Each resident CTA keeps one row in flight, so pick the
         // vectors-per-thread that lets the most CTAs share an SM, counting up
         // to kRowsInFlight (measured on GB300: four rows per SM keep HBM busy),
+        // or fewer for heavy rows (the byte budget above, never below two),
         // then the most threads per SM; one ring stage counted for the staged
         // path.
         const bool staged = path == MB_ROW_STAGED;
         const int smem1 = kHdrBytes + (staged ? stage_bytes : 0);
+        const int64_t row_io = (int64_t)(C::kInputs + tun.outs) * cols * (int64_t)sizeof(T);
+        const int64_t budget = sizeof(T) == 2 ? kFlightBytesBf16 : kFlightBytesF32;
+        int target = (int)(budget / row_io < kRowsInFlight ? budget / row_io : kRowsInFlight);
+        if (target < 2) target = 2;
+        const bool heavy = target < kRowsInFlight;      // the budget binds
         int best_vpt = 0, best_occ = 0, best_threads = 0;
         for (int cand = 1; cand <= max_vpt(vec); cand *= 2) {
             if (tun.vpt > 0 && cand != tun.vpt) continue;
@@ -728,13 +741,18 @@ template <class C> struct RowEngine {
             if (st != MB_OK) return st;
             if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
             if (occ < 1) continue;
-            const int rows_in_flight = occ < kRowsInFlight ? occ : kRowsInFlight;
-            const int best_rows = best_occ < kRowsInFlight ? best_occ : kRowsInFlight;
+            const int rows_in_flight = occ < target ? occ : target;
+            const int best_rows = best_occ < target ? best_occ : target;
+            // tie-break on threads per SM, counting only the CTAs that will
+            // be resident when the budget caps them
+            const int tie = heavy ? rows_in_flight : occ;
+            const int best_tie = heavy ? best_rows : best_occ;
             if (rows_in_flight > best_rows ||
-                (rows_in_flight == best_rows && occ * threads > best_occ * best_threads)) {
+                (rows_in_flight == best_rows && tie * threads > best_tie * best_threads)) {
                 best_vpt = cand; best_occ = occ; best_threads = threads;
             }
         }
+        if (heavy && tun.ctas_per_sm <= 0 && best_occ > target) best_occ = target;
         if (!best_vpt && tun.vpt > 0) {
             RowTuning t2 = tun;
             t2.vpt = 0;
@@ -782,7 +800,9 @@ template <class C> struct RowEngine {
                          int64_t rows, int cols, bool aligned, RowPlan *plan_out, bool launch) {
         RowPlan p;
         const void *fn = nullptr;
-        mb_status st = plan(ctx, tun, rows, cols, aligned, &p, &fn);
+        RowTuning tn = tun;      // the per-call planning inputs
+        if (C::outputs(a) > tn.outs) tn.outs = C::outputs(a);
+        mb_status st = plan(ctx, tn, rows, cols, aligned, &p, &fn);
         if (st != MB_OK) return st;
         if (launch && p.path == MB_ROW_STAGED) {
             // Bulk-async copies read device memory only: rows held in host
@@ -790,7 +810,7 @@ template <class C> struct RowEngine {
             bool dev = true;
             for (int i = 0; i < C::kInputs; ++i) dev = dev && device_resident(a.in[i]);
             if (!dev) {
-                RowTuning t2 = tun;
+                RowTuning t2 = tn;
                 t2.no_bulk = 1;
                 if ((st = plan(ctx, t2, rows, cols, aligned, &p, &fn)) != MB_OK) return st;
             }

@@ -2,8 +2,9 @@
 
     python -m memory_bound_gb300.profile_case ln_bf16 8192 8192 --iters 3
 
-Chains: pointwise_f32, pointwise_bf16, inductor_f32, ln_f32, ln_bf16,
-softmax_f32, softmax_bf16.
+Chains: pointwise_f32, pointwise_bf16, pointwise_bcast_f32, inductor_f32,
+ln_f32, ln_bf16, lnrelu_f32 (LayerNorm -> ReLU, no residual), lnrelu_drop_f32
+and lnrelu_drop_bf16 (with dropout p = 0.1), softmax_f32, softmax_bf16.
 Inputs are seeded synthetic tensors from synth; nothing is checked here (the
 tests do that).  Keep ncu captures small: a few hundred MB on the device.
 """
@@ -44,7 +45,18 @@ def main(argv=None):
         return torch.from_numpy(h).to(dev)
 
     mb.set_row_path(a.path, a.ctas, a.stages)
-    if a.chain.startswith("pointwise"):
+    if a.chain == "pointwise_bcast_f32":
+        x, b1, b2 = t(0, (a.rows, a.cols)), t(1, (a.cols,)), t(2, (a.cols,))
+        out = torch.empty_like(x)
+        run = lambda: mb.fused_add_relu_scale(x, b1, b2, 0.5, out=out)
+    elif a.chain.startswith("lnrelu"):
+        x = t(0, (a.rows, a.cols))
+        w, b = t(2, (a.cols,), 0.5, 1.5, True), t(3, (a.cols,), 0, 0.1)
+        out = torch.empty_like(x)
+        p = 0.1 if "drop" in a.chain else 0.0
+        run = lambda: mb.fused_layernorm_act(x, None, w, b, 1e-5, act="relu", out=out, p=p,
+                                             seed=2024)
+    elif a.chain.startswith("pointwise"):
         n = a.rows * a.cols
         x, b1, b2 = t(0, (n,)), t(1, (n,)), t(2, (n,))
         out = torch.empty_like(x)
@@ -66,7 +78,9 @@ def main(argv=None):
     for _ in range(a.iters):
         run()
     torch.cuda.synchronize()
-    kind = ("ln" if a.chain.startswith("ln") else
+    kind = ("lnact_dropout" if a.chain.startswith("lnrelu_drop") else
+            "lnact" if a.chain.startswith("lnrelu") else
+            "ln" if a.chain.startswith("ln") else
             "softmax" if a.chain.startswith("softmax") else "inductor")
     print("plan:", mb.row_plan(kind, dt, a.rows, a.cols)
           if not a.chain.startswith("pointwise") else "pointwise")

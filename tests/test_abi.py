@@ -170,7 +170,7 @@ def test_layernorm_ex_argument_checks(lib):
     assert f(A, B, C, D, E, F, None, F + 64, 4, 64, 1e-5, 1, 0.0, 1, 0, 0, None) == MB_ERR_OVERLAP
     assert f(A, B, C, D, E, None, None, None, 4, 64, 1e-5, 7, 0.1, 1, 0, 0, None) == MB_ERR_VALUE
     assert f(None, B, C, D, E, None, F, G, 4, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_ERR_NULL
-    assert lib.mb_row_plan(7, 0, 4, 64, 1, (ctypes.c_int32 * 7)()) == MB_ERR_VALUE
+    assert lib.mb_row_plan(8, 0, 4, 64, 1, (ctypes.c_int32 * 7)()) == MB_ERR_VALUE
 
 
 def test_pointwise_bcast_argument_checks(lib):

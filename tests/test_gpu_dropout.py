@@ -2,10 +2,10 @@
 activation output ("Operator fusion and kernel optimisation" §2.1:
 LayerNorm -> ReLU -> Dropout in one kernel) and the per-row statistics.
 
-Dropout decisions are integer work (Philox-4x32-10 words against an exact
-threshold), so the kept/dropped pattern must match the oracle's element for
-element, dropped elements must be exact (signed) zeros, and kept ones are
-within the fp32 / bf16 bar of the oracle's act / (1 - p)."""
+Dropout decisions are integer work (16-bit halves of Philox-4x32-10 words
+against an exact threshold), so the kept/dropped pattern must match the
+oracle's element for element, dropped elements must be exact (signed) zeros,
+and kept ones are within the fp32 / bf16 bar of the oracle's act / (1 - p)."""
 import numpy as np
 import pytest
 import torch
@@ -121,7 +121,7 @@ def test_dropout_activations(act, bf16):
 
 
 def test_offset_crosses_the_32_bit_counter_word():
-    """g = offset + i / 4 carries into the counter's high word inside the call."""
+    """g = offset + i / 8 carries into the counter's high word inside the call."""
     shape = (8, 1024)
     x, r, w, b = _inputs(*shape, 951, False)
     offset = (1 << 32) - 1000
@@ -151,9 +151,9 @@ def test_successive_offsets_give_fresh_masks():
     shape = (128, 4096)
     x, r, w, b = _inputs(*shape, 953, False)
     d = [to_dev(a) for a in (x, r, w, b)]
-    n4 = x.size // 4
+    n8 = x.size // 8
     a = mb.fused_layernorm_act(*d, act="none", p=0.5, seed=9, offset=0)
-    c = mb.fused_layernorm_act(*d, act="none", p=0.5, seed=9, offset=n4)
+    c = mb.fused_layernorm_act(*d, act="none", p=0.5, seed=9, offset=n8)
     ka, kc = (a != 0), (c != 0)
     agree = (ka == kc).float().mean().item()
     assert 0.45 < agree < 0.55
