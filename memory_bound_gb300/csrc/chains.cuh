@@ -7,9 +7,15 @@
 // nearest, as the scalar form); scalar slots (VEC 1) use the scalar forms.
 #pragma once
 
+#include <type_traits>
+
 #include "rows.cuh"
 
 namespace mb {
+
+// Per-slot values a chain draws before the row arrives (hook `early`), for
+// chains that have none.
+struct NoEarly {};
 
 // v <- v - s for a slot; returns the sum of the squares (second LN pass)
 template <int VEC>
@@ -94,6 +100,9 @@ template <typename TT> struct LnGeluChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
     static constexpr int kPostPC = 2;     // per-column vectors the epilogue reads
+    template <int VEC> using Early = NoEarly;
+    template <int VEC>
+    __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
     template <int VEC>
@@ -125,7 +134,7 @@ template <typename TT> struct LnGeluChain {
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,
                                                 const PostPC<VEC> &pc, const Args &, int64_t,
-                                                float (&o)[VEC]) {
+                                                const Early<VEC> &, float (&o)[VEC]) {
         ln_affine_act<T, VEC, 2>(v, rstd, pc.w, pc.b, o);
     }
 };
@@ -158,6 +167,9 @@ template <typename TT> struct InductorChainT {
     template <int VEC> struct PrePC { Frag<T, VEC> bias; };
     template <int VEC> struct PostPC { Frag<T, VEC> gamma, beta; };
     static constexpr int kPostPC = 2;
+    template <int VEC> using Early = NoEarly;
+    template <int VEC>
+    __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC>
     __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc) {
         pc.bias.load_cached(a.bias + col);
@@ -201,7 +213,7 @@ template <typename TT> struct InductorChainT {
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
                                                 const PostPC<VEC> &pc, const Args &, int64_t,
-                                                float (&o)[VEC]) {
+                                                const Early<VEC> &, float (&o)[VEC]) {
         if constexpr (VEC == 1) {
             o[0] = __fadd_rn(__fmul_rn(__fsub_rn(v[0], mean), pc.gamma.f[0]), pc.beta.f[0]);
         } else {
@@ -251,6 +263,14 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
     static constexpr int kPostPC = 2;
+    // with dropout: the slot's 16-bit uniforms, drawn while the row is in
+    // flight (they depend only on the element index)
+    template <int VEC> struct EarlyDrop { DropBits<VEC> bits; };
+    template <int VEC> using Early = std::conditional_t<DROP, EarlyDrop<VEC>, NoEarly>;
+    template <int VEC>
+    __device__ __forceinline__ static void early(const Args &a, int64_t off, Early<VEC> &e) {
+        if constexpr (DROP) dropout_bits<VEC>(off, a.drop, e.bits);
+    }
     template <int VEC>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
     template <int VEC>
@@ -292,11 +312,12 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,
                                                 const PostPC<VEC> &pc, const Args &a,
-                                                int64_t off, float (&o)[VEC]) {
+                                                int64_t, const Early<VEC> &ea,
+                                                float (&o)[VEC]) {
         if (a.act == kActGelu) ln_affine_act<T, VEC, 2>(v, rstd, pc.w, pc.b, o);
         else if (a.act == kActRelu) ln_affine_act<T, VEC, 1>(v, rstd, pc.w, pc.b, o);
         else ln_affine_act<T, VEC, 0>(v, rstd, pc.w, pc.b, o);
-        if constexpr (DROP) dropout_slot<VEC>(o, off, a.drop);
+        if constexpr (DROP) dropout_apply<VEC>(o, ea.bits, a.drop);
     }
     // full-size outputs per row: out, and h when it is written
     static int outputs(const Args &a) { return a.h ? 2 : 1; }
@@ -327,6 +348,9 @@ template <typename TT> struct SoftmaxChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC {};
     static constexpr int kPostPC = 0;
+    template <int VEC> using Early = NoEarly;
+    template <int VEC>
+    __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
     template <int VEC>
@@ -368,7 +392,7 @@ template <typename TT> struct SoftmaxChain {
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,
                                                 const PostPC<VEC> &, const Args &, int64_t,
-                                                float (&o)[VEC]) {
+                                                const Early<VEC> &, float (&o)[VEC]) {
         if constexpr (VEC == 1) {
             o[0] = v[0] * inv;
         } else {

@@ -134,21 +134,27 @@ __device__ __forceinline__ float keep_scale(uint32_t half, const DropoutArgs &d)
     return half >= d.thr ? d.inv_keep : 0.0f;
 }
 
-// Dropout over one slot of VEC values whose first element has index `off`
-// in the whole tensor.  Slots of eight or more start at a multiple of 8 (rows
-// hold a whole number of slots), so each group of eight takes one block.
+// The 16-bit halves of one slot of VEC elements: a slot of eight or more
+// holds whole blocks (its first index is a multiple of 8, rows holding a whole
+// number of slots), four words per block; a scalar slot keeps its element's
+// half in the low bits of one word per element.
+template <int VEC> struct DropBits {
+    static constexpr int kWords = VEC % 8 == 0 ? VEC / 2 : VEC;
+    uint32_t w[kWords];
+};
+
+// The halves of the slot whose first element has index `off` in the whole
+// tensor (they depend on nothing else, so they can be drawn early).
 template <int VEC>
-__device__ __forceinline__ void dropout_slot(float (&o)[VEC], int64_t off, const DropoutArgs &d) {
+__device__ __forceinline__ void dropout_bits(int64_t off, const DropoutArgs &d, DropBits<VEC> &b) {
     if constexpr (VEC % 8 == 0) {
 #pragma unroll
         for (int q = 0; q < VEC / 8; ++q) {
             const uint4 w = philox_block(d.offset + (uint64_t)(off >> 3) + (uint64_t)q, d);
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                o[8 * q + 2 * k] *= keep_scale(words[k] & 0xFFFFu, d);
-                o[8 * q + 2 * k + 1] *= keep_scale(words[k] >> 16, d);
-            }
+            b.w[4 * q + 0] = w.x;
+            b.w[4 * q + 1] = w.y;
+            b.w[4 * q + 2] = w.z;
+            b.w[4 * q + 3] = w.w;
         }
     } else {
 #pragma unroll
@@ -157,8 +163,24 @@ __device__ __forceinline__ void dropout_slot(float (&o)[VEC], int64_t off, const
             const uint4 w = philox_block(d.offset + (uint64_t)(i >> 3), d);
             const int k = (int)((i & 7) >> 1);
             const uint32_t word = k == 0 ? w.x : k == 1 ? w.y : k == 2 ? w.z : w.w;
-            o[e] *= keep_scale((i & 1) ? (word >> 16) : (word & 0xFFFFu), d);
+            b.w[e] = (i & 1) ? (word >> 16) : (word & 0xFFFFu);
         }
+    }
+}
+
+// Applies the decisions: kept values times 1 / (1 - p), dropped ones times 0.
+template <int VEC>
+__device__ __forceinline__ void dropout_apply(float (&o)[VEC], const DropBits<VEC> &b,
+                                              const DropoutArgs &d) {
+    if constexpr (VEC % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < VEC / 2; ++k) {
+            o[2 * k] *= keep_scale(b.w[k] & 0xFFFFu, d);
+            o[2 * k + 1] *= keep_scale(b.w[k] >> 16, d);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] *= keep_scale(b.w[e], d);
     }
 }
 

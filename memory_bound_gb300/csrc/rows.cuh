@@ -10,6 +10,9 @@
 //                         values (PostPC) and the index of the slot's first
 //                         element in the whole tensor
 //   store_stats           one thread per row may write s1 and s2 out
+//   early (per slot)      values the epilogue needs that depend only on the
+//                         element index (dropout's random bits), drawn while
+//                         the row is still in flight and passed to post
 // and, with C::kStorePre, store_pre writes the prologue value v out as well
 // (the residual-stream output of a residual + LayerNorm block).
 // The row is read from device memory once and held in registers (v) between
@@ -103,6 +106,10 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             C::template load_pre<VEC>(a, vc * VEC, pre[k]);
             C::template load_post<VEC>(a, vc * VEC, post[k]);
         }
+        typename C::template Early<VEC> ea[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+            C::template early<VEC>(a, base + min(lane + 32 * k, nvec - 1) * VEC, ea[k]);
         float v[VPL][VEC];
         float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
@@ -130,7 +137,7 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
             const int vi = lane + 32 * k;
             if (vi < nvec) {
                 Frag<T, VEC> o;
-                C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, o.f);
+                C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, ea[k], o.f);
                 o.store_stream(a.out + base + vi * VEC);
             }
         }
@@ -215,6 +222,12 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             C::template load_pre<VEC>(a, vc * VEC, pre[k]);
             if constexpr (kEarlyPost) C::template load_post<VEC>(a, vc * VEC, post[k]);
         }
+        // values the epilogue needs that do not depend on the row's data,
+        // drawn while the row is still in flight
+        typename C::template Early<VEC> ea[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            C::template early<VEC>(a, base + min(tid + k * (int)blockDim.x, nvec - 1) * VEC, ea[k]);
         if constexpr (STAGED) {
             if (!mbar_wait_bounded(smem_addr(&bars[s]), parity)) abort_flag[li & 1] = 1;
         }
@@ -265,11 +278,11 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             if (vi < nvec) {
                 Frag<T, VEC> o;
                 if constexpr (kEarlyPost) {
-                    C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, ea[k], o.f);
                 } else {
                     PostPC pc;
                     C::template load_post<VEC>(a, vi * VEC, pc);
-                    C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, ea[k], o.f);
                 }
                 o.store_stream(a.out + base + vi * VEC);
             }
@@ -368,6 +381,12 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     int rb = 0, xb = 0;
     for (int64_t row = cid; row < rows; row += nclusters) {
         const int64_t base = row * cols + lo;
+        typename C::template Early<VEC> ea[VPT];
+        if (nvec > 0) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+                C::template early<VEC>(a, base + min(tid + k * (int)blockDim.x, nvec - 1) * VEC, ea[k]);
+        }
         float v[VPT][VEC];
         float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
@@ -407,11 +426,11 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
             if (vi < nvec) {
                 Frag<T, VEC> o;
                 if constexpr (kEarlyPost) {
-                    C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, ea[k], o.f);
                 } else {
                     PostPC pc;
                     C::template load_post<VEC>(a, lo + vi * VEC, pc);
-                    C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, o.f);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, ea[k], o.f);
                 }
                 o.store_stream(a.out + base + vi * VEC);
             }
