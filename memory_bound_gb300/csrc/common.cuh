@@ -377,6 +377,28 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
 // of %globaltimer (or kWaitLimitPolls polls).  Returns false if it gave up.
+// Arrive on a local mbarrier and add `bytes` to the transaction count it
+// expects, with no release of this thread's earlier accesses (so loads and
+// stores still in flight do not have to land first).
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_cluster(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Stores 4 bytes into another CTA's shared memory (a cluster address) and
+// completes 4 transaction bytes on that CTA's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 :: "r"(remote_addr), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -55,6 +55,7 @@ constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims 
 constexpr int64_t kFlightBytesF32 = 160 * 1024;
 constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
+constexpr int kClusterElems = 16; // values per thread the cluster planner prefers
 constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
 // Folds one slot's VEC values into the running first-pass partial (a sum, or a
@@ -314,20 +315,32 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
 // one thread-block cluster per row (rows longer than one CTA can hold)
 // ---------------------------------------------------------------------------
 
-// Sum (or maximum) of one value per CTA over the cluster.  `xch` is this
-// CTA's pair of exchange slots (alternated between reductions, as block_sum's
-// buffers are); thread 0 publishes, the cluster barrier orders it, and every
-// thread reads the cluster's slots in rank order, so all CTAs get the
-// bitwise-same result.
+// Sum (or maximum) of one value per CTA over the cluster.  Thread 0 pushes
+// this CTA's partial into slot `rank` of every CTA's exchange buffer `xch`
+// (kMaxCluster floats) with st.async, which completes 4 transaction bytes on
+// that CTA's mbarrier `bar`; every CTA arms its own mbarrier for cs pushes,
+// waits on it (bounded; a timeout sets *abort) and folds the slots in rank
+// order, so all CTAs get the bitwise-same value.  No cluster barrier: its
+// release half would first wait for every load and store this thread has in
+// flight (the next row's prefetch, this row's stores), serialising them with
+// the exchange.  Two buffers alternate between reductions; a CTA pushes into
+// buffer b again only after every CTA has pushed the reduction in between,
+// which each does after reading b.
 template <bool MAX>
-__device__ __forceinline__ float cluster_reduce(float v, float *xch,
-                                                cooperative_groups::cluster_group &cl) {
-    if (threadIdx.x == 0) *xch = v;
-    cl.sync();
-    const unsigned n = cl.num_blocks();
+__device__ __forceinline__ float cluster_reduce(float v, float *xch, uint64_t *bar,
+                                                uint32_t &parity, unsigned cs, unsigned rank,
+                                                volatile int *abort) {
+    const uint32_t bar_a = smem_addr(bar);
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx_relaxed(bar_a, cs * 4u);
+        const uint32_t slot = smem_addr(xch + rank);
+        for (unsigned j = 0; j < cs; ++j) st_async_f32(map_cluster(slot, j), v, map_cluster(bar_a, j));
+    }
+    if (!mbar_wait_bounded(bar_a, parity)) *abort = 1;
+    parity ^= 1u;
     float r = MAX ? -INFINITY : 0.0f;
-    for (unsigned j = 0; j < n; ++j) {
-        const float p = *cl.map_shared_rank(xch, j);
+    for (unsigned j = 0; j < cs; ++j) {
+        const float p = xch[j];
         r = MAX ? fmaxf(r, p) : r + p;
     }
     return r;
@@ -337,10 +350,10 @@ __device__ __forceinline__ float cluster_reduce(float v, float *xch,
 // columns [rank * slice, (rank + 1) * slice) of each of them in registers.
 // Direct vector loads, the next row's issued as soon as the current row has
 // left the input registers; the two statistics combine CTA partials through
-// distributed shared memory.
+// distributed shared memory (cluster_reduce).
 template <class C, int VPT, int VEC>
 __global__ void __launch_bounds__(kCtaMaxThreads, 1)
-rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *) {
+rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *err) {
     namespace cg = cooperative_groups;
     using T = typename C::T;
     constexpr int NIN = C::kInputs;
@@ -348,7 +361,9 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     using PrePC = typename C::template PrePC<VEC>;
     using PostPC = typename C::template PostPC<VEC>;
     __shared__ float red[2][32];
-    __shared__ float xch[2];
+    __shared__ float xch[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ int abort_flag[2];
     cg::cluster_group cl = cg::this_cluster();
     const int tid = threadIdx.x;
     const int rank = (int)cl.block_rank();
@@ -357,6 +372,15 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     const int lo = rank * slice;                               // first column of this CTA
     const int hi = lo + slice < cols ? lo + slice : cols;
     const int nvec = hi > lo ? (hi - lo) / VEC : 0;            // vectors this CTA holds
+    const unsigned cs = cl.num_blocks();
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
+        fence_mbar_init();
+    }
+    cl.sync();      // every CTA's barriers are initialised before any push
     pdl_wait();
     pdl_launch_dependents();
 
@@ -379,7 +403,9 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     if (cid < rows) load_row(cid);
 
     int rb = 0, xb = 0;
-    for (int64_t row = cid; row < rows; row += nclusters) {
+    uint32_t xpar[2] = {0u, 0u};
+    int64_t it = 0;
+    for (int64_t row = cid; row < rows; row += nclusters, ++it) {
         const int64_t base = row * cols + lo;
         typename C::template Early<VEC> ea[VPT];
         if (nvec > 0) {
@@ -403,7 +429,11 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
         if (row + nclusters < rows) load_row(row + nclusters);
         const float c1 = C::kMaxFirst ? block_max(l1, red[rb]) : block_sum(l1, red[rb]);
         rb ^= 1;
-        const float r1 = cluster_reduce<C::kMaxFirst>(c1, &xch[xb], cl);
+        // a wait that timed out in the previous row (flags alternate by row,
+        // as in the CTA engine, so every thread reads the same value here)
+        if (abort_flag[(it + 1) & 1]) break;
+        volatile int *ab = &abort_flag[it & 1];
+        const float r1 = cluster_reduce<C::kMaxFirst>(c1, xch[xb], &xbar[xb], xpar[xb], cs, rank, ab);
         xb ^= 1;
         const float mean = C::stat1(r1, cols, a);
         float rstd = 0.0f;
@@ -416,7 +446,8 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
             }
             const float c2 = block_sum(l2, red[rb]);
             rb ^= 1;
-            rstd = C::stat2(cluster_reduce<false>(c2, &xch[xb], cl), cols, a);
+            rstd = C::stat2(cluster_reduce<false>(c2, xch[xb], &xbar[xb], xpar[xb], cs, rank, ab),
+                            cols, a);
             xb ^= 1;
         }
         if (rank == 0 && tid == 0) C::store_stats(a, row, mean, rstd);
@@ -436,7 +467,8 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
             }
         }
     }
-    cl.sync();     // no CTA leaves while another may still read its slots
+    if (tid == 0 && (abort_flag[0] | abort_flag[1])) atomicOr(err, kDevErrWaitTimeout);
+    cl.sync();     // no CTA leaves while another may still push into its slots
 }
 
 // ---------------------------------------------------------------------------
@@ -560,8 +592,24 @@ template <class C> struct RowEngine {
     // in flight, so among cluster sizes 2, 4, 8, 16 (or the requested one) and
     // the vectors-per-thread that fit a slice in one CTA, take the launch with
     // the most resident clusters (ties: the larger cluster); no rank is empty.
+    // Launches holding at most kClusterElems values per thread come first: a
+    // thread keeps its slice and the next row's prefetch in registers, and
+    // more than that spills (sweeps on GB300: 16 values per thread ran LN fp32
+    // at 65536 columns at 6.1 TB/s, 32 at 3.9).
     static mb_status plan_cluster(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows,
                                   int nvec, bool vec, RowPlan *p, const void **fn) {
+        const int VEC = vec ? kVecN : 1;
+        for (int pass = 0; pass < 2; ++pass) {
+            mb_status st = plan_cluster_pass(ctx, tun, rows, nvec, vec,
+                                             pass == 0 ? kClusterElems / VEC : 1 << 30, p, fn);
+            if (st != MB_ERR_SHAPE) return st;
+        }
+        return MB_ERR_SHAPE;
+    }
+
+    static mb_status plan_cluster_pass(const LaunchCtx &ctx, const RowTuning &tun,
+                                       int64_t rows, int nvec, bool vec, int max_vpt_regs,
+                                       RowPlan *p, const void **fn) {
         int best_n = 0, best_cs = 0, best_vpt = 0, best_threads = 0, best_slice = 0;
         for (int cs0 : {2, 4, 8, 16}) {
             int cs = cs0;
@@ -575,6 +623,7 @@ template <class C> struct RowEngine {
             if (cs < 2) continue;
             for (int vpt = 1; vpt <= max_vpt(vec); vpt *= 2) {
                 if (tun.vpt > 0 && vpt != tun.vpt) continue;
+                if (tun.vpt <= 0 && vpt > max_vpt_regs) continue;
                 if (ceil_div(slice_v, vpt) > kCtaMaxThreads) continue;
                 const int threads = round_up32(ceil_div(slice_v, vpt));
                 const void *f = cluster_fn(vpt, vec);
@@ -593,7 +642,7 @@ template <class C> struct RowEngine {
             t2.vpt = 0;
             return plan_cluster(ctx, t2, rows, nvec, vec, p, fn);
         }
-        if (!best_n) return MB_ERR_SHAPE;
+        if (!best_n) return MB_ERR_SHAPE;       // the caller tries the next pass
         *fn = cluster_fn(best_vpt, vec);
         const int64_t ncl = rows < best_n ? rows : best_n;
         p->path = MB_ROW_CLUSTER; p->threads = best_threads; p->vpt = best_vpt;
