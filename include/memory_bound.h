@@ -58,10 +58,10 @@
  *               launched, and the call returns without side effects.
  *               A failed launch returns MB_ERR_CUDA (see mb_last_cuda_error).
  *               Faults during execution surface at the caller's next
- *               synchronisation, as for any CUDA kernel.  The staged row path
- *               waits on shared-memory barriers with a time limit; if a wait
- *               ever ran out, the kernel stops early and records it in a
- *               device flag that mb_device_error() reports.
+ *               synchronisation, as for any CUDA kernel.  The staged row paths
+ *               and the cluster path wait on shared-memory barriers with a
+ *               time limit; if a wait ever ran out, the kernel stops early and
+ *               records it in a device flag that mb_device_error() reports.
  *   Threads     Entry points may be called from several host threads.
  *               mb_set_row_path changes process-wide state and should not
  *               race with calls.
@@ -313,14 +313,17 @@ typedef enum mb_row_path {
     MB_ROW_STAGED = 3,   /* one CTA per row, rows staged into shared memory by
                             bulk async copies in a multi-stage ring            */
     MB_ROW_CLUSTER = 4   /* one thread-block cluster per row: each CTA holds a
-                            slice, statistics combined through distributed
-                            shared memory (automatic above 32768 elements)    */
+                            slice (staged by bulk async copies when the rows
+                            are vectorised device memory), statistics combined
+                            through distributed shared memory (automatic above
+                            32768 elements)                                    */
 } mb_row_path;
 
 /*
  * Process-wide override of the row-chain path and launch shape, for tuning
- * and testing.  ctas_per_sm (CTAs resident per SM), stages (ring depth of the
- * staged path; CTAs per row, 2..16, on the cluster path) and vec_per_thread (16-byte vectors each thread holds per row
+ * and testing.  ctas_per_sm (CTAs resident per SM; the staging ring depth on
+ * the cluster path), stages (ring depth of the staged path; CTAs per row,
+ * 2..16, on the cluster path) and vec_per_thread (vector slots each thread holds per row
  * on the CTA paths; a power of two) of 0 mean "choose automatically"; a
  * value that cannot serve a shape is ignored.  A forced path that cannot
  * serve a shape (MB_ROW_WARP beyond 256 vectors per row, MB_ROW_STAGED on

@@ -53,6 +53,7 @@ struct PointwiseTuning {
 struct RowPlan {
     int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
     int slice = 0;     // cluster path: vectors of the row each CTA holds
+    int ring = 0;      // cluster path: staging ring depth (0: direct loads)
     int64_t cap = 0;   // CTAs (warp/CTA paths, at 256 threads for warp) or clusters resident at once
 };
 

@@ -56,6 +56,7 @@ constexpr int64_t kFlightBytesF32 = 160 * 1024;
 constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
 constexpr int kClusterElems = 16; // values per thread the cluster planner prefers
+constexpr int kClusterRing = 1;   // staging ring depth on the cluster path
 constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
 // Folds one slot's VEC values into the running first-pass partial (a sum, or a
@@ -348,70 +349,134 @@ __device__ __forceinline__ float cluster_reduce(float v, float *xch, uint64_t *b
 
 // The cluster of CS CTAs owns rows c, c + nclusters, ...; CTA `rank` holds the
 // columns [rank * slice, (rank + 1) * slice) of each of them in registers.
-// Direct vector loads, the next row's issued as soon as the current row has
-// left the input registers; the two statistics combine CTA partials through
-// distributed shared memory (cluster_reduce).
-template <class C, int VPT, int VEC>
+//   STAGED  one elected thread streams the CTA's slice of each row (every
+//           input) into a ring of `nstage` shared-memory stages with bulk async
+//           copies, as the one-CTA staged engine does; a stage is refilled as
+//           soon as the first reduction barrier shows every thread holds its
+//           row in registers.
+//   DIRECT  vector loads, the next row's issued into registers as soon as the
+//           current row has left them (unaligned rows, rows in host memory).
+// The two statistics combine CTA partials through distributed shared memory
+// (cluster_reduce).  Every wait is bounded; a timeout ends the CTA's row loop
+// (after its copies in flight have landed) and is reported in `err`.
+template <class C, int VPT, int VEC, bool STAGED>
 __global__ void __launch_bounds__(kCtaMaxThreads, 1)
-rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *err) {
+rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *err,
+                    int nstage) {
     namespace cg = cooperative_groups;
     using T = typename C::T;
     constexpr int NIN = C::kInputs;
     constexpr bool kEarlyPost = VPT * VEC * C::kPostPC <= 8;
     using PrePC = typename C::template PrePC<VEC>;
     using PostPC = typename C::template PostPC<VEC>;
+    extern __shared__ __align__(1024) unsigned char ring[];   // STAGED: [nstage][NIN][slice]
     __shared__ float red[2][32];
     __shared__ float xch[2][kMaxCluster];
     __shared__ __align__(8) uint64_t xbar[2];
-    __shared__ int abort_flag[2];
+    __shared__ __align__(8) uint64_t sbar[kMaxStages];
+    __shared__ int stage_abort[2];    // a stage wait timed out (by row parity)
+    __shared__ int xch_abort[2];      // an exchange wait timed out (by row parity)
     cg::cluster_group cl = cg::this_cluster();
     const int tid = threadIdx.x;
     const int rank = (int)cl.block_rank();
-    const int64_t nclusters = gridDim.x / cl.num_blocks();
-    const int64_t cid = blockIdx.x / cl.num_blocks();
+    const unsigned cs = cl.num_blocks();
+    const int64_t nclusters = gridDim.x / cs;
+    const int64_t cid = blockIdx.x / cs;
     const int lo = rank * slice;                               // first column of this CTA
     const int hi = lo + slice < cols ? lo + slice : cols;
     const int nvec = hi > lo ? (hi - lo) / VEC : 0;            // vectors this CTA holds
-    const unsigned cs = cl.num_blocks();
+    const int64_t nlocal = cid < rows ? (rows - cid + nclusters - 1) / nclusters : 0;
+    const uint32_t pitch = (uint32_t)slice * (uint32_t)sizeof(T);           // per input, in a stage
+    const uint32_t my_bytes = (uint32_t)(nvec * VEC) * (uint32_t)sizeof(T);
+    const uint32_t stage_bytes = (uint32_t)NIN * pitch;
     if (tid == 0) {
         mbar_init(smem_addr(&xbar[0]), 1);
         mbar_init(smem_addr(&xbar[1]), 1);
-        abort_flag[0] = 0;
-        abort_flag[1] = 0;
+        if constexpr (STAGED) {
+            for (int q = 0; q < nstage; ++q) mbar_init(smem_addr(&sbar[q]), 1);
+        }
+        stage_abort[0] = stage_abort[1] = 0;
+        xch_abort[0] = xch_abort[1] = 0;
         fence_mbar_init();
     }
     cl.sync();      // every CTA's barriers are initialised before any push
     pdl_wait();
     pdl_launch_dependents();
 
-    // Loads of one row's slice (and of its per-column values); the planner
-    // leaves no rank empty, and indices stay in bounds regardless.
+    // STAGED: refill stage q with local row li (one elected thread).
+    auto issue = [&](int q, int64_t li) {
+        const int64_t row = cid + li * nclusters;
+        const uint32_t bar = smem_addr(&sbar[q]);
+        mbar_arrive_expect_tx(bar, (uint32_t)NIN * my_bytes);
+        if (my_bytes == 0) return;
+#pragma unroll
+        for (int i = 0; i < NIN; ++i)
+            bulk_g2s(smem_addr(ring + (size_t)q * stage_bytes + (size_t)i * pitch),
+                     a.in[i] + row * cols + lo, my_bytes, bar);
+    };
+    if constexpr (STAGED) {
+        if (tid == 0) {
+            const int64_t n0 = nlocal < nstage ? nlocal : nstage;
+            for (int q = 0; q < (int)n0; ++q) issue(q, q);
+        }
+    }
+
+    // Per-column values of the slots (and, DIRECT, the row's slice) for row
+    // r; the planner leaves no rank empty, and indices stay in bounds
+    // regardless.
     PrePC pre[VPT];
     PostPC post[kEarlyPost ? VPT : 1];
     Frag<T, VEC> in[VPT][NIN];
-    auto load_row = [&](int64_t r) {
+    auto load_cols = [&]() {
         if (nvec == 0) return;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
             C::template load_pre<VEC>(a, lo + vc * VEC, pre[k]);
             if constexpr (kEarlyPost) C::template load_post<VEC>(a, lo + vc * VEC, post[k]);
+        }
+    };
+    auto load_row = [&](int64_t r) {
+        if (nvec == 0) return;
+        load_cols();
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
 #pragma unroll
             for (int i = 0; i < NIN; ++i) in[k][i].load_stream(a.in[i] + r * cols + lo + vc * VEC);
         }
     };
-    if (cid < rows) load_row(cid);
+    if constexpr (!STAGED) {
+        if (nlocal > 0) load_row(cid);
+    }
 
     int rb = 0, xb = 0;
     uint32_t xpar[2] = {0u, 0u};
-    int64_t it = 0;
-    for (int64_t row = cid; row < rows; row += nclusters, ++it) {
+    int q = 0;                  // ring stage of local row li
+    uint32_t parity = 0;        // its phase parity
+    int64_t li = 0;
+    for (; li < nlocal; ++li) {
+        const int64_t row = cid + li * nclusters;
         const int64_t base = row * cols + lo;
         typename C::template Early<VEC> ea[VPT];
         if (nvec > 0) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
                 C::template early<VEC>(a, base + min(tid + k * (int)blockDim.x, nvec - 1) * VEC, ea[k]);
+        }
+        if constexpr (STAGED) {
+            load_cols();
+            if (!mbar_wait_bounded(smem_addr(&sbar[q]), parity)) stage_abort[li & 1] = 1;
+            const T *stage = reinterpret_cast<const T *>(ring + (size_t)q * stage_bytes);
+            if (nvec > 0) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
+#pragma unroll
+                    for (int i = 0; i < NIN; ++i)
+                        in[k][i].load_shared(stage + (size_t)i * slice + vc * VEC);
+                }
+            }
         }
         float v[VPT][VEC];
         float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
@@ -424,15 +489,20 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
                 if (vi < nvec) C::template store_pre<VEC>(v[k], a, base + vi * VEC);
             }
         }
-        // The input registers are free now: the next row's loads stay in
-        // flight through this row's reductions, cluster barriers and epilogue.
-        if (row + nclusters < rows) load_row(row + nclusters);
+        // DIRECT: the input registers are free now, so the next row's loads
+        // stay in flight through this row's reductions and epilogue.
+        if constexpr (!STAGED) {
+            if (li + 1 < nlocal) load_row(row + nclusters);
+        }
         const float c1 = C::kMaxFirst ? block_max(l1, red[rb]) : block_sum(l1, red[rb]);
         rb ^= 1;
-        // a wait that timed out in the previous row (flags alternate by row,
-        // as in the CTA engine, so every thread reads the same value here)
-        if (abort_flag[(it + 1) & 1]) break;
-        volatile int *ab = &abort_flag[it & 1];
+        // Timeouts: this row's stage wait, or an exchange of the previous row
+        // (flags alternate by row, so every thread reads the same values here).
+        if (stage_abort[li & 1] | xch_abort[(li + 1) & 1]) break;
+        if constexpr (STAGED) {
+            if (tid == 0 && li + nstage < nlocal) issue(q, li + nstage);
+        }
+        volatile int *ab = &xch_abort[li & 1];
         const float r1 = cluster_reduce<C::kMaxFirst>(c1, xch[xb], &xbar[xb], xpar[xb], cs, rank, ab);
         xb ^= 1;
         const float mean = C::stat1(r1, cols, a);
@@ -466,8 +536,29 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
                 o.store_stream(a.out + base + vi * VEC);
             }
         }
+        if constexpr (STAGED) {
+            if (++q == nstage) {
+                q = 0;
+                parity ^= 1u;
+            }
+        }
     }
-    if (tid == 0 && (abort_flag[0] | abort_flag[1])) atomicOr(err, kDevErrWaitTimeout);
+    if (tid == 0) {
+        if (li < nlocal || (xch_abort[0] | xch_abort[1])) atomicOr(err, kDevErrWaitTimeout);
+        if constexpr (STAGED) {
+            // Only after a timeout: wait (bounded) for this CTA's copies still
+            // in flight before its shared memory goes away.
+            int qq = q;
+            uint32_t pp = parity;
+            for (int64_t lj = li; lj < nlocal && lj < li + nstage; ++lj) {
+                (void)mbar_wait_bounded(smem_addr(&sbar[qq]), pp);
+                if (++qq == nstage) {
+                    qq = 0;
+                    pp ^= 1u;
+                }
+            }
+        }
+    }
     cl.sync();     // no CTA leaves while another may still push into its slots
 }
 
@@ -479,10 +570,15 @@ inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 inline int round_up32(int v) { return (v + 31) & ~31; }
 
 // Raises a kernel's dynamic shared memory limit to the device's opt-in
-// maximum (needed above 48 KB, before occupancy queries and launches).
+// maximum less the kernel's static shared memory (needed above 48 KB, before
+// occupancy queries and launches).
 inline cudaError_t allow_smem(const void *fn, const LaunchCtx &ctx, int bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ctx.smem_optin);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ctx.smem_optin - (int)fa.sharedSizeBytes);
 }
 
 template <class C> struct RowEngine {
@@ -541,23 +637,33 @@ template <class C> struct RowEngine {
         return nullptr;
     }
 
-    static const void *cluster_fn(int vpt, bool vec) {
+    static const void *cluster_fn(int vpt, bool vec, bool staged) {
         if (vec) {
-            switch (vpt) {
-                case 1: return (const void *)rows_cluster_kernel<C, 1, kVecN>;
-                case 2: return (const void *)rows_cluster_kernel<C, 2, kVecN>;
-                case 4: return (const void *)rows_cluster_kernel<C, 4, kVecN>;
-                case 8: if constexpr (kVecN == 4) return (const void *)rows_cluster_kernel<C, 8, kVecN>;
-                        break;
+            if (staged) {
+                switch (vpt) {
+                    case 1: return (const void *)rows_cluster_kernel<C, 1, kVecN, true>;
+                    case 2: return (const void *)rows_cluster_kernel<C, 2, kVecN, true>;
+                    case 4: return (const void *)rows_cluster_kernel<C, 4, kVecN, true>;
+                    case 8: if constexpr (kVecN == 4) return (const void *)rows_cluster_kernel<C, 8, kVecN, true>;
+                            break;
+                }
+            } else {
+                switch (vpt) {
+                    case 1: return (const void *)rows_cluster_kernel<C, 1, kVecN, false>;
+                    case 2: return (const void *)rows_cluster_kernel<C, 2, kVecN, false>;
+                    case 4: return (const void *)rows_cluster_kernel<C, 4, kVecN, false>;
+                    case 8: if constexpr (kVecN == 4) return (const void *)rows_cluster_kernel<C, 8, kVecN, false>;
+                            break;
+                }
             }
-        } else {
+        } else if (!staged) {
             switch (vpt) {
-                case 1: return (const void *)rows_cluster_kernel<C, 1, 1>;
-                case 2: return (const void *)rows_cluster_kernel<C, 2, 1>;
-                case 4: return (const void *)rows_cluster_kernel<C, 4, 1>;
-                case 8: return (const void *)rows_cluster_kernel<C, 8, 1>;
-                case 16: return (const void *)rows_cluster_kernel<C, 16, 1>;
-                case 32: return (const void *)rows_cluster_kernel<C, 32, 1>;
+                case 1: return (const void *)rows_cluster_kernel<C, 1, 1, false>;
+                case 2: return (const void *)rows_cluster_kernel<C, 2, 1, false>;
+                case 4: return (const void *)rows_cluster_kernel<C, 4, 1, false>;
+                case 8: return (const void *)rows_cluster_kernel<C, 8, 1, false>;
+                case 16: return (const void *)rows_cluster_kernel<C, 16, 1, false>;
+                case 32: return (const void *)rows_cluster_kernel<C, 32, 1, false>;
             }
         }
         return nullptr;
@@ -565,14 +671,16 @@ template <class C> struct RowEngine {
 
     // Resident clusters of `fn` with `cs` CTAs of `threads` threads (0 if none fit).
     static mb_status active_clusters(const LaunchCtx &ctx, const void *fn, int cs, int threads,
-                                     int *n) {
+                                     int smem, int *n) {
         cudaError_t e = cudaSuccess;
         if (cs > 8)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess) e = allow_smem(fn, ctx, smem);
         if (e != cudaSuccess) return cuda_fail(e);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs * ctx.sm_count);
         cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = (size_t)smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = cs;
@@ -591,7 +699,7 @@ template <class C> struct RowEngine {
     // One cluster of `cs` CTAs per row.  Each resident cluster keeps one row
     // in flight, so among cluster sizes 2, 4, 8, 16 (or the requested one) and
     // the vectors-per-thread that fit a slice in one CTA, take the launch with
-    // the most resident clusters (ties: the larger cluster); no rank is empty.
+    // the most resident clusters (ties: the smaller cluster); no rank is empty.
     // Launches holding at most kClusterElems values per thread come first: a
     // thread keeps its slice and the next row's prefetch in registers, and
     // more than that spills (sweeps on GB300: 16 values per thread ran LN fp32
@@ -610,7 +718,16 @@ template <class C> struct RowEngine {
     static mb_status plan_cluster_pass(const LaunchCtx &ctx, const RowTuning &tun,
                                        int64_t rows, int nvec, bool vec, int max_vpt_regs,
                                        RowPlan *p, const void **fn) {
+        // Staged (bulk-async ring) for bf16 rows that are vectorised and in
+        // device memory, ring depth kClusterRing; fp32 rows load directly.
+        // Sweeps on GB300 (LN, 65536 columns): bf16 staged 4.24 TB/s against
+        // 3.49 direct (its register prefetch holds unpacked floats, halving
+        // the resident threads); fp32 direct 6.10 against 5.53 staged.  A
+        // requested depth (ctas_per_sm on this path) stages any dtype.
+        const bool staged = vec && !tun.no_bulk && (sizeof(T) == 2 || tun.ctas_per_sm > 0);
+        const int VEC = vec ? kVecN : 1;
         int best_n = 0, best_cs = 0, best_vpt = 0, best_threads = 0, best_slice = 0;
+        int best_ring = 0, best_smem = 0;
         for (int cs0 : {2, 4, 8, 16}) {
             int cs = cs0;
             if (tun.stages >= 2 && tun.stages <= kMaxCluster) {
@@ -621,19 +738,29 @@ template <class C> struct RowEngine {
             const int slice_v = ceil_div(nvec, cs);
             cs = ceil_div(nvec, slice_v);                  // no empty rank
             if (cs < 2) continue;
+            const int64_t stage_bytes = (int64_t)C::kInputs * slice_v * VEC * (int64_t)sizeof(T);
+            int ring = 0, smem = 0;
+            if (staged) {
+                ring = tun.ctas_per_sm > 0 ? tun.ctas_per_sm : kClusterRing;
+                if (ring > kMaxStages) ring = kMaxStages;
+                // (the kernel's static shared memory stays within kHdrBytes)
+                while (ring > 1 && ring * stage_bytes + kHdrBytes > ctx.smem_optin) --ring;
+                if (stage_bytes + kHdrBytes > ctx.smem_optin) ring = 0;   // direct loads
+                smem = (int)(ring * stage_bytes);
+            }
             for (int vpt = 1; vpt <= max_vpt(vec); vpt *= 2) {
                 if (tun.vpt > 0 && vpt != tun.vpt) continue;
                 if (tun.vpt <= 0 && vpt > max_vpt_regs) continue;
                 if (ceil_div(slice_v, vpt) > kCtaMaxThreads) continue;
                 const int threads = round_up32(ceil_div(slice_v, vpt));
-                const void *f = cluster_fn(vpt, vec);
+                const void *f = cluster_fn(vpt, vec, ring > 0);
                 if (!f) continue;
                 int n = 0;
-                mb_status st = active_clusters(ctx, f, cs, threads, &n);
+                mb_status st = active_clusters(ctx, f, cs, threads, smem, &n);
                 if (st != MB_OK) return st;
-                if (n > best_n || (n == best_n && n > 0 && cs > best_cs)) {
+                if (n > best_n) {   // ties keep the smaller cluster (fewer exchange partners)
                     best_n = n; best_cs = cs; best_vpt = vpt; best_threads = threads;
-                    best_slice = slice_v;
+                    best_slice = slice_v; best_ring = ring; best_smem = smem;
                 }
             }
         }
@@ -643,12 +770,13 @@ template <class C> struct RowEngine {
             return plan_cluster(ctx, t2, rows, nvec, vec, p, fn);
         }
         if (!best_n) return MB_ERR_SHAPE;       // the caller tries the next pass
-        *fn = cluster_fn(best_vpt, vec);
+        *fn = cluster_fn(best_vpt, vec, best_ring > 0);
         const int64_t ncl = rows < best_n ? rows : best_n;
         p->path = MB_ROW_CLUSTER; p->threads = best_threads; p->vpt = best_vpt;
-        p->stages = best_cs; p->smem = 0;
+        p->stages = best_cs; p->smem = best_smem;
         p->ctas = (int)(ncl * best_cs);
         p->slice = best_slice;
+        p->ring = best_ring;
         p->cap = best_n;
         return MB_OK;
     }
@@ -872,7 +1000,7 @@ template <class C> struct RowEngine {
         if (C::outputs(a) > tn.outs) tn.outs = C::outputs(a);
         mb_status st = plan(ctx, tn, rows, cols, aligned, &p, &fn);
         if (st != MB_OK) return st;
-        if (launch && p.path == MB_ROW_STAGED) {
+        if (launch && (p.path == MB_ROW_STAGED || (p.path == MB_ROW_CLUSTER && p.ring > 0))) {
             // Bulk-async copies read device memory only: rows held in host
             // memory (pinned, read over the host link) take a plain-load path.
             bool dev = true;
@@ -893,7 +1021,8 @@ template <class C> struct RowEngine {
         // the fourth kernel argument: ring depth, or the cluster's slice length
         int stages_arg = p.path == MB_ROW_CLUSTER ? p.slice * p.vec : (p.stages > 0 ? p.stages : 1);
         unsigned *err = ctx.dev_err;
-        void *kargs[] = {&args, &rows_arg, &cols_arg, &stages_arg, &err};
+        int ring_arg = p.ring;      // the cluster kernel's sixth argument
+        void *kargs[] = {&args, &rows_arg, &cols_arg, &stages_arg, &err, &ring_arg};
         cudaError_t e = launch_kernel(lctx, fn, dim3(p.ctas), dim3(p.threads), kargs, p.smem,
                                       p.path == MB_ROW_CLUSTER ? p.stages : 1);
         if (e != cudaSuccess) return cuda_fail(e);

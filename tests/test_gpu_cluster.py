@@ -90,3 +90,22 @@ def test_long_rows_many_rows_and_unaligned():
     an unaligned scalar row length."""
     _check_chains(700, 40000, 5001, True)
     _check_chains(6, 33333, 5002, False)
+
+
+@pytest.mark.parametrize("ring", [1, 2, 3])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(11, 65536), (5, 40000), (9, 4096)])
+def test_staged_cluster_ring_depths(ring, bf16, shape, row_path):
+    """The bulk-copy ring of the cluster path at every depth, both dtypes
+    (auto stages bf16 only), more rows than stages."""
+    rows, cols = shape
+    row_path("cluster", ring, 0)
+    p = mb.row_plan("ln", "bf16" if bf16 else "f32", rows, cols)
+    assert p["path"] == "cluster" and p["smem"] > 0
+    _check_chains(rows, cols, 6000 + ring * 7 + cols % 101, bf16)
+
+
+def test_direct_cluster_when_rows_are_unaligned_or_fp32():
+    assert mb.row_plan("ln", "f32", 4, 65536)["smem"] == 0
+    assert mb.row_plan("ln", "bf16", 4, 65536)["smem"] > 0
+    assert mb.row_plan("ln", "bf16", 4, 65536, aligned=False)["smem"] == 0
