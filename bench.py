@@ -270,6 +270,23 @@ class Case:
                       approximate="tanh")
 
 
+class CopyCase:
+    """A plain device-to-device copy moving as many bytes as a workload's
+    call (half read, half written), cycling through buffer sets like Case:
+    the size-matched copy each kernel is compared with."""
+
+    def __init__(self, case, device):
+        import torch
+        from types import SimpleNamespace
+        self.w = SimpleNamespace(name=case.w.name)
+        n = case.ideal // 2 // 4
+        self.src = [torch.ones(n, dtype=torch.float32, device=device) for _ in range(case.nsets)]
+        self.dst = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(case.nsets)]
+
+    def call(self, k=0):
+        self.dst[k % len(self.dst)].copy_(self.src[k % len(self.src)])
+
+
 def aggregate_ranks(step_ms, step_bytes, world, device=None):
     """Whole-job throughput: every rank processed `step_bytes` per step; the
     job's step time is the slowest rank's.  Returns (max step ms, GB/s).
@@ -541,6 +558,9 @@ def run_ours(args):
         dist.barrier()
     clocks = clk.summary()
 
+    copies = [CopyCase(c, device) for c in cases]
+    copy_ms = time_graph(copies, lambda c, k: c.call(k), args.steps, 2)
+    del copies
     stream_api = time_steady(cases, lambda c, k: c.call(k), args.steps, 2)
     single = time_single_flushed(cases, lambda c, k: c.call(k), 7, flush)
     eager = None
@@ -569,7 +589,9 @@ def run_ours(args):
                  "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                  "buffer_sets": c.nsets,
                  "us_per_call_python_stream": round(stream_api[c.w.name] * 1e3, 3),
-                 "us_single_call_l2_flushed": round(single[c.w.name] * 1e3, 3)}
+                 "us_single_call_l2_flushed": round(single[c.w.name] * 1e3, 3),
+                 "size_matched_copy_us": round(copy_ms[c.w.name] * 1e3, 3),
+                 "frac_of_size_matched_copy": round(copy_ms[c.w.name] / mean_ms, 4)}
         if c.w.chain != "add_relu_scale":
             entry["launch"] = mb.row_plan("ln" if c.w.chain == "ln_gelu" else "inductor",
                                           c.w.dtype, c.w.rows, c.w.cols)
