@@ -352,8 +352,9 @@ def time_graph(cases, fn, steps, warmup):
 
 
 def time_single_flushed(cases, fn, reps, flush):
-    """Per case: median milliseconds of one call after an L2 flush (a 1 GiB
-    read, outside the events) -- the latency of an isolated call."""
+    """Per case: (p10, median, p90) milliseconds of one call after an L2
+    flush (a 1 GiB read, outside the events) -- the latency of an isolated
+    call and its spread."""
     import torch
     stream = torch.cuda.current_stream()
     out = {}
@@ -368,7 +369,8 @@ def time_single_flushed(cases, fn, reps, flush):
             b.record(stream)
             b.synchronize()
             ts.append(a.elapsed_time(b))
-        out[c.w.name] = statistics.median(ts)
+        q = np.percentile(np.array(ts), [10, 50, 90])
+        out[c.w.name] = tuple(float(v) for v in q)
     return out
 
 
@@ -562,7 +564,7 @@ def run_ours(args):
     copy_ms = time_graph(copies, lambda c, k: c.call(k), args.steps, 2)
     del copies
     stream_api = time_steady(cases, lambda c, k: c.call(k), args.steps, 2)
-    single = time_single_flushed(cases, lambda c, k: c.call(k), 7, flush)
+    single = time_single_flushed(cases, lambda c, k: c.call(k), 21, flush)
     eager = None
     if not args.no_eager:
         eager = time_graph(cases, lambda c, k: c.eager(k), max(5, args.steps // 5), 2)
@@ -589,7 +591,9 @@ def run_ours(args):
                  "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                  "buffer_sets": c.nsets,
                  "us_per_call_python_stream": round(stream_api[c.w.name] * 1e3, 3),
-                 "us_single_call_l2_flushed": round(single[c.w.name] * 1e3, 3),
+                 "us_single_call_l2_flushed": round(single[c.w.name][1] * 1e3, 3),
+                 "us_single_call_l2_flushed_p10_p90": [round(single[c.w.name][0] * 1e3, 3),
+                                                       round(single[c.w.name][2] * 1e3, 3)],
                  "size_matched_copy_us": round(copy_ms[c.w.name] * 1e3, 3),
                  "frac_of_size_matched_copy": round(copy_ms[c.w.name] / mean_ms, 4)}
         if c.w.chain != "add_relu_scale":
