@@ -479,6 +479,26 @@ def time_e2e_zero_copy(cases, steps, warmup):
     return ms, bi, bo
 
 
+def host_info():
+    """The CPU the oracle runs on: model and the cores this process may use."""
+    import platform
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = f"{platform.machine()} {ln.split(':', 1)[1].strip()}"
+                    break
+    except OSError:
+        pass
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except AttributeError:
+        avail = os.cpu_count()
+    return {"cpu": model, "cores_available": avail}
+
+
 def cpu_sample(fraction):
     """The inputs of a `fraction` sample of the step: the first rows of each
     row workload, the first elements of the pointwise one."""
@@ -538,6 +558,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, secs, sample = cpu_baseline(cpu_sample(0.25))
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "host": host_info(),
                "sample": f"first quarter of each workload ({sample}); {secs:.1f} s single-threaded"}
 
     props = torch.cuda.get_device_properties(device)
