@@ -289,7 +289,7 @@ int mb_last_cuda_error(void);
 
 /*
  * Reads and clears the device-side failure flags of the current device
- * (bit 0: a staged-row barrier wait ran out of time).  Synchronises the
+ * (bit 0: a staged-row or cluster-exchange barrier wait ran out of time).  Synchronises the
  * device.  *flags receives the bits; returns MB_ERR_DEVICE if any bit was
  * set, MB_OK if none, MB_ERR_NULL / MB_ERR_CUDA on failure.
  */
@@ -304,6 +304,16 @@ mb_status mb_device_error(uint32_t *flags);
  * context stays usable.  Asynchronous on `stream`.
  */
 mb_status mb_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
+/*
+ * Self-test of the cluster exchange's failure path: a cluster of two CTAs
+ * exchanges partials as the cluster row kernels do (st.async pushes that
+ * complete bytes on each CTA's own mbarrier), except that one push is never
+ * sent.  The waiting CTA's bounded wait (limit_us microseconds, 1 .. 1000000)
+ * runs out and records bit 0 in the device flags; both CTAs end normally.
+ * Asynchronous on `stream`.
+ */
+mb_status mb_selftest_exchange_timeout(uint32_t limit_us, cudaStream_t stream);
 
 /* Row-chain execution paths (all row chains). */
 typedef enum mb_row_path {

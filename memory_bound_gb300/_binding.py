@@ -36,6 +36,7 @@ SIGNATURES = {
     "mb_set_pointwise_shape": (_I, [_I, _I]),
     "mb_set_launch_overlap": (_I, [_I]),
     "mb_selftest_wait_timeout": (_I, [ctypes.c_uint32, _P]),
+    "mb_selftest_exchange_timeout": (_I, [ctypes.c_uint32, _P]),
     "mb_row_plan": (_I, [_I, _I, _I64, _I64, _I, _I32P]),
 }
 

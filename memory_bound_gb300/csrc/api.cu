@@ -398,6 +398,14 @@ mb_status mb_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
     return selftest_wait_timeout(ctx, limit_us);
 }
 
+mb_status mb_selftest_exchange_timeout(uint32_t limit_us, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return MB_ERR_VALUE;
+    LaunchCtx ctx;
+    mb_status st = device_ctx(stream, &ctx);
+    if (st != MB_OK) return st;
+    return selftest_exchange_timeout(ctx, limit_us);
+}
+
 mb_status mb_set_launch_overlap(int enable) {
     if (enable != 0 && enable != 1) return MB_ERR_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);

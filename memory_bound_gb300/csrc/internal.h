@@ -113,6 +113,7 @@ mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtyp
                        RowPlan *plan, bool launch);
 
 mb_status selftest_wait_timeout(const LaunchCtx &ctx, uint32_t limit_us);
+mb_status selftest_exchange_timeout(const LaunchCtx &ctx, uint32_t limit_us);
 
 // Records a CUDA error for mb_last_cuda_error and returns MB_ERR_CUDA.
 mb_status cuda_fail(cudaError_t e);

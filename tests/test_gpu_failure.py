@@ -38,3 +38,26 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert np.array_equal(to_host(y).view(np.uint32),
                           oracle.add_relu_scale(x, b1, b2, 0.5).view(np.uint32))
     assert lib.mb_selftest_wait_timeout(0, None) == 6          # MB_ERR_VALUE
+
+
+def test_cluster_exchange_timeout_is_reported_and_context_survives():
+    """The cluster exchange's bounded wait: one push never sent, the wait runs
+    out after 2 ms, the flag is reported, and a long-row call (the cluster
+    path) still works afterwards."""
+    from memory_bound_gb300 import build as lib_build
+    lib_build.build()
+    torch.cuda.set_device(0)
+    lib = mb.load_library()
+    assert mb.device_error() == 0
+    t0 = time.perf_counter()
+    assert lib.mb_selftest_exchange_timeout(2000, torch.cuda.current_stream().cuda_stream) == 0
+    flags = ctypes.c_uint32(0)
+    assert lib.mb_device_error(ctypes.byref(flags)) == 8
+    assert flags.value == 1
+    assert time.perf_counter() - t0 < 30
+    assert mb.device_error() == 0
+    x = synth.normal(1301, 0, (3, 65536))
+    y = mb.fused_row_softmax(to_dev(x))
+    want = oracle.row_softmax(x).astype(np.float64)
+    assert np.all(np.abs(to_host(y).astype(np.float64) - want) <= 1e-5 * want + 2.0 ** -126)
+    assert lib.mb_selftest_exchange_timeout(2000000, None) == 6
