@@ -40,6 +40,13 @@ static int args_mode(void)
     CHECK(fused_layernorm_act(A, NULL, C, D, E, NULL, 4, 64, 1e-5f, (mb_activation)7, MB_F32, 0) ==
           MB_ERR_VALUE);
     CHECK(fused_row_softmax(A, A, 4, 64, MB_F32, 0) == MB_ERR_OVERLAP);
+    CHECK(fused_layernorm_act_ex(A, B, C, D, E, NULL, NULL, NULL, 4, 64, 1e-5f, MB_ACT_RELU,
+                                 1.0f, 7u, 0u, MB_F32, 0) == MB_ERR_VALUE);
+    CHECK(fused_layernorm_act_ex(A, B, C, D, E, NULL, (float *)(A + 8), NULL, 4, 64, 1e-5f,
+                                 MB_ACT_RELU, 0.1f, 7u, 0u, MB_F32, 0) == MB_ERR_OVERLAP);
+    CHECK(fused_add_relu_scale_bcast(A, B, C, D, 4, 64, 2, 1, 0.5f, MB_F32, 0) == MB_ERR_VALUE);
+    CHECK(fused_add_relu_scale_bcast(A, B, C, A + 16, 4, 64, 1, 1, 0.5f, MB_F32, 0) ==
+          MB_ERR_OVERLAP);
     CHECK(mb_set_row_path(MB_ROW_AUTO, 0, 0, 0) == MB_OK);
     printf("args ok\n");
     return 0;
