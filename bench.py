@@ -634,12 +634,19 @@ def run_ours(args):
         t_next = time_graph(nxt, lambda c, k: c.call(k), args.steps, args.warmup)
         e_next = (time_graph(nxt, lambda c, k: c.eager(k), max(5, args.steps // 5), 2)
                   if not args.no_eager else None)
+        cp_next = {}
+        for c in nxt:                       # one chain's copies at a time (memory)
+            cc = CopyCase(c, device)
+            cp_next.update(time_graph([cc], lambda x, k: x.call(k), args.steps, 2))
+            del cc
         next_rows = {}
         for c in nxt:
             ms = t_next[c.w.name]
             gbs = c.ideal / (ms * 1e-3) / 1e9
             ent = {"us_per_call": round(ms * 1e3, 3), "ideal_bytes": c.ideal,
-                   "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+                   "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                   "size_matched_copy_us": round(cp_next[c.w.name] * 1e3, 3),
+                   "frac_of_size_matched_copy": round(cp_next[c.w.name] / ms, 4)}
             if e_next:
                 ent["eager_us_per_call"] = round(e_next[c.w.name] * 1e3, 3)
                 ent["speedup_vs_eager"] = round(e_next[c.w.name] / ms, 2)
