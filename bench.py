@@ -273,7 +273,11 @@ class Case:
 class CopyCase:
     """A plain device-to-device copy moving as many bytes as a workload's
     call (half read, half written), cycling through buffer sets like Case:
-    the size-matched copy each kernel is compared with."""
+    the size-matched copy each kernel is compared with.  Copies are issued in
+    pieces of at most 256 MiB: single copies above about 1 GB ran at half the
+    speed on GB300, which would flatter the kernels."""
+
+    PIECE = 64 << 20     # floats (256 MiB)
 
     def __init__(self, case, device):
         import torch
@@ -284,7 +288,9 @@ class CopyCase:
         self.dst = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(case.nsets)]
 
     def call(self, k=0):
-        self.dst[k % len(self.dst)].copy_(self.src[k % len(self.src)])
+        d, src = self.dst[k % len(self.dst)], self.src[k % len(self.src)]
+        for a in range(0, d.numel(), self.PIECE):
+            d[a:a + self.PIECE].copy_(src[a:a + self.PIECE])
 
 
 def aggregate_ranks(step_ms, step_bytes, world, device=None):
