@@ -106,3 +106,39 @@ def test_graph_layernorm(w):
         want = oracle.residual_layernorm_gelu(t["x"], t["r"], t["w"], t["b"], 1e-5)
         assert_close(to_host(out), want, bf16=bf16, what=f"replay seed {seed}")
     assert np.all(np.isfinite(to_host(out).astype(np.float32) if not bf16 else 1.0))
+
+
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_graph_long_rows_cluster_path(bf16):
+    """Rows of 65536 elements (one cluster per row: staged for bf16, direct
+    for fp32) and LayerNorm -> ReLU -> Dropout, captured and replayed on new
+    inputs copied into the captured buffers."""
+    import synth
+    rows, cols = 12, 65536
+    dt = "bf16" if bf16 else "f32"
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    assert mb.row_plan("ln", dt, rows, cols)["path"] == "cluster"
+    dx = torch.empty(rows, cols, dtype=tdt, device="cuda")
+    dr = torch.empty_like(dx)
+    w = to_dev(synth.uniform(77, 2, (cols,), 0.5, 1.5, dtype=dt), bf16)
+    b = to_dev(synth.normal(77, 3, (cols,), 0.0, 0.1, dtype=dt), bf16)
+    out = torch.empty_like(dx)
+    dout = torch.empty_like(dx)
+    def calls():
+        mb.fused_residual_layernorm_gelu(dx, dr, w, b, 1e-5, out=out)
+        mb.fused_layernorm_act(dx, None, w, b, act="relu", out=dout, p=0.1, seed=5, offset=3)
+    x0 = synth.normal(78, 0, (rows, cols), dtype=dt)
+    r0 = synth.normal(78, 1, (rows, cols), dtype=dt)
+    dx.copy_(to_dev(x0, bf16)); dr.copy_(to_dev(r0, bf16))
+    g = _capture(calls)
+    for seed in (79, 80):
+        x = synth.normal(seed, 0, (rows, cols), dtype=dt)
+        r = synth.normal(seed, 1, (rows, cols), dtype=dt)
+        dx.copy_(to_dev(x, bf16)); dr.copy_(to_dev(r, bf16))
+        g.replay()
+        torch.cuda.synchronize()
+        wh, bh = to_host(w), to_host(b)
+        assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, wh, bh, 1e-5), bf16=bf16)
+        want, _, _, _ = oracle.layernorm_act_ex(x, None, wh, bh, 1e-5, oracle.ACT_RELU, p=0.1,
+                                                seed=5, offset=3)
+        assert_close(to_host(dout), want, bf16=bf16)
