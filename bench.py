@@ -524,12 +524,15 @@ def host_info():
     """The CPU the oracle runs on: model and the cores this process may use."""
     import platform
     model = platform.processor() or platform.machine()
+    arm_parts = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+                 "0xd49": "Arm Neoverse N2", "0xd8f": "Arm Neoverse V3"}
     try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
                 key = ln.split(":")[0].strip().lower()
-                if key in ("model name", "cpu part", "hardware"):
-                    model = f"{platform.machine()} {ln.split(':', 1)[1].strip()}"
+                if key in ("model name", "cpu part"):
+                    val = ln.split(":", 1)[1].strip()
+                    model = f"{platform.machine()} {arm_parts.get(val, val)}"
                     break
     except OSError:
         pass
