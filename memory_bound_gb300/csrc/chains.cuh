@@ -86,6 +86,8 @@ template <typename TT> struct LnGeluChain {
     using T = TT;
     static constexpr int kInputs = 2;     // x, r
     static constexpr int kVec = Elem<T>::kVec;   // elements per vector slot (16 bytes)
+    static constexpr bool kRegCap = false;     // see LnActChain
+    static constexpr int kRowsTarget = 0;
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = false;
@@ -151,6 +153,8 @@ template <typename TT> struct InductorChainT {
     using T = TT;
     static constexpr int kInputs = 1;     // x
     static constexpr int kVec = Elem<T>::kVec;
+    static constexpr bool kRegCap = false;     // see LnActChain
+    static constexpr int kRowsTarget = 0;
     static constexpr bool kTwoPass = false;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = false;
@@ -245,6 +249,15 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     // with dropout a slot is eight elements (one generator block; 32 bytes
     // of fp32), else 16 bytes
     static constexpr int kVec = DROP ? 8 : Elem<T>::kVec;
+    // With dropout on fp32 rows the kernel is latency-bound (the generator's
+    // multiply chains): registers capped (rows_cta_kernel_capped) so that six
+    // 256-thread CTAs share an SM, and six rows in flight per SM.  Measured
+    // on GB300 (8192 x 4096 fp32): 49.4 us against 51.2 uncapped with four.
+    // bf16 rows hold twice the values per byte and would spill under the cap,
+    // and the cap slows the other chains (LN bf16 245 -> 296 us): they keep
+    // the ordinary kernel.
+    static constexpr bool kRegCap = DROP && sizeof(T) == 4;
+    static constexpr int kRowsTarget = kRegCap ? 6 : 0;
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = true;
@@ -338,6 +351,8 @@ template <typename TT> struct SoftmaxChain {
     using T = TT;
     static constexpr int kInputs = 1;
     static constexpr int kVec = Elem<T>::kVec;
+    static constexpr bool kRegCap = false;     // see LnActChain
+    static constexpr int kRowsTarget = 0;
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = true;
     static constexpr bool kStorePre = false;

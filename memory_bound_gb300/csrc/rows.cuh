@@ -48,6 +48,7 @@ constexpr int kWarpBlock = 256;
 constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
 constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
+constexpr int kCappedRegs = 40;   // registers per thread of rows_cta_kernel_capped
 // Bytes of row reads and writes per SM in flight beyond which more resident
 // rows stop paying (sweeps on GB300: LayerNorm rows of 48 KB in + out run
 // fastest three to an SM in fp32, four in bf16, whose rows carry twice the
@@ -150,8 +151,8 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
 // one CTA per row, persistent; DIRECT or STAGED (bulk-async shared ring)
 // ---------------------------------------------------------------------------
 template <class C, int VPT, int VEC, bool STAGED>
-__global__ void __launch_bounds__(kCtaMaxThreads)
-rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, unsigned *err) {
+__device__ __forceinline__ void rows_cta_body(const typename C::Args &a, int64_t rows, int cols,
+                                              int nstage, unsigned *err) {
     using T = typename C::T;
     constexpr int NIN = C::kInputs;
     // The epilogue's per-column values are loaded with the row (before the
@@ -310,6 +311,20 @@ rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, un
             }
         }
     }
+}
+
+template <class C, int VPT, int VEC, bool STAGED>
+__global__ void __launch_bounds__(kCtaMaxThreads)
+rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, unsigned *err) {
+    rows_cta_body<C, VPT, VEC, STAGED>(a, rows, cols, nstage, err);
+}
+
+// The same engine with the registers per thread capped (chains with
+// C::kRegCap): more CTAs resident per SM for latency-bound chains.
+template <class C, int VPT, int VEC, bool STAGED>
+__global__ void __maxnreg__(kCappedRegs)
+rows_cta_kernel_capped(const typename C::Args a, int64_t rows, int cols, int nstage, unsigned *err) {
+    rows_cta_body<C, VPT, VEC, STAGED>(a, rows, cols, nstage, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -605,33 +620,39 @@ template <class C> struct RowEngine {
     }
     // Vector slots per thread allowed on the CTA engine: VPT * VEC <= 32.
     static int max_vpt(bool vec) { return vec ? 32 / kVecN : 32; }
+    // The CTA engine's kernels: the register-capped form for chains that ask
+    // for it (C::kRegCap), the ordinary one otherwise.
+    template <int VPT, int VEC, bool STAGED> static const void *cta_kernel() {
+        if constexpr (C::kRegCap) return (const void *)rows_cta_kernel_capped<C, VPT, VEC, STAGED>;
+        else return (const void *)rows_cta_kernel<C, VPT, VEC, STAGED>;
+    }
     static const void *cta_fn(int vpt, bool vec, bool staged) {
         if (vec) {
             if (staged) {
                 switch (vpt) {
-                    case 1: return (const void *)rows_cta_kernel<C, 1, kVecN, true>;
-                    case 2: return (const void *)rows_cta_kernel<C, 2, kVecN, true>;
-                    case 4: return (const void *)rows_cta_kernel<C, 4, kVecN, true>;
-                    case 8: if constexpr (kVecN == 4) return (const void *)rows_cta_kernel<C, 8, kVecN, true>;
+                    case 1: return cta_kernel<1, kVecN, true>();
+                    case 2: return cta_kernel<2, kVecN, true>();
+                    case 4: return cta_kernel<4, kVecN, true>();
+                    case 8: if constexpr (kVecN == 4) return cta_kernel<8, kVecN, true>();
                             break;
                 }
             } else {
                 switch (vpt) {
-                    case 1: return (const void *)rows_cta_kernel<C, 1, kVecN, false>;
-                    case 2: return (const void *)rows_cta_kernel<C, 2, kVecN, false>;
-                    case 4: return (const void *)rows_cta_kernel<C, 4, kVecN, false>;
-                    case 8: if constexpr (kVecN == 4) return (const void *)rows_cta_kernel<C, 8, kVecN, false>;
+                    case 1: return cta_kernel<1, kVecN, false>();
+                    case 2: return cta_kernel<2, kVecN, false>();
+                    case 4: return cta_kernel<4, kVecN, false>();
+                    case 8: if constexpr (kVecN == 4) return cta_kernel<8, kVecN, false>();
                             break;
                 }
             }
         } else if (!staged) {
             switch (vpt) {
-                case 1: return (const void *)rows_cta_kernel<C, 1, 1, false>;
-                case 2: return (const void *)rows_cta_kernel<C, 2, 1, false>;
-                case 4: return (const void *)rows_cta_kernel<C, 4, 1, false>;
-                case 8: return (const void *)rows_cta_kernel<C, 8, 1, false>;
-                case 16: return (const void *)rows_cta_kernel<C, 16, 1, false>;
-                case 32: return (const void *)rows_cta_kernel<C, 32, 1, false>;
+                case 1: return cta_kernel<1, 1, false>();
+                case 2: return cta_kernel<2, 1, false>();
+                case 4: return cta_kernel<4, 1, false>();
+                case 8: return cta_kernel<8, 1, false>();
+                case 16: return cta_kernel<16, 1, false>();
+                case 32: return cta_kernel<32, 1, false>();
             }
         }
         return nullptr;
@@ -924,6 +945,7 @@ template <class C> struct RowEngine {
         const int64_t budget = sizeof(T) == 2 ? kFlightBytesBf16 : kFlightBytesF32;
         int target = (int)(budget / row_io < kRowsInFlight ? budget / row_io : kRowsInFlight);
         if (target < 2) target = 2;
+        if (C::kRowsTarget > 0) target = C::kRowsTarget;     // the chain's own measured target
         const bool heavy = target < kRowsInFlight;      // the budget binds
         int best_vpt = 0, best_occ = 0, best_threads = 0;
         for (int cand = 1; cand <= max_vpt(vec); cand *= 2) {
