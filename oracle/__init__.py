@@ -110,6 +110,10 @@ def load(path=None):
     lib.oracle_dropout_keep.restype = ctypes.c_int
     lib.oracle_dropout_mask.argtypes = [u64, u64, i64, i64, f32, ctypes.POINTER(ctypes.c_uint8)]
     lib.oracle_dropout_mask.restype = None
+    lib.oracle_scale_mask_softmax_f32.argtypes = [F32P, F32P, i64, i64, f32, ctypes.c_int, i64, i64]
+    lib.oracle_scale_mask_softmax_f32.restype = None
+    lib.oracle_scale_mask_softmax_bf16.argtypes = [U16P, U16P, i64, i64, f32, ctypes.c_int, i64, i64]
+    lib.oracle_scale_mask_softmax_bf16.restype = None
     lib.oracle_row_softmax_f32.argtypes = [F32P, F32P, i64, i64]
     lib.oracle_row_softmax_f32.restype = None
     lib.oracle_row_softmax_bf16.argtypes = [U16P, U16P, i64, i64]
@@ -390,6 +394,26 @@ def row_softmax(x, lib=None):
         lib.oracle_row_softmax_f32(_f32p(x), _f32p(y), rows, cols)
     elif x.dtype == np.uint16:
         lib.oracle_row_softmax_bf16(_u16p(x), _u16p(y), rows, cols)
+    else:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    return y
+
+
+def scale_mask_softmax(x, scale=1.0, causal=False, period=None, offset=0, lib=None):
+    """Softmax of each row of x * scale, with an optional causal mask: element
+    j of row i is masked when j > (i mod period) + offset (period defaults to
+    the row count); masked outputs are 0."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    period = rows if period is None else period
+    y = np.empty_like(x)
+    if x.dtype == np.float32:
+        lib.oracle_scale_mask_softmax_f32(_f32p(x), _f32p(y), rows, cols, float(scale),
+                                          int(bool(causal)), int(period), int(offset))
+    elif x.dtype == np.uint16:
+        lib.oracle_scale_mask_softmax_bf16(_u16p(x), _u16p(y), rows, cols, float(scale),
+                                           int(bool(causal)), int(period), int(offset))
     else:
         raise TypeError(f"unsupported dtype {x.dtype}")
     return y

@@ -574,3 +574,60 @@ void oracle_row_softmax_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64
 {
     o5_rows(x, load_bf16, y, 1, rows, cols);
 }
+
+/* o5 on attention scores ([P1] §4.1: the score matrix is scaled before the
+ * softmax; §4.2: a causal mask keeps each query from the keys after it):
+ * v = x * scale, one fp32 multiply; with causal masking element j of row i is
+ * masked when j > (i mod period) + offset (row i is query i mod period of its
+ * head; offset aligns the diagonal), and masked elements take no part: the
+ * softmax runs in double over the row's unmasked elements, masked outputs
+ * are 0. */
+static float o5m_value(const void *x, o3_load_fn load, int64_t k, float scale)
+{
+    float v = load(x, k) * scale;
+    return v;
+}
+
+static void o5m_rows(const void *x, o3_load_fn load, void *y, int bf16, int64_t rows,
+                     int64_t cols, float scale, int causal, int64_t period, int64_t offset)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        int64_t base = i * cols;
+        int64_t end = cols;                     /* elements [0, end) are unmasked */
+        if (causal) {
+            int64_t last = i % period + offset; /* the last key query i may see */
+            if (last + 1 < end)
+                end = last + 1;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < end; ++j) {
+            double v = (double)o5m_value(x, load, base + j, scale);
+            if (v > m)
+                m = v;
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < end; ++j)
+            sum += exp((double)o5m_value(x, load, base + j, scale) - m);
+        for (int64_t j = 0; j < cols; ++j) {
+            double p = 0.0;
+            if (j < end)
+                p = exp((double)o5m_value(x, load, base + j, scale) - m) / sum;
+            if (bf16)
+                ((uint16_t *)y)[base + j] = oracle_bf16_from_double(p);
+            else
+                ((float *)y)[base + j] = (float)p;
+        }
+    }
+}
+
+void oracle_scale_mask_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols,
+                                   float scale, int causal, int64_t period, int64_t offset)
+{
+    o5m_rows(x, load_f32, y, 0, rows, cols, scale, causal, period, offset);
+}
+
+void oracle_scale_mask_softmax_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                                    float scale, int causal, int64_t period, int64_t offset)
+{
+    o5m_rows(x, load_bf16, y, 1, rows, cols, scale, causal, period, offset);
+}

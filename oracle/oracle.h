@@ -144,6 +144,15 @@ void oracle_dropout_mask(uint64_t seed, uint64_t offset, int64_t start, int64_t 
 void oracle_row_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols);
 void oracle_row_softmax_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols);
 
+/* ---- o5 on attention scores ([P1] §4.1 scaled scores, §4.2 causal mask):
+ *   v = x * scale (one fp32 multiply); causal: element j of row i is masked
+ *   when j > (i mod period) + offset; y = softmax over the unmasked elements
+ *   (double, as o5), masked outputs 0.  period >= 1, offset >= 0. */
+void oracle_scale_mask_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols,
+                                   float scale, int causal, int64_t period, int64_t offset);
+void oracle_scale_mask_softmax_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                                    float scale, int causal, int64_t period, int64_t offset);
+
 #ifdef __cplusplus
 }
 #endif

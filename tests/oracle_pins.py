@@ -633,4 +633,51 @@ def pin_layernorm_dropout(lib):
         assert 0.6 < keep.mean() < 0.9
 
 
+def pin_scale_mask_softmax_library(lib):
+    """[P1] §4.1-4.2's scaled, causally masked score rows: torch float64
+    softmax of the fp32 product x * scale with the masked keys filled with
+    -inf, within one fp32 rounding; masked outputs exactly 0; with period p
+    and offset k, row i keeps keys 0 .. (i mod p) + k; bf16 within half a step."""
+    rows, cols, period, offset = 12, 9, 4, 2
+    x = synth.normal(65, 0, (rows, cols), 0.0, 3.0)
+    scale = np.float32(0.3)
+    y = oracle.scale_mask_softmax(x, scale, True, period, offset, lib=lib).astype(np.float64)
+    v = torch.from_numpy((x * scale).astype(np.float32)).double()      # the fp32 product
+    i = torch.arange(rows)[:, None] % period + offset
+    j = torch.arange(cols)[None, :]
+    masked = j > i
+    want = torch.softmax(v.masked_fill(masked, float("-inf")), dim=1).numpy()
+    assert np.all(y[masked.numpy()] == 0.0)
+    assert np.all(np.abs(y - want) <= U32 * want * 1.0001)
+    assert np.all(np.abs(y.sum(axis=1) - 1.0) <= cols * U32)
+    y0 = oracle.scale_mask_softmax(x, 1.0, True, period, 0, lib=lib)
+    assert np.array_equal(y0[0], np.eye(cols, dtype=np.float32)[0])       # query 0 sees key 0
+    xb = synth.normal(66, 0, (8, 40), 0.0, 2.0, dtype="bf16")
+    vb = torch.from_numpy(synth.bf16_bits_to_f32(xb) * np.float32(0.25)).double()
+    mb_ = torch.arange(40)[None, :] > (torch.arange(8)[:, None] % 8 + 30)
+    wb = torch.softmax(vb.masked_fill(mb_, float("-inf")), dim=1).numpy()
+    gb = synth.bf16_bits_to_f32(oracle.scale_mask_softmax(xb, 0.25, True, 8, 30, lib=lib))
+    assert np.all(np.abs(gb.astype(np.float64) - wb) <= 2.0 ** -8 * wb * 1.0001 + 1e-40)
+
+
+def pin_scale_mask_softmax_special_cases(lib):
+    """No mask and scale 1: the plain row softmax bit for bit; an offset past
+    the row length masks nothing; scale 2^-3 is exact, so scaling the input
+    by hand gives the same bits."""
+    x = synth.normal(67, 0, (5, 33), 0.0, 2.0)
+    plain = oracle.row_softmax(x, lib=lib)
+    assert np.array_equal(oracle.scale_mask_softmax(x, 1.0, False, lib=lib), plain)
+    assert np.array_equal(oracle.scale_mask_softmax(x, 1.0, True, 5, 40, lib=lib), plain)
+    a = oracle.scale_mask_softmax(x, 0.125, True, 5, 3, lib=lib)
+    b = oracle.scale_mask_softmax((x * np.float32(0.125)).astype(np.float32), 1.0, True, 5, 3,
+                                  lib=lib)
+    assert np.array_equal(a, b)
+    # masked elements take no part, however large: a masked +1000 changes nothing
+    big = x.copy()
+    big[1, 20] = 1000.0                     # row 1 keeps keys 0 .. 4
+    m1 = oracle.scale_mask_softmax(big, 1.0, True, 5, 3, lib=lib)
+    m0 = oracle.scale_mask_softmax(x, 1.0, True, 5, 3, lib=lib)
+    assert np.all(np.isfinite(m1)) and np.array_equal(m1, m0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

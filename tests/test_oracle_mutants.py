@@ -103,6 +103,15 @@ MUTANTS = {
     "dropout_scale_inverted": ("g = g / (1.0 - (double)ex->p);", "g = g * (1.0 - (double)ex->p);"),
     "dropout_dropped_kept": ("                else\n                    g = g * 0.0;",
                              "                else\n                    g = g * 1.0;"),
+    "o5m_mask_off_by_one": ("if (last + 1 < end)\n                end = last + 1;",
+                            "if (last < end)\n                end = last;"),
+    "o5m_period_ignored": ("int64_t last = i % period + offset;", "int64_t last = i + offset;"),
+    "o5m_offset_ignored": ("int64_t last = i % period + offset;", "int64_t last = i % period;"),
+    "o5m_scale_dropped": ("float v = load(x, k) * scale;", "float v = load(x, k);"),
+    "o5m_masked_not_zero": ("            double p = 0.0;\n            if (j < end)",
+                            "            double p = 1e-30;\n            if (j < end)"),
+    "o5m_max_over_row": ("        double m = -INFINITY;\n        for (int64_t j = 0; j < end; ++j) {\n            double v = (double)o5m_value",
+                         "        double m = -INFINITY;\n        for (int64_t j = 0; j < cols; ++j) {\n            double v = (double)o5m_value"),
     "o5_min_not_max": ("if (v > m)\n                m = v;", "if (v < m || m == -INFINITY)\n                m = v;"),
 }
 
