@@ -224,6 +224,9 @@ class Case:
                                                     p["x_scale"], p["branch_scale"], out=out)
         elif self.w.chain == "softmax":
             mb.fused_row_softmax(d["x"], out=out)
+        elif self.w.chain == "softmax_mask":
+            mb.fused_row_softmax(d["x"], out=out, scale=p["scale"], causal=p["causal"],
+                                 period=p["period"], offset=p["offset"])
         elif self.w.chain == "lnact":
             mb.fused_layernorm_act(d["x"], d.get("r"), d["w"], d["b"], eps=p["eps"],
                                    act=p["act"], out=out,
@@ -256,6 +259,13 @@ class Case:
             return torch.relu(d["x"] + d["b1"]) * p["scale"] + d["b2"]
         if self.w.chain == "softmax":
             return torch.softmax(d["x"], dim=1)
+        if self.w.chain == "softmax_mask":
+            if not hasattr(self, "_mask"):
+                q = torch.arange(self.w.rows, device=d["x"].device)[:, None] % p["period"]
+                k = torch.arange(self.w.cols, device=d["x"].device)[None, :]
+                self._mask = k > q + p["offset"]          # built once, outside the timing
+            return torch.softmax((d["x"] * p["scale"]).masked_fill(self._mask, float("-inf")),
+                                 dim=1)
         if self.w.chain == "lnact":
             v = d["x"] + d["r"] if "r" in d else d["x"]
             n = F.layer_norm(v, (self.w.cols,), d["w"], d["b"], p["eps"])

@@ -13,7 +13,8 @@
  * (per-column b1 / b2), and, built on the same row engines,
  * fused_layernorm_act (LayerNorm with an optional residual, residual-stream
  * output and activation) and its extended form fused_layernorm_act_ex
- * (dropout, per-row statistics), fused_row_softmax and the bf16 variant of the
+ * (dropout, per-row statistics), fused_row_softmax, its scaled and causally
+ * masked form fused_scale_mask_softmax and the bf16 variant of the
  * TorchInductor chain.
  *
  * Sources (the pages these chains come from):
@@ -263,6 +264,28 @@ mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols,
                             mb_dtype dtype, cudaStream_t stream);
 
 /*
+ * Softmax of attention-score rows, scaled and optionally causally masked:
+ *   v[i, j] = x[i, j] * scale (one fp32 multiply; the caller passes 1/sqrt(d));
+ *   key j of row i is masked when causal and j > (i mod period) + offset;
+ *   y[i, j] = exp(v[i, j] - m_i) / sum_k exp(v[i, k] - m_i) over the unmasked
+ *   keys (m_i their maximum), and y = 0 where masked.
+ * [P1] §4.1 (the score matrix divided by a scale before the softmax, rows of
+ * batch x heads x seq_len queries) and §4.2 (a causal mask that keeps each
+ * query from the keys after it).  Rows are (batch, head, query) flattened
+ * with `period` queries per head; offset >= 0 aligns the diagonal (seq_k -
+ * seq_q for bottom-right alignment), so no row is fully masked.  Masked keys
+ * take no part whatever their value, and the masked tail of a row is not read
+ * on the staged paths.
+ *
+ *   x, y    rows x cols (input, output)        1 <= cols <= MB_MAX_COLS
+ *   scale   finite, else MB_ERR_VALUE
+ *   causal  0 or 1; with 1, period >= 1 and offset >= 0, else MB_ERR_VALUE
+ */
+mb_status fused_scale_mask_softmax(const void *x, void *y, int64_t rows, int64_t cols,
+                                   float scale, int causal, int64_t period, int64_t offset,
+                                   mb_dtype dtype, cudaStream_t stream);
+
+/*
  * fused_bias_relu_branch_mean_epilogue with bf16 I/O: x, bias, gamma, beta
  * and y are bf16 bit patterns; inputs are widened exactly, the same fp32
  * steps run, and y is rounded once to bf16.
@@ -371,7 +394,7 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * GeLU, 1 the TorchInductor chain, 2 the LayerNorm family with a residual,
  * 3 without, 4 row softmax, 5 and 6 the LayerNorm family with dropout (with
  * a residual, without), 7 the LayerNorm family with a residual that also
- * writes the residual stream h.  `aligned` says whether every pointer is 16-byte
+ * writes the residual stream h, 8 the scaled, causally masked softmax.  `aligned` says whether every pointer is 16-byte
  * aligned.  Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,

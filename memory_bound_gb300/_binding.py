@@ -28,6 +28,7 @@ SIGNATURES = {
     "fused_layernorm_act_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _F,
                                     ctypes.c_uint64, ctypes.c_uint64, _I, _P]),
     "fused_row_softmax": (_I, [_P, _P, _I64, _I64, _I, _P]),
+    "fused_scale_mask_softmax": (_I, [_P, _P, _I64, _I64, _F, _I, _I64, _I64, _I, _P]),
     "mb_status_string": (ctypes.c_char_p, [_I]),
     "mb_abi_version": (_I, []),
     "mb_last_cuda_error": (_I, []),
@@ -325,8 +326,12 @@ def fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", out=None, h_out=N
     return (out, h_out) if h_out is not None else out
 
 
-def fused_row_softmax(x, out=None):
-    """Softmax over the last dim of a 2-D x (float32 or bfloat16)."""
+def fused_row_softmax(x, out=None, scale=1.0, causal=False, period=None, offset=0):
+    """Softmax over the last dim of a 2-D x (float32 or bfloat16).
+
+    With ``scale`` != 1 or ``causal``: the softmax of attention-score rows
+    x * scale, key j of row i masked when j > (i mod period) + offset
+    (period defaults to the row count); masked outputs are 0."""
     if x.dim() != 2:
         raise ValueError("x must be 2-D (rows, cols)")
     if out is None:
@@ -335,10 +340,18 @@ def fused_row_softmax(x, out=None):
     if out.numel() != x.numel():
         raise ValueError("out must match x")
     rows, cols = x.shape
+    if scale == 1.0 and not causal:
+        with _on_device(dev):
+            st = load_library().fused_row_softmax(x.data_ptr(), out.data_ptr(), rows, cols,
+                                                  _dtype_code(x), _stream_handle(dev))
+        _check("fused_row_softmax", st)
+        return out
+    per = rows if period is None else int(period)
     with _on_device(dev):
-        st = load_library().fused_row_softmax(x.data_ptr(), out.data_ptr(), rows, cols,
-                                              _dtype_code(x), _stream_handle(dev))
-    _check("fused_row_softmax", st)
+        st = load_library().fused_scale_mask_softmax(
+            x.data_ptr(), out.data_ptr(), rows, cols, float(scale), int(bool(causal)),
+            max(per, 1), int(offset), _dtype_code(x), _stream_handle(dev))
+    _check("fused_scale_mask_softmax", st)
     return out
 
 
@@ -373,11 +386,12 @@ def set_pointwise_shape(blocks_per_sm=0, unroll=0):
 def row_plan(chain, dtype, rows, cols, aligned=True):
     """The launch a row chain would use: dict(path, threads, ctas, vpt, vec,
     stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact", "softmax",
-    "lnact_res_dropout", "lnact_dropout" or "lnact_res_h" (with the
-    residual-stream output); dtype: "f32" or "bf16"."""
+    "lnact_res_dropout", "lnact_dropout", "lnact_res_h" (with the
+    residual-stream output) or "softmax_mask"; dtype: "f32" or "bf16"."""
     out = (ctypes.c_int32 * 7)()
     code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4,
-            "lnact_res_dropout": 5, "lnact_dropout": 6, "lnact_res_h": 7}[chain]
+            "lnact_res_dropout": 5, "lnact_dropout": 6, "lnact_res_h": 7,
+            "softmax_mask": 8}[chain]
     dt = {"f32": MB_F32, "bf16": MB_BF16}[dtype]
     st = load_library().mb_row_plan(code, dt, rows, cols, int(bool(aligned)), out)
     _check("mb_row_plan", st)

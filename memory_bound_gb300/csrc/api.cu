@@ -346,6 +346,27 @@ mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols, 
     return softmax_rows(ctx, g_tuning, dtype, x, y, rows, (int)cols, aligned, nullptr, true);
 }
 
+mb_status fused_scale_mask_softmax(const void *x, void *y, int64_t rows, int64_t cols,
+                                   float scale, int causal, int64_t period, int64_t offset,
+                                   mb_dtype dtype, cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
+    mb_status st = check_rows(rows, cols);
+    if (st != MB_OK) return st;
+    if (!std::isfinite(scale) || (causal != 0 && causal != 1)) return MB_ERR_VALUE;
+    if (causal && (period < 1 || offset < 0)) return MB_ERR_VALUE;
+    if (rows == 0) return MB_OK;
+    if (!x || !y) return MB_ERR_NULL;
+    const int es = elem_size(dtype);
+    if (!aligned_to(x, es) || !aligned_to(y, es)) return MB_ERR_ALIGN;
+    const int64_t big = rows * cols * es;
+    if (overlaps(y, big, x, big)) return MB_ERR_OVERLAP;
+    const bool aligned = aligned_to(x, 16) && aligned_to(y, 16);
+    LaunchCtx ctx;
+    if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
+    return softmax_mask_rows(ctx, g_tuning, dtype, x, y, rows, (int)cols, scale, causal != 0,
+                             causal ? period : 1, causal ? offset : 0, aligned, nullptr, true);
+}
+
 const char *mb_status_string(mb_status s) {
     switch (s) {
         case MB_OK: return "ok";
@@ -425,7 +446,7 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll) {
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int aligned,
                       int32_t out[7]) {
     if (!out) return MB_ERR_NULL;
-    if (chain < 0 || chain > 7) return MB_ERR_VALUE;
+    if (chain < 0 || chain > 8) return MB_ERR_VALUE;
     if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
     mb_status st = check_rows(rows, cols);
     if (st != MB_OK) return st;
@@ -452,6 +473,9 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
             (int)cols, 0.0f, 0, LnExtras{}, al, &p, false);
     else if (chain == 4)
         st = softmax_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, al, &p, false);
+    else if (chain == 8)
+        st = softmax_mask_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, 1.0f,
+                               true, 1, 0, al, &p, false);
     else if (dtype == MB_F32)
         st = ln_gelu_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                               (int)cols, 0.0f, aligned != 0, &p, false);

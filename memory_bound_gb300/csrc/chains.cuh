@@ -114,7 +114,7 @@ template <typename TT> struct LnGeluChain {
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[2], const PrePC<VEC> &,
-                                               const Args &, float (&v)[VEC]) {
+                                               const Args &, int64_t, int, float (&v)[VEC]) {
         add_inputs<T, VEC>(in[0], in[1], v);
     }
     template <int VEC>
@@ -133,6 +133,8 @@ template <typename TT> struct LnGeluChain {
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    // leading elements of row `row` the chain reads (the staged engines copy no more)
+    __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,
                                                 const PostPC<VEC> &pc, const Args &, int64_t,
@@ -185,7 +187,7 @@ template <typename TT> struct InductorChainT {
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1],
-                                               const PrePC<VEC> &pc, const Args &a,
+                                               const PrePC<VEC> &pc, const Args &a, int64_t, int,
                                                float (&v)[VEC]) {
         if constexpr (VEC == 1) {
             const float t = __fadd_rn(__fmul_rn(in[0].f[0], a.x_scale), pc.bias.f[0]);
@@ -214,6 +216,8 @@ template <typename TT> struct InductorChainT {
     __device__ __forceinline__ static float stat2(float, int, const Args &) { return 0.0f; }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    // leading elements of row `row` the chain reads (the staged engines copy no more)
+    __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float mean, float,
                                                 const PostPC<VEC> &pc, const Args &, int64_t,
@@ -293,7 +297,7 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[kInputs],
-                                               const PrePC<VEC> &, const Args &,
+                                               const PrePC<VEC> &, const Args &, int64_t, int,
                                                float (&v)[VEC]) {
         if constexpr (RES) {
             add_inputs<T, VEC>(in[0], in[1], v);
@@ -334,6 +338,7 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     }
     // full-size outputs per row: out, and h when it is written
     static int outputs(const Args &a) { return a.h ? 2 : 1; }
+    __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     // the row's mean and rstd, written by one thread per row when asked for
     __device__ __forceinline__ static void store_stats(const Args &a, int64_t row, float mean,
                                                        float rstd) {
@@ -372,7 +377,7 @@ template <typename TT> struct SoftmaxChain {
     __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1], const PrePC<VEC> &,
-                                               const Args &, float (&v)[VEC]) {
+                                               const Args &, int64_t, int, float (&v)[VEC]) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) v[e] = in[0].f[e];
     }
@@ -404,6 +409,86 @@ template <typename TT> struct SoftmaxChain {
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    // leading elements of row `row` the chain reads (the staged engines copy no more)
+    __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
+    template <int VEC>
+    __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,
+                                                const PostPC<VEC> &, const Args &, int64_t,
+                                                const Early<VEC> &, float (&o)[VEC]) {
+        if constexpr (VEC == 1) {
+            o[0] = v[0] * inv;
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                const float2 y = mul2(make_float2(v[e], v[e + 1]), splat2(inv));
+                o[e] = y.x;
+                o[e + 1] = y.y;
+            }
+        }
+    }
+};
+
+// Softmax of attention-score rows ("PyTorch operator fusion in practice"
+// (0539edu.com) §4.1-4.2): v = x * scale (one fp32 multiply, the caller's
+// 1/sqrt(d)); with a causal mask, key j of row i takes no part when
+// j > (i mod period) + offset, and its output is 0.  The masked tail of a row
+// is never read: the staged engines copy only the row's first
+// row_extent() elements.
+template <typename TT> struct ScaleMaskSoftmaxChain {
+    using T = TT;
+    static constexpr int kInputs = 1;
+    static constexpr int kVec = Elem<T>::kVec;
+    static constexpr bool kRegCap = false;
+    static constexpr int kRowsTarget = 0;
+    static constexpr bool kTwoPass = true;
+    static constexpr bool kMaxFirst = true;
+    static constexpr bool kStorePre = false;
+    struct Args {
+        const T *in[1];
+        T *out;
+        float scale;
+        int causal;
+        int64_t period;
+        int64_t offset;
+    };
+    template <int VEC> struct PrePC {};
+    template <int VEC> struct PostPC {};
+    static constexpr int kPostPC = 0;
+    template <int VEC> using Early = NoEarly;
+    template <int VEC>
+    __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
+    template <int VEC>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
+    template <int VEC>
+    __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
+    // elements [0, end) of row `row` are unmasked
+    __host__ __device__ static int row_extent(const Args &a, int64_t row, int cols) {
+        if (!a.causal) return cols;
+        const int64_t last = row % a.period + a.offset;
+        return last + 1 < cols ? (int)(last + 1) : cols;
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1], const PrePC<VEC> &,
+                                               const Args &a, int64_t row, int col,
+                                               float (&v)[VEC]) {
+        const int end = row_extent(a, row, 1 << 30);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            v[e] = col + e < end ? __fmul_rn(in[0].f[e], a.scale) : -INFINITY;
+    }
+    template <int VEC>
+    __device__ __forceinline__ static void store_pre(const float (&)[VEC], const Args &, int64_t) {}
+    __device__ __forceinline__ static float stat1(float mx, int, const Args &) { return mx; }
+    template <int VEC>
+    __device__ __forceinline__ static float p2(float (&v)[VEC], float mx) {
+        return SoftmaxChain<T>::template p2<VEC>(v, mx);
+    }
+    __device__ __forceinline__ static float stat2(float sum, int, const Args &) {
+        return 1.0f / sum;
+    }
+    __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
+    static int outputs(const Args &) { return 1; }
+    // y = e * (1 / sum); masked elements hold exp(-inf) = 0
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,
                                                 const PostPC<VEC> &, const Args &, int64_t,

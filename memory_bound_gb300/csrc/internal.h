@@ -108,6 +108,10 @@ MB_LNACT_DECL(lnact_rows_bf16);
 MB_LNACT_DECL(lnact_drop_rows_f32);
 MB_LNACT_DECL(lnact_drop_rows_bf16);
 #undef MB_LNACT_DECL
+mb_status softmax_mask_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
+                            const void *x, void *y, int64_t rows, int cols, float scale,
+                            bool causal, int64_t period, int64_t offset, bool aligned,
+                            RowPlan *plan, bool launch);
 mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
                        const void *x, void *y, int64_t rows, int cols, bool aligned,
                        RowPlan *plan, bool launch);

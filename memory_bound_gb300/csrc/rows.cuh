@@ -117,7 +117,7 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
         float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
-            C::template pre<VEC>(in[k], pre[k], a, v[k]);
+            C::template pre<VEC>(in[k], pre[k], a, row, (lane + 32 * k) * VEC, v[k]);
             l1 = fold1<C, VEC>(l1, v[k], lane + 32 * k < nvec);
             if constexpr (C::kStorePre) {
                 if (lane + 32 * k < nvec) C::template store_pre<VEC>(v[k], a, base + (lane + 32 * k) * VEC);
@@ -192,11 +192,15 @@ __device__ __forceinline__ void rows_cta_body(const typename C::Args &a, int64_t
     auto issue = [&](int s, int64_t li) {
         const int64_t row = first + li * G;
         const uint32_t bar = smem_addr(&bars[s]);
-        mbar_arrive_expect_tx(bar, stage_bytes);
+        // the row's first row_extent() elements, rounded up to 16 bytes
+        // (rows hold a whole number of 16-byte vectors on this path)
+        uint32_t bytes = ((uint32_t)C::row_extent(a, row, cols) * (uint32_t)sizeof(T) + 15u) & ~15u;
+        if (bytes > row_bytes) bytes = row_bytes;
+        mbar_arrive_expect_tx(bar, (uint32_t)NIN * bytes);
 #pragma unroll
         for (int i = 0; i < NIN; ++i)
             bulk_g2s(smem_addr(ring + (size_t)s * stage_bytes + (size_t)i * row_bytes),
-                     a.in[i] + row * cols, row_bytes, bar);
+                     a.in[i] + row * cols, bytes, bar);
     };
     if constexpr (STAGED) {
         if (tid == 0) {
@@ -248,7 +252,7 @@ __device__ __forceinline__ void rows_cta_body(const typename C::Args &a, int64_t
         float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            C::template pre<VEC>(in[k], pre[k], a, v[k]);
+            C::template pre<VEC>(in[k], pre[k], a, row, (tid + k * (int)blockDim.x) * VEC, v[k]);
             l1 = fold1<C, VEC>(l1, v[k], tid + k * (int)blockDim.x < nvec);
             if constexpr (C::kStorePre) {
                 const int vi = tid + k * (int)blockDim.x;
@@ -422,12 +426,18 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     auto issue = [&](int q, int64_t li) {
         const int64_t row = cid + li * nclusters;
         const uint32_t bar = smem_addr(&sbar[q]);
-        mbar_arrive_expect_tx(bar, (uint32_t)NIN * my_bytes);
-        if (my_bytes == 0) return;
+        // this rank's part of the row's first row_extent() elements, rounded
+        // up to whole vectors (16 or 32 bytes) within the slice
+        const int ext = C::row_extent(a, row, cols) - lo;
+        uint32_t bytes = ext <= 0 ? 0u
+                       : ((uint32_t)((ext + VEC - 1) / VEC) * VEC) * (uint32_t)sizeof(T);
+        if (bytes > my_bytes) bytes = my_bytes;
+        mbar_arrive_expect_tx(bar, (uint32_t)NIN * bytes);
+        if (bytes == 0) return;
 #pragma unroll
         for (int i = 0; i < NIN; ++i)
             bulk_g2s(smem_addr(ring + (size_t)q * stage_bytes + (size_t)i * pitch),
-                     a.in[i] + row * cols + lo, my_bytes, bar);
+                     a.in[i] + row * cols + lo, bytes, bar);
     };
     if constexpr (STAGED) {
         if (tid == 0) {
@@ -498,7 +508,7 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vi = tid + k * (int)blockDim.x;
-            C::template pre<VEC>(in[k], pre[k], a, v[k]);
+            C::template pre<VEC>(in[k], pre[k], a, row, lo + vi * VEC, v[k]);
             l1 = fold1<C, VEC>(l1, v[k], vi < nvec);
             if constexpr (C::kStorePre) {
                 if (vi < nvec) C::template store_pre<VEC>(v[k], a, base + vi * VEC);

@@ -11,8 +11,9 @@ Shapes and distributions are the pages' example workloads:
   hidden 8192 bf16;
 * for the further chains (NEXT): row softmax on [P1] §4.1's attention-score
   matrix, the LayerNorm family with a residual-stream output or a ReLU, the
-  TorchInductor chain in bf16, [P2] §2.1's LayerNorm -> ReLU -> Dropout, and
-  the pointwise chain with per-column b1 / b2.
+  TorchInductor chain in bf16, [P2] §2.1's LayerNorm -> ReLU -> Dropout, the
+  pointwise chain with per-column b1 / b2, and [P1] §4.1-4.2's score matrix
+  scaled and causally masked.
 
 N(mu, s) takes ``s`` as the standard deviation.  Tensor ids are assigned in
 the order each workload lists its tensors.
@@ -38,7 +39,7 @@ class Tensor:
 class Workload:
     name: str
     chain: str         # "add_relu_scale" | "add_relu_scale_bcast" | "inductor" |
-    #                    "ln_gelu" | "lnact" | "softmax"
+    #                    "ln_gelu" | "lnact" | "softmax" | "softmax_mask"
     dtype: str         # "f32" | "bf16"
     rows: int          # 1 for the pointwise chain
     cols: int          # n for the pointwise chain
@@ -59,9 +60,15 @@ class Workload:
 
     def ideal_bytes(self, rows=None):
         """Read-once / write-once bytes of one call (optionally for a prefix
-        of ``rows`` rows)."""
+        of ``rows`` rows).  A causally masked softmax reads only the unmasked
+        keys of each row and writes every output."""
         rows = self.rows if rows is None else rows
         eb = self.elem_bytes
+        if self.params.get("causal"):
+            per, off = self.params["period"], self.params["offset"]
+            i = np.arange(rows, dtype=np.int64)
+            read = int(np.minimum(self.cols, i % per + off + 1).sum())
+            return (read + rows * self.cols) * eb
         full = sum(1 for t in self.tensors if not t.per_column)
         percol = sum(1 for t in self.tensors if t.per_column)
         outs = 2 if self.params.get("write_h") else 1
@@ -146,8 +153,14 @@ POINTWISE_BCAST_F32 = Workload("pointwise_bcast_f32_4096x1024", "add_relu_scale_
                                    Tensor("b1", 1, "normal", 0.0, 1.0, True),
                                    Tensor("b2", 2, "normal", 0.0, 1.0, True),
                                ), {"scale": 0.5})
+# The same score matrix as an attention layer's softmax sees it (§4.1-4.2 of
+# the same page): scaled by 1/sqrt(64) and causally masked, 4096 queries per
+# head, keys aligned to the queries (offset 0).
+SOFTMAX_CAUSAL_F32 = Workload("softmax_scale_causal_f32_131072x4096", "softmax_mask", "f32",
+                              32 * 4096, 4096, 11, SOFTMAX_F32.tensors,
+                              {"scale": 0.125, "causal": True, "period": 4096, "offset": 0})
 NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16, LNACT_RELU_DROP_F32,
-        POINTWISE_BCAST_F32)
+        POINTWISE_BCAST_F32, SOFTMAX_CAUSAL_F32)
 
 ALL = (POINTWISE_TINY, POINTWISE_4M, INDUCTOR_1024, LN_F32, LN_BF16)
 BY_NAME = {w.name: w for w in ALL + NEXT}

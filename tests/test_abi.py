@@ -170,7 +170,7 @@ def test_layernorm_ex_argument_checks(lib):
     assert f(A, B, C, D, E, F, None, F + 64, 4, 64, 1e-5, 1, 0.0, 1, 0, 0, None) == MB_ERR_OVERLAP
     assert f(A, B, C, D, E, None, None, None, 4, 64, 1e-5, 7, 0.1, 1, 0, 0, None) == MB_ERR_VALUE
     assert f(None, B, C, D, E, None, F, G, 4, 64, 1e-5, 1, 0.1, 1, 0, 0, None) == MB_ERR_NULL
-    assert lib.mb_row_plan(8, 0, 4, 64, 1, (ctypes.c_int32 * 7)()) == MB_ERR_VALUE
+    assert lib.mb_row_plan(9, 0, 4, 64, 1, (ctypes.c_int32 * 7)()) == MB_ERR_VALUE
 
 
 def test_pointwise_bcast_argument_checks(lib):
@@ -187,3 +187,16 @@ def test_pointwise_bcast_argument_checks(lib):
     assert f(A, B, C, A + 64, 4, 64, 1, 1, 0.5, 0, None) == MB_ERR_OVERLAP
     # a per-column b1 occupies cols elements only; a full one rows * cols
     assert f(A, D + 4 * 64, C, D, 4, 64, 0, 1, 0.5, 0, None) == MB_ERR_OVERLAP
+
+
+def test_scale_mask_softmax_argument_checks(lib):
+    f = lib.fused_scale_mask_softmax
+    assert f(A, B, 0, 64, 0.125, 1, 4, 0, 0, None) == MB_OK
+    assert f(A, B, 4, 64, float("nan"), 1, 4, 0, 0, None) == MB_ERR_VALUE
+    assert f(A, B, 4, 64, 0.125, 2, 4, 0, 0, None) == MB_ERR_VALUE
+    assert f(A, B, 4, 64, 0.125, 1, 0, 0, 0, None) == MB_ERR_VALUE      # period
+    assert f(A, B, 4, 64, 0.125, 1, 4, -1, 0, None) == MB_ERR_VALUE     # offset
+    assert f(A, A + 64, 4, 64, 0.125, 1, 4, 0, 0, None) == MB_ERR_OVERLAP
+    assert f(A + 2, B, 4, 64, 0.125, 0, 1, 0, 0, None) == MB_ERR_ALIGN
+    assert f(A, None, 4, 64, 0.125, 0, 1, 0, 1, None) == MB_ERR_NULL
+    assert f(A, B, 4, 0, 0.125, 0, 1, 0, 0, None) == MB_ERR_SHAPE

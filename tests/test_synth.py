@@ -97,5 +97,7 @@ def test_workload_ideal_bytes(w):
         "inductor_bf16_1024x1024": 2 * 1024 * 1024 * 2 + 3 * 1024 * 2,
         "lnact_relu_dropout_f32_8192x4096": 2 * 8192 * 4096 * 4 + 2 * 4096 * 4,
         "pointwise_bcast_f32_4096x1024": 2 * 4096 * 1024 * 4 + 2 * 1024 * 4,
+        # 32 heads x (1 + 2 + ... + 4096) unmasked keys read, every output written
+        "softmax_scale_causal_f32_131072x4096": (32 * 4096 * 4097 // 2 + 131072 * 4096) * 4,
     }[w.name]
     assert w.ideal_bytes() == want
