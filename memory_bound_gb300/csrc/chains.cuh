@@ -449,7 +449,8 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
         float scale;
         int causal;
         int64_t period;
-        int64_t offset;
+        int64_t offset;    // at most cols (larger masks nothing more)
+        uint64_t recip;    // (2^64 - 1) / period, for row mod period on the device
     };
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC {};
@@ -461,10 +462,23 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
     template <int VEC>
     __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
+    // row mod period: on the device a multiply-high by the reciprocal gives
+    // the quotient or one less (the reciprocal is rounded down and the row is
+    // below 2^63), so one conditional subtraction finishes it
+    __host__ __device__ static int64_t query_of(const Args &a, int64_t row) {
+#ifdef __CUDA_ARCH__
+        const uint64_t q = __umul64hi((uint64_t)row, a.recip);
+        uint64_t r = (uint64_t)row - q * (uint64_t)a.period;
+        if (r >= (uint64_t)a.period) r -= (uint64_t)a.period;
+        return (int64_t)r;
+#else
+        return row % a.period;
+#endif
+    }
     // elements [0, end) of row `row` are unmasked
     __host__ __device__ static int row_extent(const Args &a, int64_t row, int cols) {
         if (!a.causal) return cols;
-        const int64_t last = row % a.period + a.offset;
+        const int64_t last = query_of(a, row) + a.offset;
         return last + 1 < cols ? (int)(last + 1) : cols;
     }
     template <int VEC>
