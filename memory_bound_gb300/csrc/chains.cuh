@@ -121,15 +121,17 @@ template <typename TT> struct LnGeluChain {
     __device__ __forceinline__ static void store_pre(const float (&)[VEC], const Args &, int64_t) {}
     // mean = sum(v) / H; second pass: v <- v - mean, summing the squares;
     // rstd = 1/sqrt(var + eps)
+    // mean = sum * (1 / H): the reciprocal is loop-invariant, so the compiler
+    // takes it once per kernel, not once per row (exact for H a power of 2)
     __device__ __forceinline__ static float stat1(float sum, int cols, const Args &) {
-        return sum / (float)cols;
+        return sum * (1.0f / (float)cols);
     }
     template <int VEC>
     __device__ __forceinline__ static float p2(float (&v)[VEC], float mean) {
         return center_sumsq<VEC>(v, mean);
     }
     __device__ __forceinline__ static float stat2(float m2, int cols, const Args &a) {
-        return rsqrtf(m2 / (float)cols + a.eps);
+        return rsqrtf(m2 * (1.0f / (float)cols) + a.eps);
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
@@ -316,15 +318,17 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
             f.store_stream(a.h + off);
         }
     }
+    // mean = sum * (1 / H): the reciprocal is loop-invariant, so the compiler
+    // takes it once per kernel, not once per row (exact for H a power of 2)
     __device__ __forceinline__ static float stat1(float sum, int cols, const Args &) {
-        return sum / (float)cols;
+        return sum * (1.0f / (float)cols);
     }
     template <int VEC>
     __device__ __forceinline__ static float p2(float (&v)[VEC], float mean) {
         return center_sumsq<VEC>(v, mean);
     }
     __device__ __forceinline__ static float stat2(float m2, int cols, const Args &a) {
-        return rsqrtf(m2 / (float)cols + a.eps);
+        return rsqrtf(m2 * (1.0f / (float)cols) + a.eps);
     }
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float rstd,

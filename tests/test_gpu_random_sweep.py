@@ -12,7 +12,8 @@ import memory_bound_gb300 as mb
 import oracle
 import synth
 
-from gpu_util import assert_bitexact, assert_close, bf16_to_f64, to_dev, to_host
+from gpu_util import assert_bitexact, assert_close, bf16_to_f64, to_dev
+from gpu_util import to_host as _to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +48,14 @@ def gpu():
     mb.set_row_path("auto")
     torch.cuda.synchronize()
     assert mb.device_error() == 0
+
+
+def to_host(t):
+    """Outputs in pinned host memory are written asynchronously by the
+    kernels: synchronise before reading them (a device tensor's copy to the
+    host synchronises by itself)."""
+    torch.cuda.synchronize()
+    return _to_host(t)
 
 
 def _place(a, bf16, offset_view, host):
