@@ -807,7 +807,8 @@ def run_ours(args):
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32+bf16", "data": "synthetic (seeded SplitMix64/Box-Muller)",
+            "dtype": "f32", "io_dtypes": ["f32", "bf16"],
+            "data": "synthetic (seeded SplitMix64/Box-Muller)",
             "config": {"workload": WORKLOAD,
                        "l2": f"inputs larger than L2: each chain cycles through buffer copies "
                              f"totalling >= 2x the {l2_bytes >> 20} MiB L2",
@@ -877,7 +878,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * statistics.mean(secs), 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16 (oracle: fp32 / fp64)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "dtype_note": "the oracle: fp32 op by op for the pointwise steps, "
+                                                "double for the statistics and the transcendentals",
             "data": "synthetic (seeded SplitMix64/Box-Muller)",
             "config": {"workload": WORKLOAD,
                        "sample": f"{fraction:.4f} of each workload per step"},
