@@ -138,7 +138,8 @@ def _stream_handle(dev):
 
 def _empty_like(x):
     """An output like x: on x's device, or in pinned host memory when x is
-    there (the kernels then write it over the host link)."""
+    there (the kernels then write it over the host link, asynchronously:
+    synchronise the stream before reading it on the host)."""
     torch = _torch()
     if x.is_cuda:
         return torch.empty_like(x)
