@@ -394,8 +394,9 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * GeLU, 1 the TorchInductor chain, 2 the LayerNorm family with a residual,
  * 3 without, 4 row softmax, 5 and 6 the LayerNorm family with dropout (with
  * a residual, without), 7 the LayerNorm family with a residual that also
- * writes the residual stream h, 8 the scaled, causally masked softmax.  `aligned` says whether every pointer is 16-byte
- * aligned.  Queries the current device (SM count, shared memory).
+ * writes the residual stream h, 8 the scaled softmax under a square causal
+ * mask (period = cols, offset 0: row i reads keys 0 .. i mod cols).
+ * `aligned` says whether every pointer is 16-byte aligned.  Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,
                       int aligned, int32_t out[7]);

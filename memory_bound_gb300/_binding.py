@@ -388,7 +388,8 @@ def row_plan(chain, dtype, rows, cols, aligned=True):
     """The launch a row chain would use: dict(path, threads, ctas, vpt, vec,
     stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact", "softmax",
     "lnact_res_dropout", "lnact_dropout", "lnact_res_h" (with the
-    residual-stream output) or "softmax_mask"; dtype: "f32" or "bf16"."""
+    residual-stream output) or "softmax_mask" (the scaled softmax under a square
+    causal mask: period = cols, offset 0); dtype: "f32" or "bf16"."""
     out = (ctypes.c_int32 * 7)()
     code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4,
             "lnact_res_dropout": 5, "lnact_dropout": 6, "lnact_res_h": 7,

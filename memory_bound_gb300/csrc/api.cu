@@ -475,7 +475,7 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
         st = softmax_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, al, &p, false);
     else if (chain == 8)
         st = softmax_mask_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, 1.0f,
-                               true, 1, 0, al, &p, false);
+                               true, cols, 0, al, &p, false);
     else if (dtype == MB_F32)
         st = ln_gelu_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                               (int)cols, 0.0f, aligned != 0, &p, false);

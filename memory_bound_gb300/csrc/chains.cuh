@@ -135,6 +135,7 @@ template <typename TT> struct LnGeluChain {
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    static int read_percent(const Args &, int64_t, int) { return 100; }
     // leading elements of row `row` the chain reads (the staged engines copy no more)
     __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     template <int VEC>
@@ -218,6 +219,7 @@ template <typename TT> struct InductorChainT {
     __device__ __forceinline__ static float stat2(float, int, const Args &) { return 0.0f; }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    static int read_percent(const Args &, int64_t, int) { return 100; }
     // leading elements of row `row` the chain reads (the staged engines copy no more)
     __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     template <int VEC>
@@ -342,6 +344,7 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     }
     // full-size outputs per row: out, and h when it is written
     static int outputs(const Args &a) { return a.h ? 2 : 1; }
+    static int read_percent(const Args &, int64_t, int) { return 100; }
     __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     // the row's mean and rstd, written by one thread per row when asked for
     __device__ __forceinline__ static void store_stats(const Args &a, int64_t row, float mean,
@@ -413,6 +416,7 @@ template <typename TT> struct SoftmaxChain {
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    static int read_percent(const Args &, int64_t, int) { return 100; }
     // leading elements of row `row` the chain reads (the staged engines copy no more)
     __host__ __device__ static int row_extent(const Args &, int64_t, int cols) { return cols; }
     template <int VEC>
@@ -506,6 +510,21 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     }
     __device__ __forceinline__ static void store_stats(const Args &, int64_t, float, float) {}
     static int outputs(const Args &) { return 1; }
+    // The share of the row read on average (the staged engines copy the
+    // unmasked prefix only): the mean of min(q + offset + 1, cols) over the
+    // query positions q = row mod period that the rows take, as a percent of
+    // cols.
+    static int read_percent(const Args &a, int64_t rows, int cols) {
+        if (!a.causal || cols <= 0) return 100;
+        const int64_t P = rows < a.period ? (rows > 0 ? rows : 1) : a.period;
+        int64_t k = (int64_t)cols - a.offset - 1;     // positions whose prefix is shorter
+        if (k < 0) k = 0;
+        if (k > P) k = P;
+        const double read = (double)k * (double)(k - 1) / 2.0 + (double)k * (double)(a.offset + 1) +
+                            (double)(P - k) * (double)cols;
+        const int pct = (int)(100.0 * read / ((double)P * (double)cols) + 0.5);
+        return pct < 1 ? 1 : (pct > 100 ? 100 : pct);
+    }
     // y = e * (1 / sum); masked elements hold exp(-inf) = 0
     template <int VEC>
     __device__ __forceinline__ static void post(const float (&v)[VEC], float, float inv,

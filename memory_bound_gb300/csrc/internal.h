@@ -41,6 +41,8 @@ struct RowTuning {
                            // bulk-async copies (the STAGED path) are planned
     int outs = 1;          // full-size outputs written per row (2 with the
                            // LayerNorm family's residual-stream output)
+    int read_pct = 100;    // share of each row's input elements read, on
+                           // average over the rows (percent, 1..100)
 };
 
 // Process-wide pointwise override (mb_set_pointwise_shape).

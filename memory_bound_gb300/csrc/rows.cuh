@@ -47,13 +47,15 @@ constexpr int kCtaMaxThreads = 1024;
 constexpr int kWarpBlock = 256;
 constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
-constexpr int kRowsInFlight = 4;  // resident CTAs per SM that the planner aims for
+constexpr int kMaxRowsInFlight = 8;  // resident CTAs per SM the planner aims for, at most
 constexpr int kCappedRegs = 40;   // registers per thread of rows_cta_kernel_capped
-// Bytes of row reads and writes per SM in flight beyond which more resident
-// rows stop paying (sweeps on GB300: LayerNorm rows of 48 KB in + out run
-// fastest three to an SM in fp32, four in bf16, whose rows carry twice the
-// arithmetic per byte; 64 KB bf16 rows three to an SM).
-constexpr int64_t kFlightBytesF32 = 160 * 1024;
+// Bytes of row reads and writes per SM in flight that keep HBM busy; the
+// planner aims for this many bytes' worth of resident rows, rounded to the
+// nearest row count (sweeps on GB300, fp32: LayerNorm rows of 48 KB in + out
+// fastest three to an SM, softmax rows of 32 KB four, causal score rows of
+// 24 KB read + written five; bf16, whose rows carry twice the arithmetic per
+// byte: LayerNorm rows of 48 KB four, 16 KB softmax rows eight).
+constexpr int64_t kFlightBytesF32 = 128 * 1024;
 constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
 constexpr int kClusterElems = 16; // values per thread the cluster planner prefers
@@ -827,7 +829,7 @@ template <class C> struct RowEngine {
     // only sizes the grid for its rows.
     struct CacheEntry {
         bool used;
-        int device, cols, aligned, path, ctas_per_sm, stages, vpt, no_bulk, outs;
+        int device, cols, aligned, path, ctas_per_sm, stages, vpt, no_bulk, outs, read_pct;
         RowPlan core;
         const void *fn;
     };
@@ -854,7 +856,7 @@ template <class C> struct RowEngine {
                 if (e.used && e.device == ctx.device && e.cols == cols && e.aligned == (int)aligned &&
                     e.path == tun.path && e.ctas_per_sm == tun.ctas_per_sm &&
                     e.stages == tun.stages && e.vpt == tun.vpt && e.no_bulk == tun.no_bulk &&
-                    e.outs == tun.outs) {
+                    e.outs == tun.outs && e.read_pct == tun.read_pct) {
                     core = e.core;
                     f = e.fn;
                     hit = true;
@@ -868,7 +870,7 @@ template <class C> struct RowEngine {
             std::lock_guard<std::mutex> lock(pc.mu);
             pc.entries[pc.next] = CacheEntry{true, ctx.device, cols, (int)aligned, tun.path,
                                              tun.ctas_per_sm, tun.stages, tun.vpt, tun.no_bulk,
-                                             tun.outs, core, f};
+                                             tun.outs, tun.read_pct, core, f};
             pc.next = (pc.next + 1) % kCacheSize;
         }
         *p = core;
@@ -945,18 +947,25 @@ template <class C> struct RowEngine {
 
         // CTA engine.  Each resident CTA keeps one row in flight, so pick the
         // vectors-per-thread that lets the most CTAs share an SM, counting up
-        // to kRowsInFlight (measured on GB300: four rows per SM keep HBM busy),
-        // or fewer for heavy rows (the byte budget above, never below two),
-        // then the most threads per SM; one ring stage counted for the staged
-        // path.
+        // to a target, then the most threads per SM; one ring stage counted
+        // for the staged path.  The target is the per-SM byte budget over one
+        // row's reads and writes (on the staged path reads count over the
+        // share of the row the chain reads: a causal score row's copy holds
+        // its unmasked prefix only),
+        // rounded to the nearest row count between 2 and kMaxRowsInFlight,
+        // unless the chain sets its own; the grid holds no more resident CTAs
+        // than the target.
         const bool staged = path == MB_ROW_STAGED;
         const int smem1 = kHdrBytes + (staged ? stage_bytes : 0);
-        const int64_t row_io = (int64_t)(C::kInputs + tun.outs) * cols * (int64_t)sizeof(T);
+        const int64_t row_io =
+            ((int64_t)C::kInputs * cols * (staged ? tun.read_pct : 100) / 100 +
+             (int64_t)tun.outs * cols) *
+            (int64_t)sizeof(T);
         const int64_t budget = sizeof(T) == 2 ? kFlightBytesBf16 : kFlightBytesF32;
-        int target = (int)(budget / row_io < kRowsInFlight ? budget / row_io : kRowsInFlight);
-        if (target < 2) target = 2;
+        int64_t want_rows = row_io > 0 ? (budget + row_io / 2) / row_io : kMaxRowsInFlight;
+        if (want_rows > kMaxRowsInFlight) want_rows = kMaxRowsInFlight;
+        int target = want_rows < 2 ? 2 : (int)want_rows;
         if (C::kRowsTarget > 0) target = C::kRowsTarget;     // the chain's own measured target
-        const bool heavy = target < kRowsInFlight;      // the budget binds
         int best_vpt = 0, best_occ = 0, best_threads = 0;
         for (int cand = 1; cand <= max_vpt(vec); cand *= 2) {
             if (tun.vpt > 0 && cand != tun.vpt) continue;
@@ -971,16 +980,15 @@ template <class C> struct RowEngine {
             if (occ < 1) continue;
             const int rows_in_flight = occ < target ? occ : target;
             const int best_rows = best_occ < target ? best_occ : target;
-            // tie-break on threads per SM, counting only the CTAs that will
-            // be resident when the budget caps them
-            const int tie = heavy ? rows_in_flight : occ;
-            const int best_tie = heavy ? best_rows : best_occ;
+            // tie-break on threads per SM, counting the CTAs that will be
+            // resident once the target caps them
             if (rows_in_flight > best_rows ||
-                (rows_in_flight == best_rows && tie * threads > best_tie * best_threads)) {
+                (rows_in_flight == best_rows &&
+                 rows_in_flight * threads > best_rows * best_threads)) {
                 best_vpt = cand; best_occ = occ; best_threads = threads;
             }
         }
-        if (heavy && tun.ctas_per_sm <= 0 && best_occ > target) best_occ = target;
+        if (tun.ctas_per_sm <= 0 && best_occ > target) best_occ = target;
         if (!best_vpt && tun.vpt > 0) {
             RowTuning t2 = tun;
             t2.vpt = 0;
@@ -1030,6 +1038,7 @@ template <class C> struct RowEngine {
         const void *fn = nullptr;
         RowTuning tn = tun;      // the per-call planning inputs
         if (C::outputs(a) > tn.outs) tn.outs = C::outputs(a);
+        tn.read_pct = C::read_percent(a, rows, cols);
         mb_status st = plan(ctx, tn, rows, cols, aligned, &p, &fn);
         if (st != MB_OK) return st;
         if (launch && (p.path == MB_ROW_STAGED || (p.path == MB_ROW_CLUSTER && p.ring > 0))) {
