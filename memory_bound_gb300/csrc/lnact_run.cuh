@@ -39,6 +39,7 @@ mb_status lnact_run(const LaunchCtx &ctx, const RowTuning &tun, bool residual, c
         a.out = static_cast<T *>(out);
         a.h = static_cast<T *>(h);
         a.eps = eps;
+        a.inv_cols = 1.0f / (float)cols;
         a.act = act;
         a.mean_out = ex.mean;
         a.rstd_out = ex.rstd;

@@ -44,6 +44,7 @@
 namespace mb {
 
 constexpr int kCtaMaxThreads = 1024;
+constexpr int kWideThreads = 512;  // CTA bound of the cluster kernels holding 32+ values per thread
 constexpr int kWarpBlock = 256;
 constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
@@ -58,7 +59,6 @@ constexpr int kCappedRegs = 40;   // registers per thread of rows_cta_kernel_cap
 constexpr int64_t kFlightBytesF32 = 128 * 1024;
 constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
-constexpr int kClusterElems = 16; // values per thread the cluster planner prefers
 constexpr int kClusterRing = 1;   // staging ring depth on the cluster path
 constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
@@ -380,8 +380,12 @@ __device__ __forceinline__ float cluster_reduce(float v, float *xch, uint64_t *b
 // The two statistics combine CTA partials through distributed shared memory
 // (cluster_reduce).  Every wait is bounded; a timeout ends the CTA's row loop
 // (after its copies in flight have landed) and is reported in `err`.
-template <class C, int VPT, int VEC, bool STAGED>
-__global__ void __launch_bounds__(kCtaMaxThreads, 1)
+// MAXT bounds the CTA size: launches of 32 or more values per thread on at
+// most kWideThreads threads take the kWideThreads form, whose threads may hold
+// up to 128 registers (the slice, the next row's prefetch and the per-column
+// values), where under the 64 of the 1024-thread form they spill.
+template <class C, int VPT, int VEC, bool STAGED, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1)
 rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *err,
                     int nstage) {
     namespace cg = cooperative_groups;
@@ -670,33 +674,43 @@ template <class C> struct RowEngine {
         return nullptr;
     }
 
-    static const void *cluster_fn(int vpt, bool vec, bool staged) {
+    // The cluster kernel for a launch of `threads` threads: the 512-thread
+    // form for 32 or more values per thread when the CTA fits it, else the
+    // 1024-thread form.
+    template <int VPT, int VEC, bool STAGED> static const void *cluster_kernel(int threads) {
+        if constexpr (VPT * VEC >= 32) {
+            if (threads <= kWideThreads)
+                return (const void *)rows_cluster_kernel<C, VPT, VEC, STAGED, kWideThreads>;
+        }
+        return (const void *)rows_cluster_kernel<C, VPT, VEC, STAGED, kCtaMaxThreads>;
+    }
+    static const void *cluster_fn(int vpt, bool vec, bool staged, int threads) {
         if (vec) {
             if (staged) {
                 switch (vpt) {
-                    case 1: return (const void *)rows_cluster_kernel<C, 1, kVecN, true>;
-                    case 2: return (const void *)rows_cluster_kernel<C, 2, kVecN, true>;
-                    case 4: return (const void *)rows_cluster_kernel<C, 4, kVecN, true>;
-                    case 8: if constexpr (kVecN == 4) return (const void *)rows_cluster_kernel<C, 8, kVecN, true>;
+                    case 1: return cluster_kernel<1, kVecN, true>(threads);
+                    case 2: return cluster_kernel<2, kVecN, true>(threads);
+                    case 4: return cluster_kernel<4, kVecN, true>(threads);
+                    case 8: if constexpr (kVecN == 4) return cluster_kernel<8, kVecN, true>(threads);
                             break;
                 }
             } else {
                 switch (vpt) {
-                    case 1: return (const void *)rows_cluster_kernel<C, 1, kVecN, false>;
-                    case 2: return (const void *)rows_cluster_kernel<C, 2, kVecN, false>;
-                    case 4: return (const void *)rows_cluster_kernel<C, 4, kVecN, false>;
-                    case 8: if constexpr (kVecN == 4) return (const void *)rows_cluster_kernel<C, 8, kVecN, false>;
+                    case 1: return cluster_kernel<1, kVecN, false>(threads);
+                    case 2: return cluster_kernel<2, kVecN, false>(threads);
+                    case 4: return cluster_kernel<4, kVecN, false>(threads);
+                    case 8: if constexpr (kVecN == 4) return cluster_kernel<8, kVecN, false>(threads);
                             break;
                 }
             }
         } else if (!staged) {
             switch (vpt) {
-                case 1: return (const void *)rows_cluster_kernel<C, 1, 1, false>;
-                case 2: return (const void *)rows_cluster_kernel<C, 2, 1, false>;
-                case 4: return (const void *)rows_cluster_kernel<C, 4, 1, false>;
-                case 8: return (const void *)rows_cluster_kernel<C, 8, 1, false>;
-                case 16: return (const void *)rows_cluster_kernel<C, 16, 1, false>;
-                case 32: return (const void *)rows_cluster_kernel<C, 32, 1, false>;
+                case 1: return cluster_kernel<1, 1, false>(threads);
+                case 2: return cluster_kernel<2, 1, false>(threads);
+                case 4: return cluster_kernel<4, 1, false>(threads);
+                case 8: return cluster_kernel<8, 1, false>(threads);
+                case 16: return cluster_kernel<16, 1, false>(threads);
+                case 32: return cluster_kernel<32, 1, false>(threads);
             }
         }
         return nullptr;
@@ -732,17 +746,16 @@ template <class C> struct RowEngine {
     // One cluster of `cs` CTAs per row.  Each resident cluster keeps one row
     // in flight, so among cluster sizes 2, 4, 8, 16 (or the requested one) and
     // the vectors-per-thread that fit a slice in one CTA, take the launch with
-    // the most resident clusters (ties: the smaller cluster); no rank is empty.
-    // Launches holding at most kClusterElems values per thread come first: a
-    // thread keeps its slice and the next row's prefetch in registers, and
-    // more than that spills (sweeps on GB300: 16 values per thread ran LN fp32
-    // at 65536 columns at 6.1 TB/s, 32 at 3.9).
+    // the most resident clusters (ties: the smaller cluster, then the more
+    // values per thread); no rank is empty.  Launches holding at most the
+    // chain's C::kClusterVals values per thread come first: a thread keeps
+    // its slice and the next row's prefetch in registers.
     static mb_status plan_cluster(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows,
                                   int nvec, bool vec, RowPlan *p, const void **fn) {
         const int VEC = vec ? kVecN : 1;
         for (int pass = 0; pass < 2; ++pass) {
             mb_status st = plan_cluster_pass(ctx, tun, rows, nvec, vec,
-                                             pass == 0 ? kClusterElems / VEC : 1 << 30, p, fn);
+                                             pass == 0 ? C::kClusterVals / VEC : 1 << 30, p, fn);
             if (st != MB_ERR_SHAPE) return st;
         }
         return MB_ERR_SHAPE;
@@ -784,14 +797,26 @@ template <class C> struct RowEngine {
             for (int vpt = 1; vpt <= max_vpt(vec); vpt *= 2) {
                 if (tun.vpt > 0 && vpt != tun.vpt) continue;
                 if (tun.vpt <= 0 && vpt > max_vpt_regs) continue;
+                // the first pass leaves out the 1024-thread form of the
+                // 32-value kernels (it spills); the second takes it when
+                // nothing else fits (fp32 rows of 524288)
+                if (tun.vpt <= 0 && max_vpt_regs < (1 << 30) && vpt * VEC >= 32 &&
+                    ceil_div(slice_v, vpt) > kWideThreads)
+                    continue;
                 if (ceil_div(slice_v, vpt) > kCtaMaxThreads) continue;
                 const int threads = round_up32(ceil_div(slice_v, vpt));
-                const void *f = cluster_fn(vpt, vec, ring > 0);
+                const void *f = cluster_fn(vpt, vec, ring > 0, threads);
                 if (!f) continue;
+                cudaFuncAttributes fa;
+                const cudaError_t fe = cudaFuncGetAttributes(&fa, f);
+                if (fe != cudaSuccess) return cuda_fail(fe);
+                if (threads > fa.maxThreadsPerBlock) continue;    // the kernel's launch bound
                 int n = 0;
                 mb_status st = active_clusters(ctx, f, cs, threads, smem, &n);
                 if (st != MB_OK) return st;
-                if (n > best_n) {   // ties keep the smaller cluster (fewer exchange partners)
+                // ties keep the smaller cluster (fewer exchange partners), and
+                // within it the more values per thread (fewer, busier threads)
+                if (n > best_n || (n > 0 && n == best_n && cs == best_cs)) {
                     best_n = n; best_cs = cs; best_vpt = vpt; best_threads = threads;
                     best_slice = slice_v; best_ring = ring; best_smem = smem;
                 }
@@ -803,7 +828,7 @@ template <class C> struct RowEngine {
             return plan_cluster(ctx, t2, rows, nvec, vec, p, fn);
         }
         if (!best_n) return MB_ERR_SHAPE;       // the caller tries the next pass
-        *fn = cluster_fn(best_vpt, vec, best_ring > 0);
+        *fn = cluster_fn(best_vpt, vec, best_ring > 0, best_threads);
         const int64_t ncl = rows < best_n ? rows : best_n;
         p->path = MB_ROW_CLUSTER; p->threads = best_threads; p->vpt = best_vpt;
         p->stages = best_cs; p->smem = best_smem;

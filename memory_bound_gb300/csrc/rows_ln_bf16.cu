@@ -10,7 +10,7 @@ mb_status ln_gelu_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const vo
     using C = LnGeluChain<uint16_t>;
     C::Args a{{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(r)},
               static_cast<const uint16_t *>(w), static_cast<const uint16_t *>(b),
-              static_cast<uint16_t *>(out), eps};
+              static_cast<uint16_t *>(out), eps, 1.0f / (float)cols};
     return RowEngine<C>::run(ctx, tun, a, rows, cols, aligned, plan, launch);
 }
 

@@ -10,7 +10,7 @@ mb_status ln_gelu_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const voi
     using C = LnGeluChain<float>;
     C::Args a{{static_cast<const float *>(x), static_cast<const float *>(r)},
               static_cast<const float *>(w), static_cast<const float *>(b),
-              static_cast<float *>(out), eps};
+              static_cast<float *>(out), eps, 1.0f / (float)cols};
     return RowEngine<C>::run(ctx, tun, a, rows, cols, aligned, plan, launch);
 }
 
