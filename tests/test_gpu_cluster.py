@@ -85,6 +85,21 @@ def test_forced_cluster_sizes(cs, shape, row_path):
     _check_chains(rows, cols, 4000 + cs * 31 + cols, False)
 
 
+@pytest.mark.parametrize("ring", [0, 1], ids=["direct", "staged"])
+@pytest.mark.parametrize("cs", [2, 4])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_32_value_kernel_forms(cs, ring, bf16, row_path):
+    """32 values per thread on 65536 columns: four CTAs of 512 threads take
+    the kernel form bounded at 512 threads (up to 128 registers), two CTAs
+    of 1024 threads the 1024-thread form; directly loaded and staged."""
+    vpt = 4 if bf16 else 8
+    row_path("cluster", ring, cs, vpt)
+    p = mb.row_plan("ln", "bf16" if bf16 else "f32", 5, 65536)
+    assert p["path"] == "cluster" and p["vpt"] == vpt and p["stages"] == cs
+    assert p["threads"] == 65536 // cs // 32
+    _check_chains(5, 65536, 7000 + 10 * cs + ring, bf16)
+
+
 def test_long_rows_many_rows_and_unaligned():
     """More rows than clusters fit at once (each cluster loops over rows), and
     an unaligned scalar row length."""
