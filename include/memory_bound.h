@@ -346,18 +346,20 @@ typedef enum mb_row_path {
     MB_ROW_STAGED = 3,   /* one CTA per row, rows staged into shared memory by
                             bulk async copies in a multi-stage ring            */
     MB_ROW_CLUSTER = 4   /* one thread-block cluster per row: each CTA holds a
-                            slice (staged by bulk async copies when the rows
-                            are vectorised device memory), statistics combined
-                            through distributed shared memory (automatic above
-                            32768 elements)                                    */
+                            slice in registers (bf16 rows in vectorised device
+                            memory staged by bulk async copies, fp32 rows
+                            loaded directly unless a ring depth is asked for),
+                            statistics combined through distributed shared
+                            memory (automatic above 32768 elements)            */
 } mb_row_path;
 
 /*
  * Process-wide override of the row-chain path and launch shape, for tuning
  * and testing.  ctas_per_sm (CTAs resident per SM; the staging ring depth on
  * the cluster path), stages (ring depth of the staged path; CTAs per row,
- * 2..16, on the cluster path) and vec_per_thread (vector slots each thread holds per row
- * on the CTA paths; a power of two) of 0 mean "choose automatically"; a
+ * 2..16, on the cluster path) and vec_per_thread (vector slots each thread
+ * holds per row on the CTA and cluster paths; a power of two) of 0 mean
+ * "choose automatically"; a
  * value that cannot serve a shape is ignored.  A forced path that cannot
  * serve a shape (MB_ROW_WARP beyond 256 vectors per row, MB_ROW_STAGED on
  * unaligned rows or rows too long for one stage, one-CTA paths on rows longer
