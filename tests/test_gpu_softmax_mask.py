@@ -146,3 +146,18 @@ def test_workload_full_size_sampled_rows_and_eager():
     eager = torch.softmax((dx * p["scale"]).masked_fill(mask, float("-inf")), dim=1)
     assert torch.equal(y == 0, eager == 0)
     assert float(((y - eager).abs() / eager.abs().clamp_min(1e-30)).max()) < 1e-5
+
+
+def test_planner_counts_the_unmasked_share():
+    """A causal score row under a square mask copies half its keys on
+    average, so the planner keeps more of them in flight per SM than it does
+    full softmax rows of the same length (the per-SM byte budget counts the
+    reads over the share of the row that is copied)."""
+    mb.set_row_path("auto")
+    for dt in ("f32", "bf16"):
+        causal = mb.row_plan("softmax_mask", dt, 131072, 4096)
+        full = mb.row_plan("softmax", dt, 131072, 4096)
+        assert causal["path"] == full["path"] == "staged"
+        assert causal["ctas"] >= full["ctas"], (dt, causal, full)
+    f32 = mb.row_plan("softmax_mask", "f32", 131072, 4096)
+    assert f32["ctas"] > mb.row_plan("softmax", "f32", 131072, 4096)["ctas"]
