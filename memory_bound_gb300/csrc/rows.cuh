@@ -59,7 +59,8 @@ constexpr int kCappedRegs = 40;   // registers per thread of rows_cta_kernel_cap
 constexpr int64_t kFlightBytesF32 = 128 * 1024;
 constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
-constexpr int kClusterRing = 1;   // staging ring depth on the cluster path
+constexpr int kClusterRing = 1;   // staging ring depth on the cluster path (bf16)
+constexpr int64_t kClusterStageMin = 64 * 1024;   // fp32 slices staged from this size (chains that ask)
 constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
 // Folds one slot's VEC values into the running first-pass partial (a sum, or a
@@ -765,12 +766,17 @@ template <class C> struct RowEngine {
                                        int64_t rows, int nvec, bool vec, int max_vpt_regs,
                                        RowPlan *p, const void **fn) {
         // Staged (bulk-async ring) for bf16 rows that are vectorised and in
-        // device memory, ring depth kClusterRing; fp32 rows load directly.
-        // Sweeps on GB300 (LN, 65536 columns): bf16 staged 4.24 TB/s against
-        // 3.49 direct (its register prefetch holds unpacked floats, halving
-        // the resident threads); fp32 direct 6.10 against 5.53 staged.  A
-        // requested depth (ctas_per_sm on this path) stages any dtype.
-        const bool staged = vec && !tun.no_bulk && (sizeof(T) == 2 || tun.ctas_per_sm > 0);
+        // device memory, ring depth kClusterRing; fp32 rows load directly,
+        // except for chains that ask (C::kClusterStageF32) when a CTA's slice
+        // is at least kClusterStageMin bytes, ring depth 2.  Sweeps on GB300:
+        // LN at 65536 columns, bf16 staged 4.24 TB/s against 3.49 direct (its
+        // register prefetch holds unpacked floats, halving the resident
+        // threads), fp32 direct 6.10 against 5.53 staged; fp32 softmax staged
+        // 6.0-6.7 against 5.0-6.3 direct for slices of 64 KB and more (65536
+        // to 524288 columns), direct ahead for smaller ones.  A requested
+        // depth (ctas_per_sm on this path) stages any dtype.
+        const bool may_stage = vec && !tun.no_bulk;
+        const bool staged = may_stage && (sizeof(T) == 2 || tun.ctas_per_sm > 0);
         const int VEC = vec ? kVecN : 1;
         int best_n = 0, best_cs = 0, best_vpt = 0, best_threads = 0, best_slice = 0;
         int best_ring = 0, best_smem = 0;
@@ -786,8 +792,10 @@ template <class C> struct RowEngine {
             if (cs < 2) continue;
             const int64_t stage_bytes = (int64_t)C::kInputs * slice_v * VEC * (int64_t)sizeof(T);
             int ring = 0, smem = 0;
-            if (staged) {
-                ring = tun.ctas_per_sm > 0 ? tun.ctas_per_sm : kClusterRing;
+            const bool stage_f32 = may_stage && C::kClusterStageF32 && sizeof(T) == 4 &&
+                                   stage_bytes >= kClusterStageMin;
+            if (staged || stage_f32) {
+                ring = tun.ctas_per_sm > 0 ? tun.ctas_per_sm : (staged ? kClusterRing : 2);
                 if (ring > kMaxStages) ring = kMaxStages;
                 // (the kernel's static shared memory stays within kHdrBytes)
                 while (ring > 1 && ring * stage_bytes + kHdrBytes > ctx.smem_optin) --ring;
