@@ -93,6 +93,7 @@ template <typename TT> struct LnGeluChain {
     // columns 5% slower), 32 for bf16 rows (3% faster than 16)
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;
     static constexpr bool kClusterStageF32 = false;   // direct loads measured faster
+    static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = false;
@@ -170,6 +171,7 @@ template <typename TT> struct InductorChainT {
     static constexpr int kRowsTarget = 0;
     static constexpr int kClusterVals = 16;   // see LnGeluChain
     static constexpr bool kClusterStageF32 = false;   // direct loads measured faster
+    static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = false;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = false;
@@ -278,6 +280,7 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     static constexpr int kRowsTarget = kRegCap ? 6 : 0;
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;   // as LnGeluChain
     static constexpr bool kClusterStageF32 = false;   // direct loads measured faster
+    static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
     static constexpr bool kStorePre = true;
@@ -383,6 +386,7 @@ template <typename TT> struct SoftmaxChain {
     // fp32 rows on the cluster path are staged when a CTA's slice is 64 KB
     // or more (softmax at 131072 columns: 6.0 TB/s staged, 5.5 direct)
     static constexpr bool kClusterStageF32 = true;
+    static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = true;
     static constexpr bool kStorePre = false;
@@ -472,6 +476,9 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     // fp32 rows on the cluster path are staged when a CTA's slice is 64 KB
     // or more (softmax at 131072 columns: 6.0 TB/s staged, 5.5 direct)
     static constexpr bool kClusterStageF32 = true;
+    // rows may end early (row_extent): the direct paths skip the loads of
+    // slots wholly past a row's unmasked prefix
+    static constexpr bool kPartialRows = true;
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = true;
     static constexpr bool kStorePre = false;

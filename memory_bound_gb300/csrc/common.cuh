@@ -259,6 +259,16 @@ template <typename T, int VEC> struct Frag {
                 unpack(__ldcs(reinterpret_cast<const uint4 *>(p) + q), q);
         }
     }
+    // the streaming load when `take`, else zeros (a slot the chain never
+    // reads: the masked tail of a causal score row)
+    __device__ __forceinline__ void load_stream_if(const T *p, bool take) {
+        if (take) {
+            load_stream(p);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) f[e] = 0.0f;
+        }
+    }
     // cached read-only load (per-column vectors, reused by every row)
     __device__ __forceinline__ void load_cached(const T *p) {
         if constexpr (VEC == 1) {

@@ -104,11 +104,13 @@ rows_warp_kernel(const typename C::Args a, int64_t rows, int cols, int, unsigned
         Frag<T, VEC> in[VPL][NIN];
         typename C::template PrePC<VEC> pre[VPL];
         typename C::template PostPC<VEC> post[VPL];
+        const int ext = C::kPartialRows ? C::row_extent(a, row, cols) : cols;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int vc = min(lane + 32 * k, nvec - 1);
 #pragma unroll
-            for (int i = 0; i < NIN; ++i) in[k][i].load_stream(a.in[i] + base + vc * VEC);
+            for (int i = 0; i < NIN; ++i)
+                in[k][i].load_stream_if(a.in[i] + base + vc * VEC, !C::kPartialRows || vc * VEC < ext);
             C::template load_pre<VEC>(a, vc * VEC, pre[k]);
             C::template load_post<VEC>(a, vc * VEC, post[k]);
         }
@@ -242,13 +244,15 @@ __device__ __forceinline__ void rows_cta_body(const typename C::Args &a, int64_t
             if (!mbar_wait_bounded(smem_addr(&bars[s]), parity)) abort_flag[li & 1] = 1;
         }
         Frag<T, VEC> in[VPT][NIN];
+        const int ext = C::kPartialRows && !STAGED ? C::row_extent(a, row, cols) : cols;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
 #pragma unroll
             for (int i = 0; i < NIN; ++i) {
                 if constexpr (STAGED) in[k][i].load_shared(stage + (size_t)i * cols + vc * VEC);
-                else in[k][i].load_stream(a.in[i] + base + vc * VEC);
+                else in[k][i].load_stream_if(a.in[i] + base + vc * VEC,
+                                             !C::kPartialRows || vc * VEC < ext);
             }
         }
         float v[VPT][VEC];
@@ -471,11 +475,14 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     auto load_row = [&](int64_t r) {
         if (nvec == 0) return;
         load_cols();
+        const int ext = C::kPartialRows ? C::row_extent(a, r, cols) : cols;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
 #pragma unroll
-            for (int i = 0; i < NIN; ++i) in[k][i].load_stream(a.in[i] + r * cols + lo + vc * VEC);
+            for (int i = 0; i < NIN; ++i)
+                in[k][i].load_stream_if(a.in[i] + r * cols + lo + vc * VEC,
+                                        !C::kPartialRows || lo + vc * VEC < ext);
         }
     };
     if constexpr (!STAGED) {
