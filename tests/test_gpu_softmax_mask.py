@@ -90,6 +90,22 @@ def test_masked_values_take_no_part(path, row_path):
     check(to_host(y), oracle.scale_mask_softmax(x, 0.125, True), False, m, path)
 
 
+@pytest.mark.parametrize("cols", [4096, 40000])
+def test_masked_values_in_host_memory(cols):
+    """Score rows in pinned host memory take the direct paths, which skip
+    the slots past each row's unmasked prefix; NaN and inf there change
+    nothing (one-CTA rows and rows on a cluster)."""
+    rows = 48
+    x = synth.normal(2204, 0, (rows, cols), 0.0, 2.0)
+    m = masked(rows, cols, rows, 3)
+    dirty = x.copy()
+    dirty[m] = np.where(np.arange(m.sum()) % 2 == 0, np.nan, np.inf).astype(np.float32)
+    y = mb.fused_row_softmax(torch.from_numpy(dirty).pin_memory(), scale=0.125, causal=True,
+                             period=rows, offset=3)
+    torch.cuda.synchronize()
+    check(y.numpy(), oracle.scale_mask_softmax(x, 0.125, True, rows, 3), False, m, f"host {cols}")
+
+
 def test_multi_head_periods_and_host_memory():
     """Rows of several heads (period 512 queries, keys offset by 256), the
     score rows in pinned host memory."""
