@@ -92,7 +92,7 @@ template <typename TT> struct LnGeluChain {
     // CTA: 16 for fp32 (x, r, w and b held per value; 32 ran LN at 65536
     // columns 5% slower), 32 for bf16 rows (3% faster than 16)
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;
-    static constexpr bool kClusterStageF32 = false;   // direct loads measured faster
+    static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
@@ -170,7 +170,7 @@ template <typename TT> struct InductorChainT {
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
     static constexpr int kClusterVals = 16;   // see LnGeluChain
-    static constexpr bool kClusterStageF32 = false;   // direct loads measured faster
+    static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = false;
     static constexpr bool kMaxFirst = false;
@@ -279,7 +279,7 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     static constexpr bool kRegCap = DROP && sizeof(T) == 4;
     static constexpr int kRowsTarget = kRegCap ? 6 : 0;
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;   // as LnGeluChain
-    static constexpr bool kClusterStageF32 = false;   // direct loads measured faster
+    static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = false;
@@ -383,9 +383,11 @@ template <typename TT> struct SoftmaxChain {
     // one input and no per-column vectors: 32 values per thread on the
     // cluster path (softmax fp32 at 40000 columns 4.5% faster than 16)
     static constexpr int kClusterVals = 32;
-    // fp32 rows on the cluster path are staged when a CTA's slice is 64 KB
-    // or more (softmax at 131072 columns: 6.0 TB/s staged, 5.5 direct)
-    static constexpr bool kClusterStageF32 = true;
+    // on the cluster path a CTA slice of 64 KB or more is staged: fp32 rows
+    // through the ring into registers (131072 columns: 6.0 TB/s against 5.5
+    // direct), bf16 rows held in the ring (rows_cluster_smem_kernel; 4.9
+    // against 4.0)
+    static constexpr bool kStageLargeSlices = true;
     static constexpr bool kPartialRows = false;   // every row read whole
     static constexpr bool kTwoPass = true;
     static constexpr bool kMaxFirst = true;
@@ -473,9 +475,11 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     // one input and no per-column vectors: 32 values per thread on the
     // cluster path (softmax fp32 at 40000 columns 4.5% faster than 16)
     static constexpr int kClusterVals = 32;
-    // fp32 rows on the cluster path are staged when a CTA's slice is 64 KB
-    // or more (softmax at 131072 columns: 6.0 TB/s staged, 5.5 direct)
-    static constexpr bool kClusterStageF32 = true;
+    // on the cluster path a CTA slice of 64 KB or more is staged: fp32 rows
+    // through the ring into registers (131072 columns: 6.0 TB/s against 5.5
+    // direct), bf16 rows held in the ring (rows_cluster_smem_kernel; 4.9
+    // against 4.0)
+    static constexpr bool kStageLargeSlices = true;
     // rows may end early (row_extent): the direct paths skip the loads of
     // slots wholly past a row's unmasked prefix
     static constexpr bool kPartialRows = true;

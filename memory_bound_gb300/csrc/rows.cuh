@@ -60,7 +60,7 @@ constexpr int64_t kFlightBytesF32 = 128 * 1024;
 constexpr int64_t kFlightBytesBf16 = 192 * 1024;
 constexpr int kMaxCluster = 16;   // CTAs per row on the cluster path (above 8: opt-in size)
 constexpr int kClusterRing = 1;   // staging ring depth on the cluster path (bf16)
-constexpr int64_t kClusterStageMin = 64 * 1024;   // fp32 slices staged from this size (chains that ask)
+constexpr int64_t kClusterStageMin = 64 * 1024;   // slices staged from this size (C::kStageLargeSlices)
 constexpr int64_t kUnboundedRows = (int64_t)1 << 40;   // row count the cached plans assume
 
 // Folds one slot's VEC values into the running first-pass partial (a sum, or a
@@ -601,6 +601,160 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     cl.sync();     // no CTA leaves while another may still push into its slots
 }
 
+// Rows longer than a CTA, the CTA's slice held in shared memory rather than
+// registers (bf16 rows of chains with C::kStageLargeSlices, slices of
+// kClusterStageMin bytes or more): one elected thread streams the slice of
+// each row into a ring of nstage stages with bulk async copies; every pass
+// (the first statistic, the second, the epilogue) reads it back from the
+// stage, so a thread holds one vector at a time and a CTA keeps 1024 threads
+// at about 40 registers.  The second pass's in-place transform (p2) is
+// applied again in the epilogue, so each value reaches `post` exactly as on
+// the register path.  A stage is refilled once the epilogue of its row has
+// read it.  Waits and exchanges are bounded as in rows_cluster_kernel.
+template <class C, int VEC>
+__global__ void __launch_bounds__(kCtaMaxThreads, 1)
+rows_cluster_smem_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
+                         unsigned *err, int nstage) {
+    namespace cg = cooperative_groups;
+    using T = typename C::T;
+    constexpr int NIN = C::kInputs;
+    using PrePC = typename C::template PrePC<VEC>;
+    using PostPC = typename C::template PostPC<VEC>;
+    extern __shared__ __align__(1024) unsigned char ring[];   // [nstage][NIN][slice]
+    __shared__ float red[2][32];
+    __shared__ float xch[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ __align__(8) uint64_t sbar[kMaxStages];
+    __shared__ int stage_abort[2];
+    __shared__ int xch_abort[2];
+    cg::cluster_group cl = cg::this_cluster();
+    const int tid = threadIdx.x;
+    const int rank = (int)cl.block_rank();
+    const unsigned cs = cl.num_blocks();
+    const int64_t nclusters = gridDim.x / cs;
+    const int64_t cid = blockIdx.x / cs;
+    const int lo = rank * slice;
+    const int hi = lo + slice < cols ? lo + slice : cols;
+    const int nvec = hi > lo ? (hi - lo) / VEC : 0;
+    const int64_t nlocal = cid < rows ? (rows - cid + nclusters - 1) / nclusters : 0;
+    const uint32_t pitch = (uint32_t)slice * (uint32_t)sizeof(T);
+    const uint32_t my_bytes = (uint32_t)(nvec * VEC) * (uint32_t)sizeof(T);
+    const uint32_t stage_bytes = (uint32_t)NIN * pitch;
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        for (int q = 0; q < nstage; ++q) mbar_init(smem_addr(&sbar[q]), 1);
+        stage_abort[0] = stage_abort[1] = 0;
+        xch_abort[0] = xch_abort[1] = 0;
+        fence_mbar_init();
+    }
+    cl.sync();
+    pdl_wait();
+    pdl_launch_dependents();
+    auto issue = [&](int q, int64_t li) {
+        const int64_t row = cid + li * nclusters;
+        const uint32_t bar = smem_addr(&sbar[q]);
+        const int ext = C::row_extent(a, row, cols) - lo;
+        uint32_t bytes = ext <= 0 ? 0u
+                       : ((uint32_t)((ext + VEC - 1) / VEC) * VEC) * (uint32_t)sizeof(T);
+        if (bytes > my_bytes) bytes = my_bytes;
+        mbar_arrive_expect_tx(bar, (uint32_t)NIN * bytes);
+        if (bytes == 0) return;
+#pragma unroll
+        for (int i = 0; i < NIN; ++i)
+            bulk_g2s(smem_addr(ring + (size_t)q * stage_bytes + (size_t)i * pitch),
+                     a.in[i] + row * cols + lo, bytes, bar);
+    };
+    if (tid == 0) {
+        const int64_t n0 = nlocal < nstage ? nlocal : nstage;
+        for (int q = 0; q < (int)n0; ++q) issue(q, q);
+    }
+    int rb = 0, xb = 0;
+    uint32_t xpar[2] = {0u, 0u};
+    int q = 0;
+    uint32_t parity = 0;
+    int64_t li = 0;
+    const int nthr = (int)blockDim.x;
+    for (; li < nlocal; ++li) {
+        const int64_t row = cid + li * nclusters;
+        const int64_t base = row * cols + lo;
+        if (!mbar_wait_bounded(smem_addr(&sbar[q]), parity)) stage_abort[li & 1] = 1;
+        const T *stage = reinterpret_cast<const T *>(ring + (size_t)q * stage_bytes);
+        // v of vector vi of the slice (the prologue applied)
+        auto value = [&](int vi, float (&v)[VEC]) {
+            Frag<T, VEC> in[NIN];
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) in[i].load_shared(stage + (size_t)i * slice + vi * VEC);
+            PrePC pc;
+            C::template load_pre<VEC>(a, lo + vi * VEC, pc);
+            C::template pre<VEC>(in, pc, a, row, lo + vi * VEC, v);
+        };
+        float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
+        for (int vi = tid; vi < nvec; vi += nthr) {
+            float v[VEC];
+            value(vi, v);
+            l1 = fold1<C, VEC>(l1, v, true);
+            if constexpr (C::kStorePre) C::template store_pre<VEC>(v, a, base + vi * VEC);
+        }
+        const float c1 = C::kMaxFirst ? block_max(l1, red[rb]) : block_sum(l1, red[rb]);
+        rb ^= 1;
+        if (stage_abort[li & 1] | xch_abort[(li + 1) & 1]) break;
+        volatile int *ab = &xch_abort[li & 1];
+        const float r1 = cluster_reduce<C::kMaxFirst>(c1, xch[xb], &xbar[xb], xpar[xb], cs, rank, ab);
+        xb ^= 1;
+        const float mean = C::stat1(r1, cols, a);
+        float rstd = 0.0f;
+        if constexpr (C::kTwoPass) {
+            float l2 = 0.0f;
+            for (int vi = tid; vi < nvec; vi += nthr) {
+                float v[VEC];
+                value(vi, v);
+                l2 += C::template p2<VEC>(v, mean);
+            }
+            const float c2 = block_sum(l2, red[rb]);
+            rb ^= 1;
+            rstd = C::stat2(cluster_reduce<false>(c2, xch[xb], &xbar[xb], xpar[xb], cs, rank, ab),
+                            cols, a);
+            xb ^= 1;
+        }
+        if (rank == 0 && tid == 0) C::store_stats(a, row, mean, rstd);
+        for (int vi = tid; vi < nvec; vi += nthr) {
+            float v[VEC];
+            value(vi, v);
+            if constexpr (C::kTwoPass) (void)C::template p2<VEC>(v, mean);
+            typename C::template Early<VEC> ea;
+            C::template early<VEC>(a, base + vi * VEC, ea);
+            PostPC pc;
+            C::template load_post<VEC>(a, lo + vi * VEC, pc);
+            Frag<T, VEC> o;
+            C::template post<VEC>(v, mean, rstd, pc, a, base + vi * VEC, ea, o.f);
+            o.store_stream(a.out + base + vi * VEC);
+        }
+        // every thread has read the stage: refill it with row li + nstage
+        __syncthreads();
+        if (tid == 0 && li + nstage < nlocal) issue(q, li + nstage);
+        if (++q == nstage) {
+            q = 0;
+            parity ^= 1u;
+        }
+    }
+    if (tid == 0) {
+        if (li < nlocal || (xch_abort[0] | xch_abort[1])) atomicOr(err, kDevErrWaitTimeout);
+        // Only after a timeout: wait (bounded) for this CTA's copies still in
+        // flight before its shared memory goes away.
+        int qq = q;
+        uint32_t pp = parity;
+        for (int64_t lj = li; lj < nlocal && lj < li + nstage; ++lj) {
+            (void)mbar_wait_bounded(smem_addr(&sbar[qq]), pp);
+            if (++qq == nstage) {
+                qq = 0;
+                pp ^= 1u;
+            }
+        }
+    }
+    cl.sync();     // no CTA leaves while another may still push into its slots
+}
+
 // ---------------------------------------------------------------------------
 // host-side planning and launch
 // ---------------------------------------------------------------------------
@@ -769,12 +923,62 @@ template <class C> struct RowEngine {
         return MB_ERR_SHAPE;
     }
 
+    // The shared-memory-resident cluster kernel (bf16 rows of chains with
+    // C::kStageLargeSlices): among cluster sizes 2, 4, 8, 16 (or the
+    // requested one) whose CTA slice is kClusterStageMin bytes or more, the
+    // most resident clusters (ties: the smaller cluster), a ring of two
+    // stages where it fits (or the requested depth).  MB_ERR_SHAPE when no
+    // slice is that large (the register kernels serve those rows).  Sweeps on
+    // GB300, softmax bf16 (µs, register-staged against this kernel): 65536
+    // columns 446 / 399, 131072 534 / 437, 262144 601 / 462, 524288 695 /
+    // 566; with 32 and 40 KB slices (32776, 40000 columns) the register
+    // kernels stay ahead.
+    static mb_status plan_cluster_smem(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows,
+                                       int nvec, RowPlan *p, const void **fn) {
+        const void *f = (const void *)rows_cluster_smem_kernel<C, kVecN>;
+        int bn = 0, bcs = 0, bthr = 0, bslice = 0, bring = 0, bsmem = 0;
+        for (int cs0 : {2, 4, 8, 16}) {
+            int cs = cs0;
+            if (tun.stages >= 2 && tun.stages <= kMaxCluster) {
+                if (cs0 != 2) continue;
+                cs = tun.stages;
+            }
+            if (cs > nvec) cs = nvec;
+            const int slice_v = ceil_div(nvec, cs);
+            cs = ceil_div(nvec, slice_v);                  // no empty rank
+            if (cs < 2) continue;
+            const int64_t sb = (int64_t)C::kInputs * slice_v * kVecN * (int64_t)sizeof(T);
+            if (sb < kClusterStageMin || sb + kHdrBytes > ctx.smem_optin) continue;
+            int ring = tun.ctas_per_sm > 0 ? tun.ctas_per_sm : 2;
+            if (ring > kMaxStages) ring = kMaxStages;
+            while (ring > 1 && ring * sb + kHdrBytes > ctx.smem_optin) --ring;
+            const int threads = slice_v < kCtaMaxThreads ? round_up32(slice_v) : kCtaMaxThreads;
+            int n = 0;
+            mb_status st = active_clusters(ctx, f, cs, threads, (int)(ring * sb), &n);
+            if (st != MB_OK) return st;
+            if (n > bn) {
+                bn = n; bcs = cs; bthr = threads; bslice = slice_v; bring = ring;
+                bsmem = (int)(ring * sb);
+            }
+        }
+        if (!bn) return MB_ERR_SHAPE;
+        *fn = f;
+        const int64_t ncl = rows < bn ? rows : bn;
+        p->path = MB_ROW_CLUSTER; p->threads = bthr; p->vpt = ceil_div(bslice, bthr);
+        p->stages = bcs; p->smem = bsmem;
+        p->ctas = (int)(ncl * bcs);
+        p->slice = bslice;
+        p->ring = bring;
+        p->cap = bn;
+        return MB_OK;
+    }
+
     static mb_status plan_cluster_pass(const LaunchCtx &ctx, const RowTuning &tun,
                                        int64_t rows, int nvec, bool vec, int max_vpt_regs,
                                        RowPlan *p, const void **fn) {
         // Staged (bulk-async ring) for bf16 rows that are vectorised and in
         // device memory, ring depth kClusterRing; fp32 rows load directly,
-        // except for chains that ask (C::kClusterStageF32) when a CTA's slice
+        // except for chains that ask (C::kStageLargeSlices) when a CTA's slice
         // is at least kClusterStageMin bytes, ring depth 2.  Sweeps on GB300:
         // LN at 65536 columns, bf16 staged 4.24 TB/s against 3.49 direct (its
         // register prefetch holds unpacked floats, halving the resident
@@ -784,6 +988,12 @@ template <class C> struct RowEngine {
         // depth (ctas_per_sm on this path) stages any dtype.
         const bool may_stage = vec && !tun.no_bulk;
         const bool staged = may_stage && (sizeof(T) == 2 || tun.ctas_per_sm > 0);
+        if constexpr (C::kStageLargeSlices && sizeof(T) == 2) {
+            if (staged) {
+                const mb_status st = plan_cluster_smem(ctx, tun, rows, nvec, p, fn);
+                if (st != MB_ERR_SHAPE) return st;
+            }
+        }
         const int VEC = vec ? kVecN : 1;
         int best_n = 0, best_cs = 0, best_vpt = 0, best_threads = 0, best_slice = 0;
         int best_ring = 0, best_smem = 0;
@@ -799,7 +1009,7 @@ template <class C> struct RowEngine {
             if (cs < 2) continue;
             const int64_t stage_bytes = (int64_t)C::kInputs * slice_v * VEC * (int64_t)sizeof(T);
             int ring = 0, smem = 0;
-            const bool stage_f32 = may_stage && C::kClusterStageF32 && sizeof(T) == 4 &&
+            const bool stage_f32 = may_stage && C::kStageLargeSlices && sizeof(T) == 4 &&
                                    stage_bytes >= kClusterStageMin;
             if (staged || stage_f32) {
                 ring = tun.ctas_per_sm > 0 ? tun.ctas_per_sm : (staged ? kClusterRing : 2);

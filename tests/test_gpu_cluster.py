@@ -100,6 +100,36 @@ def test_32_value_kernel_forms(cs, ring, bf16, row_path):
     _check_chains(5, 65536, 7000 + 10 * cs + ring, bf16)
 
 
+def _bf16_to_f64(a):
+    return (np.asarray(a).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("cols", [65536, 65544, 131072, 262152])
+def test_bf16_softmax_slices_in_shared_memory(cols):
+    """bf16 softmax rows whose CTA slices reach 64 KB keep the slice in the
+    shared-memory ring (1024 threads a CTA, every pass reading the stage):
+    plain and scaled, causally masked rows, more rows than resident
+    clusters, ragged row lengths."""
+    rows = 200
+    p = mb.row_plan("softmax", "bf16", rows, cols)
+    assert p["path"] == "cluster" and p["threads"] == 1024 and p["smem"] >= 65536, p
+    x = synth.normal(8000 + cols % 101, 0, (rows, cols), 0.0, 2.0, dtype="bf16")
+    buf, y = guarded_empty((rows, cols), torch.bfloat16)
+    mb.fused_row_softmax(to_dev(x, True), out=y)
+    want = _bf16_to_f64(oracle.row_softmax(x))
+    got = _bf16_to_f64(to_host(y))
+    assert np.all(np.abs(got - want) <= 1e-2 * np.abs(want) + 2.0 ** -126), "softmax"
+    check_guard(buf)
+    period, offset = 7, cols // 3
+    ym = to_host(mb.fused_row_softmax(to_dev(x, True), scale=0.125, causal=True, period=period,
+                                      offset=offset))
+    wm = _bf16_to_f64(oracle.scale_mask_softmax(x, 0.125, True, period, offset))
+    gm = _bf16_to_f64(ym)
+    masked = np.arange(cols)[None, :] > (np.arange(rows)[:, None] % period + offset)
+    assert np.all(gm[masked] == 0), "a masked output is not 0"
+    assert np.all(np.abs(gm - wm) <= 1e-2 * np.abs(wm) + 2.0 ** -126), "masked softmax"
+
+
 def test_long_rows_many_rows_and_unaligned():
     """More rows than clusters fit at once (each cluster loops over rows), and
     an unaligned scalar row length."""
