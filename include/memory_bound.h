@@ -348,9 +348,11 @@ typedef enum mb_row_path {
     MB_ROW_CLUSTER = 4   /* one thread-block cluster per row: each CTA holds a
                             slice in registers (bf16 rows in vectorised device
                             memory staged by bulk async copies, fp32 rows
-                            loaded directly unless a ring depth is asked for),
-                            statistics combined through distributed shared
-                            memory (automatic above 32768 elements)            */
+                            loaded directly unless a ring depth is asked for;
+                            softmax slices of 64 KB or more staged, bf16 ones
+                            kept in shared memory), statistics combined
+                            through distributed shared memory (automatic above
+                            32768 elements)                                    */
 } mb_row_path;
 
 /*
