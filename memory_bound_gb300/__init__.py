@@ -13,6 +13,9 @@ fallback of any kind, and calling a chain without the built library raises.
     fused_layernorm_act(x, r, w, b, eps=1e-5, act="gelu_tanh", want_h=False)   # r may be None
     fused_row_softmax(x, out=None)
 
+``graph.ChainGraph`` captures a sequence of these calls into one CUDA graph
+for replay.
+
 ``raw`` exposes the C entry points themselves (plain integers for pointers
 and streams) for callers that manage their own memory.
 """
@@ -22,3 +25,4 @@ from ._binding import (  # noqa: F401
     fused_residual_layernorm_gelu, fused_row_softmax, library_path, load_library, raw, row_plan,
     set_launch_overlap, set_pointwise_shape, set_row_path, status_string,
 )
+from . import graph  # noqa: F401,E402

@@ -33,12 +33,8 @@ def gpu():
 
 
 def _capture(fn):
-    fn()                                   # first call outside: plans and attributes
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, capture_error_mode="thread_local"):
-        fn()
-    return g
+    """The package's graph harness (one call outside the capture first)."""
+    return mb.graph.ChainGraph(fn)
 
 
 def _inputs(w, seed):
