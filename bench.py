@@ -402,6 +402,22 @@ def time_steps_graph(cases, steps, warmup, world=1):
     return a.elapsed_time(b) / steps
 
 
+def plan_chain(w):
+    """The row-plan query name of a workload's chain (None for the pointwise
+    chains, which have no row plan)."""
+    p = w.params
+    if w.chain == "ln_gelu":
+        return "ln"
+    if w.chain in ("inductor", "softmax", "softmax_mask"):
+        return w.chain
+    if w.chain == "lnact":
+        if p.get("write_h"):
+            return "lnact_res_h"
+        name = "lnact_res" if p.get("residual") else "lnact"
+        return name + "_dropout" if p.get("p") else name
+    return None
+
+
 def time_single_flushed(cases, fn, reps, flush):
     """Per case: (p10, median, p90) milliseconds of one call after an L2
     flush (a 1 GiB read, outside the events) -- the latency of an isolated
@@ -756,9 +772,8 @@ def run_ours(args):
                                                        round(single[c.w.name][2] * 1e3, 3)],
                  "size_matched_copy_us": round(copy_ms[c.w.name] * 1e3, 3),
                  "frac_of_size_matched_copy": round(copy_ms[c.w.name] / mean_ms, 4)}
-        if c.w.chain != "add_relu_scale":
-            entry["launch"] = mb.row_plan("ln" if c.w.chain == "ln_gelu" else "inductor",
-                                          c.w.dtype, c.w.rows, c.w.cols)
+        if plan_chain(c.w):
+            entry["launch"] = mb.row_plan(plan_chain(c.w), c.w.dtype, c.w.rows, c.w.cols)
         if eager:
             em = eager[c.w.name]
             entry["eager_us_per_call"] = round(em * 1e3, 3)
@@ -786,6 +801,8 @@ def run_ours(args):
                    "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
                    "size_matched_copy_us": round(cp_next[c.w.name] * 1e3, 3),
                    "frac_of_size_matched_copy": round(cp_next[c.w.name] / ms, 4)}
+            if plan_chain(c.w):
+                ent["launch"] = mb.row_plan(plan_chain(c.w), c.w.dtype, c.w.rows, c.w.cols)
             if e_next:
                 ent["eager_us_per_call"] = round(e_next[c.w.name] * 1e3, 3)
                 ent["speedup_vs_eager"] = round(e_next[c.w.name] / ms, 2)

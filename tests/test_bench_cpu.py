@@ -20,3 +20,19 @@ def test_cpu_baselines_on_a_small_sample():
 def test_host_info():
     h = bench.host_info()
     assert h["cores_available"] >= 1 and h["cpu"]
+
+
+def test_plan_chain_names_every_row_workload():
+    """Every row workload maps to a plan-query chain name the binding
+    accepts; the pointwise chains have none."""
+    from synth import workloads as W
+    names = {"ln", "inductor", "lnact_res", "lnact", "softmax", "lnact_res_dropout",
+             "lnact_dropout", "lnact_res_h", "softmax_mask"}
+    for w in W.ALL + W.NEXT:
+        got = bench.plan_chain(w)
+        if w.chain.startswith("add_relu_scale"):
+            assert got is None, w.name
+        else:
+            assert got in names, (w.name, got)
+    assert bench.plan_chain(W.LNACT_RELU_DROP_F32) == "lnact_dropout"
+    assert bench.plan_chain(W.LNACT_RES_BF16) == "lnact_res_h"
