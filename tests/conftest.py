@@ -16,3 +16,16 @@ for p in (ROOT, TESTS):
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the worst-case figures the whole-tensor parity checks recorded."""
+    mod = sys.modules.get("gpu_util")
+    rows = getattr(mod, "PARITY_REPORT", None) if mod else None
+    if not rows:
+        return
+    terminalreporter.write_sep("-", "parity: worst case over every element, against the oracle")
+    for what, fields in rows:
+        terminalreporter.write_line(
+            f"{what}: " + ", ".join(f"{k}={v:.3g}" if isinstance(v, float) else f"{k}={v}"
+                                   for k, v in fields.items()))

@@ -90,3 +90,22 @@ def check_guard(buf, guard=64):
         sentinel = 0x7FA5A5A5
     head, tail = v[:guard], v[-guard:]
     assert bool((head == sentinel).all()) and bool((tail == sentinel).all()), "write outside the output"
+
+
+# Worst-case figures of the whole-tensor checks, printed at the end of the
+# run by the terminal-summary hook in conftest.py.
+PARITY_REPORT = []
+
+
+def report(what, **fields):
+    PARITY_REPORT.append((what, fields))
+
+
+def max_rel_above(got, want, bf16=False, floor=1e-3):
+    """Largest pure relative error over the elements whose oracle value is at
+    least ``floor`` in magnitude (the fp32 bar carries an absolute floor below
+    1; this is the figure without it)."""
+    g = bf16_to_f64(got) if bf16 else np.asarray(got, np.float64)
+    w = bf16_to_f64(want) if bf16 else np.asarray(want, np.float64)
+    big = np.abs(w) >= floor
+    return float((np.abs(g - w)[big] / np.abs(w[big])).max()) if big.any() else 0.0

@@ -17,6 +17,7 @@ from synth import workloads as W
 
 from gpu_util import (assert_bitexact, assert_close, bf16_to_f64, check_guard, guarded_empty,
                       to_dev, to_host)
+from row_blocks import dropout_block_offset, map_row_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -68,8 +69,8 @@ def check_dropout(got, want, keep, bf16, what):
 def check_stats(mean, rstd, want_mean, want_rstd, what):
     """mean within 1e-5 of the row's standard deviation (what the normalised
     output sees), rstd within 1e-5 relative."""
-    m = to_host(mean).astype(np.float64)
-    r = to_host(rstd).astype(np.float64)
+    m = (to_host(mean) if torch.is_tensor(mean) else np.asarray(mean)).astype(np.float64)
+    r = (to_host(rstd) if torch.is_tensor(rstd) else np.asarray(rstd)).astype(np.float64)
     assert np.all(np.abs(m - want_mean) <= 1e-5 / want_rstd + 1e-7 * np.abs(want_mean)), what
     assert np.all(np.abs(r - want_rstd) <= 1e-5 * want_rstd), what
 
@@ -182,8 +183,8 @@ def test_graph_replay_is_deterministic():
 
 
 def test_pages_chain_full_size():
-    """LayerNorm -> ReLU -> Dropout(p = 0.1) on the fp32 8192 x 4096 rows:
-    sampled rows against the oracle (mask, values, statistics), and the keep
+    """LayerNorm -> ReLU -> Dropout(p = 0.1) on the fp32 8192 x 4096 rows: every
+    row against the oracle (keep mask exact, values, statistics), and the keep
     rate over the whole tensor within 5 sigma of 0.9."""
     wl = W.LNACT_RELU_DROP_F32
     t = wl.generate_all()
@@ -193,20 +194,24 @@ def test_pages_chain_full_size():
                                                 act="relu", p=p, seed=seed, offset=offset,
                                                 want_stats=True)
     torch.cuda.synchronize()
-    rows = W.sample_rows(wl.rows, 24)
-    got = to_host(out)[rows]
-    plain, _, wm, wr = oracle.layernorm_act_ex(t["x"][rows], None, t["w"], t["b"], 1e-5,
-                                               oracle.ACT_RELU, want_stats=True)
-    for k, row in enumerate(rows):
-        keep = oracle.dropout_mask(seed, offset, int(row) * wl.cols, wl.cols, p)
-        want = np.where(keep, plain[k].astype(np.float64) / (1 - p), 0.0)
-        g = got[k].astype(np.float64)
-        assert np.all(g[~keep] == 0)
-        assert np.all(np.abs(g - want) <= 2e-5 * np.maximum(np.abs(want), 1.0)), row
-    check_stats(mean[torch.from_numpy(rows).cuda()], rstd[torch.from_numpy(rows).cuda()], wm, wr,
-                wl.name)
-    # every element: zero iff dropped or relu gave zero
-    n = wl.rows * wl.cols
+    got, got_mean, got_rstd = to_host(out), to_host(mean), to_host(rstd)
+    cols = wl.cols
+
+    def block(r0, r1):
+        want, _, wm, wr = oracle.layernorm_act_ex(
+            t["x"][r0:r1], None, t["w"], t["b"], 1e-5, oracle.ACT_RELU, p=p, seed=seed,
+            offset=dropout_block_offset(offset, r0, cols), want_stats=True)
+        keep = oracle.dropout_mask(seed, offset, r0 * cols, (r1 - r0) * cols, p)
+        what = f"{wl.name} rows {r0}:{r1}"
+        check_dropout(got[r0:r1], want, keep.reshape(r1 - r0, cols), False, what)
+        check_stats(got_mean[r0:r1], got_rstd[r0:r1], wm, wr, what)
+        return int(keep.sum())
+
+    kept = sum(map_row_blocks(wl.rows, block, align=8))
+    n = wl.rows * cols
+    sigma = (n * p * (1 - p)) ** 0.5
+    assert abs(kept - n * (1 - p)) <= 5 * sigma
+    # every element: nonzero iff kept and relu gave a nonzero value
     nonzero = int((out != 0).sum().item())
     positive = int((mb.fused_layernorm_act(d["x"], None, d["w"], d["b"], act="relu") > 0)
                    .sum().item())

@@ -3,9 +3,14 @@
 and direct CTA row engines, the warp row engine).
 
 Inputs are a seeded block from synth tiled on the device (row or element i
-takes block entry i mod B, B chosen coprime to powers of two); the oracle
-computes the expected values of sampled elements and rows, including those
-around index 2^31 and the last ones.  About 35 GB of device memory per test.
+takes block entry i mod B, B chosen coprime to powers of two).  Every element
+is checked: the first period against the oracle, and every later period bit
+for bit against the first on the device (the chains are row- or
+element-local, so equal inputs give equal outputs wherever they sit); the
+elements around index 2^31 and the last ones are also compared with the
+oracle directly.  Dropout keys its decisions by the element's index, so that
+test runs the oracle over every row in blocks on the host's cores.  About
+35 GB of device memory per test.
 """
 import numpy as np
 import pytest
@@ -16,6 +21,7 @@ import oracle
 import synth
 
 from gpu_util import assert_bitexact, assert_close, to_dev, to_host
+from row_blocks import dropout_block_offset, map_row_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +55,16 @@ def _tile(block, n_lead):
     return d.repeat((reps,) + (1,) * (block.ndim - 1))[:n_lead].contiguous()
 
 
+def _assert_periodic(t, B, what):
+    """Each period of B entries along t's leading dimension equals the first,
+    bit for bit (the ragged last period against the first's prefix)."""
+    bits = t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16)
+    first = bits[:B]
+    for k0 in range(B, t.shape[0], B):
+        seg = bits[k0:k0 + B]
+        assert torch.equal(seg, first[:seg.shape[0]]), f"{what}: period at {k0} differs"
+
+
 def _sample(n, count=64, seed=5):
     rng = np.random.default_rng(seed)
     pick = {0, n - 1, TWO31 - 1, TWO31, TWO31 + 1} | set(rng.integers(0, n, count).tolist())
@@ -66,6 +82,8 @@ def test_pointwise_beyond_2_31():
     j = idx % B
     want = oracle.add_relu_scale(blk[0][j], blk[1][j], blk[2][j], 0.5)
     assert_bitexact(got, want, "pointwise > 2^31")
+    assert_bitexact(to_host(y[:B]), oracle.add_relu_scale(*blk, 0.5), "pointwise first period")
+    _assert_periodic(y, B, "pointwise > 2^31")
 
 
 @pytest.mark.parametrize("path", ["auto", "direct"])
@@ -84,6 +102,9 @@ def test_layernorm_rows_beyond_2_31(path):
     j = rows_s % B
     want = oracle.residual_layernorm_gelu(x_b[j], r_b[j], w, b, 1e-5)
     assert_close(got, want, what=f"LN rows > 2^31 elements ({path})")
+    assert_close(to_host(out[:B]), oracle.residual_layernorm_gelu(x_b, r_b, w, b, 1e-5),
+                 what=f"LN first period ({path})")
+    _assert_periodic(out, B, f"LN rows > 2^31 elements ({path})")
 
 
 def test_warp_rows_beyond_2_31():
@@ -101,6 +122,9 @@ def test_warp_rows_beyond_2_31():
     got = to_host(y[torch.from_numpy(rows_s).cuda()])
     want = oracle.bias_relu_branch_mean_epilogue(x_b[rows_s % B], bias, gamma, beta)
     assert_close(got, want, what="Inductor rows > 2^31 elements")
+    assert_close(to_host(y[:B]), oracle.bias_relu_branch_mean_epilogue(x_b, bias, gamma, beta),
+                 what="Inductor first period")
+    _assert_periodic(y, B, "Inductor rows > 2^31 elements")
 
 
 def test_softmax_rows_beyond_2_31():
@@ -114,6 +138,10 @@ def test_softmax_rows_beyond_2_31():
     got = to_host(y[torch.from_numpy(rows_s).cuda()]).astype(np.float64)
     want = oracle.row_softmax(x_b[rows_s % B]).astype(np.float64)
     assert np.all(np.abs(got - want) <= 1e-5 * want + 2.0 ** -126)
+    got = to_host(y[:B]).astype(np.float64)
+    want = oracle.row_softmax(x_b).astype(np.float64)
+    assert np.all(np.abs(got - want) <= 1e-5 * want + 2.0 ** -126)
+    _assert_periodic(y, B, "softmax rows > 2^31 elements")
 
 
 def test_layernorm_dropout_rows_beyond_2_31():
@@ -129,11 +157,19 @@ def test_layernorm_dropout_rows_beyond_2_31():
     p, seed, offset = 0.1, 31337, 12
     out = mb.fused_layernorm_act(x, None, to_dev(w), to_dev(b), act="relu", p=p, seed=seed,
                                  offset=offset)
-    rows_s = np.unique(np.r_[_sample(rows, 16), [TWO31 // cols - 1, TWO31 // cols]])
-    got = to_host(out[torch.from_numpy(rows_s).cuda()]).astype(np.float64)
-    plain = oracle.layernorm_act(x_b[rows_s % B], None, w, b, 1e-5, oracle.ACT_RELU)
-    for k, row in enumerate(rows_s):
-        keep = oracle.dropout_mask(seed, offset, int(row) * cols, cols, p)
-        want = np.where(keep, plain[k].astype(np.float64) / (1 - p), 0.0)
-        assert np.all(got[k][~keep] == 0), row
-        assert np.all(np.abs(got[k] - want) <= 2e-5 * np.maximum(np.abs(want), 1.0)), row
+    torch.cuda.synchronize()
+    got = to_host(out)
+    assert got.shape == (rows, cols)
+
+    def block(r0, r1):
+        want, _, _, _ = oracle.layernorm_act_ex(
+            x_b[np.arange(r0, r1) % B], None, w, b, 1e-5, oracle.ACT_RELU, p=p, seed=seed,
+            offset=dropout_block_offset(offset, r0, cols))
+        keep = oracle.dropout_mask(seed, offset, r0 * cols, (r1 - r0) * cols, p)
+        g, k = got[r0:r1].reshape(-1), keep
+        what = f"dropout rows {r0}:{r1} (> 2^31 elements)"
+        assert np.all(g[~k] == 0), what
+        assert np.all(g[k & (want.reshape(-1) != 0)] != 0), what
+        return assert_close(got[r0:r1], want, what=what)
+
+    map_row_blocks(rows, block, align=8)
