@@ -339,12 +339,15 @@ def time_steady(cases, fn, steps, warmup):
     return {name: a.elapsed_time(b) / steps for name, (a, b) in ev.items()}
 
 
-def time_graph(cases, fn, steps, warmup):
-    """Per case: mean milliseconds per call over `steps` back-to-back calls
+def time_graph(cases, fn, steps, warmup, replays=1):
+    """Per case: milliseconds per call over `steps` back-to-back calls
     cycling through its buffer sets, captured once into a CUDA graph and
     replayed between CUDA events, so the GPU runs the calls back to back with
     no host launch gaps (the calls themselves are the library's ordinary
-    entry points; it neither allocates nor synchronises, so it captures)."""
+    entry points; it neither allocates nor synchronises, so it captures).
+    With replays > 1 the graph is replayed that many times, each replay
+    between its own event pair; a case then maps to the list of per-call
+    means, one per replay (else to the one mean)."""
     import torch
     stream = torch.cuda.current_stream()
     out = {}
@@ -358,14 +361,23 @@ def time_graph(cases, fn, steps, warmup):
                 fn(c, k)
         g.replay()                              # untimed: the first launch uploads the graph
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(replays)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
         torch.cuda.synchronize()
-        out[c.w.name] = a.elapsed_time(b) / steps
+        ms = [a.elapsed_time(b) / steps for a, b in ev]
+        out[c.w.name] = ms if replays > 1 else ms[0]
         del g
     return out
+
+
+def spread(ms_list):
+    """(mean, median, p10, p90) of per-call milliseconds, one per replay."""
+    q = np.percentile(np.array(ms_list), [50, 10, 90])
+    return float(np.mean(ms_list)), float(q[0]), float(q[1]), float(q[2])
 
 
 def time_steps_graph(cases, steps, warmup, world=1):
@@ -726,11 +738,14 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # per-kernel figures: the K-call graph replayed until at least 100 calls
+    # (and 10 replays) are timed; median and spread over the replays
+    replays = max(10, -(-100 // args.steps))
     with ClockSampler(local, enabled=not args.no_clocks) as clk:
         t_wall0 = time.perf_counter()
         step_region_ms = time_steps_graph(cases, args.steps, args.warmup, world)
         t_wall = time.perf_counter() - t_wall0
-        ours = time_graph(cases, lambda c, k: c.call(k), args.steps, args.warmup)
+        ours = time_graph(cases, lambda c, k: c.call(k), args.steps, args.warmup, replays)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -757,11 +772,14 @@ def run_ours(args):
     step_ms = 0.0
     step_bytes = 0
     for c in cases:
-        mean_ms = ours[c.w.name]
+        mean_ms, med_ms, p10_ms, p90_ms = spread(ours[c.w.name])
         step_ms += mean_ms
         step_bytes += c.ideal
-        gbs = c.ideal / (mean_ms * 1e-3) / 1e9
-        entry = {"us_per_call": round(mean_ms * 1e3, 3),
+        gbs = c.ideal / (med_ms * 1e-3) / 1e9
+        entry = {"us_per_call": round(med_ms * 1e3, 3),
+                 "us_per_call_p10_p90": [round(p10_ms * 1e3, 3), round(p90_ms * 1e3, 3)],
+                 "us_per_call_mean": round(mean_ms * 1e3, 3),
+                 "calls_timed": replays * args.steps,
                  "ideal_bytes": c.ideal, "gbs": round(gbs, 1),
                  "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
                  "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
@@ -771,7 +789,7 @@ def run_ours(args):
                  "us_single_call_l2_flushed_p10_p90": [round(single[c.w.name][0] * 1e3, 3),
                                                        round(single[c.w.name][2] * 1e3, 3)],
                  "size_matched_copy_us": round(copy_ms[c.w.name] * 1e3, 3),
-                 "frac_of_size_matched_copy": round(copy_ms[c.w.name] / mean_ms, 4)}
+                 "frac_of_size_matched_copy": round(copy_ms[c.w.name] / med_ms, 4)}
         if plan_chain(c.w):
             entry["launch"] = mb.row_plan(plan_chain(c.w), c.w.dtype, c.w.rows, c.w.cols)
         if eager:
@@ -785,7 +803,7 @@ def run_ours(args):
     next_rows = None
     if not args.no_next:
         nxt = [Case(w, device, l2_bytes) for w in W.NEXT]
-        t_next = time_graph(nxt, lambda c, k: c.call(k), args.steps, args.warmup)
+        t_next = time_graph(nxt, lambda c, k: c.call(k), args.steps, args.warmup, replays)
         e_next = (time_graph(nxt, lambda c, k: c.eager(k), max(5, args.steps // 5), 2)
                   if not args.no_eager else None)
         cp_next = {}
@@ -795,9 +813,11 @@ def run_ours(args):
             del cc
         next_rows = {}
         for c in nxt:
-            ms = t_next[c.w.name]
+            mean_ms, ms, p10_ms, p90_ms = spread(t_next[c.w.name])
             gbs = c.ideal / (ms * 1e-3) / 1e9
-            ent = {"us_per_call": round(ms * 1e3, 3), "ideal_bytes": c.ideal,
+            ent = {"us_per_call": round(ms * 1e3, 3),
+                   "us_per_call_p10_p90": [round(p10_ms * 1e3, 3), round(p90_ms * 1e3, 3)],
+                   "us_per_call_mean": round(mean_ms * 1e3, 3), "ideal_bytes": c.ideal,
                    "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
                    "size_matched_copy_us": round(cp_next[c.w.name] * 1e3, 3),
                    "frac_of_size_matched_copy": round(cp_next[c.w.name] / ms, 4)}
@@ -825,7 +845,7 @@ def run_ours(args):
 
     dominant = max(cases, key=lambda c: per_kernel[c.w.name]["us_per_call"])
     dk = per_kernel[dominant.w.name]
-    achieved = dominant.ideal / (dk["us_per_call"] * 1e-6) / 1e9
+    achieved = dominant.ideal / (dk["us_per_call_mean"] * 1e-6) / 1e9   # average launch
     roofline = {"bound": "hbm", "kernel": dominant.w.name,
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -875,11 +895,28 @@ def run_ours(args):
                                    "D2H, each chain in 8 row chunks pipelined over 3 streams"}}
     if cpu:
         line["cpu_baseline"] = cpu
+    line["per_kernel_summary"] = kernel_summary(per_kernel, next_rows, hot_l2)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def kernel_summary(per_kernel, next_rows, hot_l2):
+    """Every measured kernel in a few characters each, printed as the last key
+    of the JSON line so that a reader keeping only the end of the line still
+    has them: per workload [median us/call, p10, p90, GB/s, fraction of the
+    measured HBM copy peak, fraction of a size-matched copy]."""
+    out = {"fields": ["us_median", "us_p10", "us_p90", "GB/s", "frac_of_measured_hbm",
+                      "frac_of_size_matched_copy"]}
+    for table in (per_kernel, next_rows or {}):
+        for name, e in table.items():
+            p10, p90 = e["us_per_call_p10_p90"]
+            out[name] = [e["us_per_call"], p10, p90, e["gbs"], e["frac_of_measured_hbm"],
+                         e["frac_of_size_matched_copy"]]
+    out["hot_l2_us_per_call"] = {k: v["us_per_call"] for k, v in hot_l2.items()}
+    return out
 
 
 # --------------------------------------------------------------------------
