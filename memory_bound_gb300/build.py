@@ -6,8 +6,10 @@ runtime linked statically (the library needs only the driver at run time).
 """
 import glob
 import os
+import shutil
 import subprocess
 import sys
+import tempfile
 from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,12 +33,13 @@ def _up_to_date():
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    deps = glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    deps = (glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+            + [os.path.abspath(__file__)])          # flags and arch live here
     return all(os.path.getmtime(p) <= t for p in deps)
 
 
-def _compile(src, verbose):
-    obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src, objdir, verbose):
+    obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
     cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
@@ -50,20 +53,29 @@ def build(force=False, verbose=False):
     """Compile every CUDA source and link the shared library; return its path."""
     if not force and _up_to_date():
         return LIB
+    # Objects go to a directory of this process's own and the library is
+    # linked to a file of its own, then renamed over the old one, so builds
+    # started at once by several processes never read each other's halves.
     os.makedirs(OBJDIR, exist_ok=True)
-    srcs = _sources()
-    with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    if verbose:
-        for _, log in results:
-            sys.stderr.write(log)
-    objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
-    cmd = [NVCC, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("link failed:\n" + res.stderr)
-    os.replace(tmp, LIB)
+    objdir = tempfile.mkdtemp(prefix="objs-", dir=OBJDIR)
+    tmp = f"{LIB}.tmp{os.getpid()}"
+    try:
+        srcs = _sources()
+        with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+            results = list(ex.map(lambda s: _compile(s, objdir, verbose), srcs))
+        if verbose:
+            for _, log in results:
+                sys.stderr.write(log)
+        objs = [o for o, _ in results]
+        cmd = [NVCC, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("link failed:\n" + res.stderr)
+        os.replace(tmp, LIB)
+    finally:
+        shutil.rmtree(objdir, ignore_errors=True)
+        if os.path.exists(tmp):
+            os.remove(tmp)
     return LIB
 
 

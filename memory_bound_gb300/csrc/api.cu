@@ -54,7 +54,8 @@ mb_status device_ctx(cudaStream_t stream, LaunchCtx *ctx) {
             return cuda_fail(e);
         d.ready = true;
     }
-    *ctx = LaunchCtx{stream, dev, d.sm_count, d.smem_optin, d.smem_per_sm, d.dev_err, g_pdl};
+    *ctx = LaunchCtx{stream, dev, d.sm_count, d.smem_optin, d.smem_per_sm, d.dev_err, g_pdl,
+                     g_tuning, g_pw_tuning};
     return MB_OK;
 }
 
@@ -115,6 +116,11 @@ mb_status cuda_fail(cudaError_t e) {
 }
 
 bool device_resident(const void *p) {
+    // The query fails for pointers the runtime does not know, and clearing
+    // that failure must not clear an error the calling thread already had
+    // pending: with one pending, the pointer is taken as not device memory
+    // (the plain-load paths serve any memory) and is not queried.
+    if (cudaPeekAtLastError() != cudaSuccess) return false;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         (void)cudaGetLastError();           // an unknown pointer is not an error here
@@ -152,7 +158,7 @@ mb_status fused_add_relu_scale(const void *x, const void *b1, const void *b2, vo
     LaunchCtx ctx;
     mb_status st = device_ctx(stream, &ctx);
     if (st != MB_OK) return st;
-    return add_relu_scale_run(ctx, g_pw_tuning, dtype, x, b1, b2, y, n, scale, vec, (int)head);
+    return add_relu_scale_run(ctx, ctx.pw, dtype, x, b1, b2, y, n, scale, vec, (int)head);
 }
 
 mb_status fused_add_relu_scale_bcast(const void *x, const void *b1, const void *b2, void *y,
@@ -208,7 +214,7 @@ mb_status fused_residual_layernorm_gelu(const void *x, const void *r, const void
         aligned = aligned && aligned_to(p, 16);
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
-    RowTuning tun = g_tuning;
+    RowTuning tun = ctx.tuning;
     if (dtype == MB_F32)
         return ln_gelu_rows_f32(ctx, tun, x, r, w, b, out, rows, (int)hidden, eps, aligned,
                                 nullptr, true);
@@ -239,7 +245,7 @@ mb_status fused_bias_relu_branch_mean_epilogue(const float *x, const float *bias
         aligned = aligned && aligned_to(p, 16);
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
-    return inductor_rows_f32(ctx, g_tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
+    return inductor_rows_f32(ctx, ctx.tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
                              branch_scale, aligned, nullptr, true);
 }
 
@@ -264,7 +270,7 @@ mb_status fused_bias_relu_branch_mean_epilogue_bf16(const void *x, const void *b
         aligned = aligned && aligned_to(p, 16);
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
-    return inductor_rows_bf16(ctx, g_tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
+    return inductor_rows_bf16(ctx, ctx.tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
                               branch_scale, aligned, nullptr, true);
 }
 
@@ -325,7 +331,7 @@ mb_status fused_layernorm_act_ex(const void *x, const void *r, const void *w, co
     const bool drop = p > 0.0f;
     auto fn = dtype == MB_F32 ? (drop ? lnact_drop_rows_f32 : lnact_rows_f32)
                               : (drop ? lnact_drop_rows_bf16 : lnact_rows_bf16);
-    return fn(ctx, g_tuning, r != nullptr, x, r, w, b, out, h_out, rows, (int)hidden, eps,
+    return fn(ctx, ctx.tuning, r != nullptr, x, r, w, b, out, h_out, rows, (int)hidden, eps,
               (int)act, ex, aligned, nullptr, true);
 }
 
@@ -343,7 +349,7 @@ mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols, 
     const bool aligned = aligned_to(x, 16) && aligned_to(y, 16);
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
-    return softmax_rows(ctx, g_tuning, dtype, x, y, rows, (int)cols, aligned, nullptr, true);
+    return softmax_rows(ctx, ctx.tuning, dtype, x, y, rows, (int)cols, aligned, nullptr, true);
 }
 
 mb_status fused_scale_mask_softmax(const void *x, void *y, int64_t rows, int64_t cols,
@@ -363,7 +369,7 @@ mb_status fused_scale_mask_softmax(const void *x, void *y, int64_t rows, int64_t
     const bool aligned = aligned_to(x, 16) && aligned_to(y, 16);
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
-    return softmax_mask_rows(ctx, g_tuning, dtype, x, y, rows, (int)cols, scale, causal != 0,
+    return softmax_mask_rows(ctx, ctx.tuning, dtype, x, y, rows, (int)cols, scale, causal != 0,
                              causal ? period : 1, causal ? offset : 0, aligned, nullptr, true);
 }
 
@@ -455,13 +461,13 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
     RowPlan p;
     const bool al = aligned != 0;
     if (chain == 1 && dtype == MB_F32)
-        st = inductor_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+        st = inductor_rows_f32(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                                (int)cols, 1.0f, 1.0f, al, &p, false);
     else if (chain == 1)
-        st = inductor_rows_bf16(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+        st = inductor_rows_bf16(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                                 (int)cols, 1.0f, 1.0f, al, &p, false);
     else if (chain == 2 || chain == 3 || chain == 7) {
-        RowTuning t = g_tuning;
+        RowTuning t = ctx.tuning;
         if (chain == 7) t.outs = 2;            // with the residual-stream output
         st = (dtype == MB_F32 ? lnact_rows_f32 : lnact_rows_bf16)(
             ctx, t, chain != 3, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
@@ -469,18 +475,18 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
     }
     else if (chain == 5 || chain == 6)
         st = (dtype == MB_F32 ? lnact_drop_rows_f32 : lnact_drop_rows_bf16)(
-            ctx, g_tuning, chain == 5, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+            ctx, ctx.tuning, chain == 5, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
             (int)cols, 0.0f, 0, LnExtras{}, al, &p, false);
     else if (chain == 4)
-        st = softmax_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, al, &p, false);
+        st = softmax_rows(ctx, ctx.tuning, dtype, nullptr, nullptr, rows, (int)cols, al, &p, false);
     else if (chain == 8)
-        st = softmax_mask_rows(ctx, g_tuning, dtype, nullptr, nullptr, rows, (int)cols, 1.0f,
+        st = softmax_mask_rows(ctx, ctx.tuning, dtype, nullptr, nullptr, rows, (int)cols, 1.0f,
                                true, cols, 0, al, &p, false);
     else if (dtype == MB_F32)
-        st = ln_gelu_rows_f32(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+        st = ln_gelu_rows_f32(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                               (int)cols, 0.0f, aligned != 0, &p, false);
     else
-        st = ln_gelu_rows_bf16(ctx, g_tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
+        st = ln_gelu_rows_bf16(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                                (int)cols, 0.0f, aligned != 0, &p, false);
     if (st != MB_OK) return st;
     out[0] = p.path; out[1] = p.threads; out[2] = p.ctas; out[3] = p.vpt;

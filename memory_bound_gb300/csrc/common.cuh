@@ -385,8 +385,6 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
-// of %globaltimer (or kWaitLimitPolls polls).  Returns false if it gave up.
 // Arrive on a local mbarrier and add `bytes` to the transaction count it
 // expects, with no release of this thread's earlier accesses (so loads and
 // stores still in flight do not have to land first).
@@ -409,6 +407,8 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
                  :: "r"(remote_addr), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
 }
 
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// of %globaltimer (or kWaitLimitPolls polls).  Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -9,26 +9,10 @@
 
 namespace mb {
 
-// What a launcher needs to know about the current device and stream.
-struct LaunchCtx {
-    cudaStream_t stream;
-    int device;
-    int sm_count;
-    int smem_optin;        // max dynamic shared memory per block (opt-in)
-    int smem_per_sm;       // shared memory per multiprocessor
-    unsigned *dev_err;     // device-side failure flags of this device
-    bool pdl;              // launch with programmatic stream serialisation
-};
-
 // Launch overlap pays for calls whose launch latency is a visible share of
 // their run time; above this many bytes moved it is noise (measured on GB300:
 // +-1%), so those launches keep plain stream order.
 constexpr int64_t kOverlapMaxBytes = 128ll << 20;
-
-// cudaLaunchKernel, or cudaLaunchKernelEx with programmatic stream
-// serialisation when ctx.pdl (the kernels wait for their predecessor).
-cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 block,
-                          void **args, size_t smem, int cluster = 1);
 
 // Process-wide row-chain override (mb_set_row_path).
 struct RowTuning {
@@ -50,6 +34,25 @@ struct PointwiseTuning {
     int blocks_per_sm;     // 0 = as many as fit
     int unroll;            // 16-byte fragments per input in flight per thread; 0 = 4
 };
+
+// What a launcher needs to know about the current device and stream, and
+// the process-wide overrides as they stood when the call began.
+struct LaunchCtx {
+    cudaStream_t stream;
+    int device;
+    int sm_count;
+    int smem_optin;        // max dynamic shared memory per block (opt-in)
+    int smem_per_sm;       // shared memory per multiprocessor
+    unsigned *dev_err;     // device-side failure flags of this device
+    bool pdl;              // launch with programmatic stream serialisation
+    RowTuning tuning;      // the row-chain override, read under the state lock
+    PointwiseTuning pw;    // the pointwise override, read under the state lock
+};
+
+// cudaLaunchKernel, or cudaLaunchKernelEx with programmatic stream
+// serialisation when ctx.pdl (the kernels wait for their predecessor).
+cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 block,
+                          void **args, size_t smem, int cluster = 1);
 
 // The launch a row chain uses (mb_row_plan reports it).
 struct RowPlan {

@@ -19,13 +19,16 @@ def build(src=None, out=None, quiet=True):
     """Compile ``src`` (default: oracle/oracle.c) into ``out``; return ``out``."""
     src = src or os.path.join(HERE, "oracle.c")
     out = out or DEFAULT_SO
-    cmd = ["gcc", *CFLAGS, "-I", HERE, src, "-o", out + ".tmp", "-lm"]
+    tmp = f"{out}.tmp{os.getpid()}"      # one file per process, renamed over the old
+    cmd = ["gcc", *CFLAGS, "-I", HERE, src, "-o", tmp, "-lm"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
+        if os.path.exists(tmp):
+            os.remove(tmp)
         raise RuntimeError("oracle build failed:\n" + res.stderr)
     if not quiet and res.stderr:
         print(res.stderr)
-    os.replace(out + ".tmp", out)
+    os.replace(tmp, out)
     return out
 
 
