@@ -88,6 +88,7 @@ template <typename TT> struct LnGeluChain {
     static constexpr int kVec = Elem<T>::kVec;   // elements per vector slot (16 bytes)
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
+    static constexpr int kWideScalarSlots = 32;   // see LnActChain
     // values per thread the cluster planner prefers for rows longer than a
     // CTA: 16 for fp32 (x, r, w and b held per value; 32 ran LN at 65536
     // columns 5% slower), 32 for bf16 rows (3% faster than 16)
@@ -169,6 +170,7 @@ template <typename TT> struct InductorChainT {
     static constexpr int kVec = Elem<T>::kVec;
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
+    static constexpr int kWideScalarSlots = 32;   // see LnActChain
     static constexpr int kClusterVals = 16;   // see LnGeluChain
     static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
@@ -278,6 +280,9 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     // the ordinary kernel.
     static constexpr bool kRegCap = DROP && sizeof(T) == 4;
     static constexpr int kRowsTarget = kRegCap ? 6 : 0;
+    // scalar slots per thread from which the one-CTA engine takes its
+    // 512-thread form (the 1024-thread one spills from there on)
+    static constexpr int kWideScalarSlots = DROP ? 16 : 32;
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;   // as LnGeluChain
     static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
@@ -380,6 +385,7 @@ template <typename TT> struct SoftmaxChain {
     static constexpr int kVec = Elem<T>::kVec;
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
+    static constexpr int kWideScalarSlots = 32;   // see LnActChain
     // one input and no per-column vectors: 32 values per thread on the
     // cluster path (softmax fp32 at 40000 columns 4.5% faster than 16)
     static constexpr int kClusterVals = 32;
@@ -472,6 +478,7 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     static constexpr int kVec = Elem<T>::kVec;
     static constexpr bool kRegCap = false;
     static constexpr int kRowsTarget = 0;
+    static constexpr int kWideScalarSlots = 32;   // see LnActChain
     // one input and no per-column vectors: 32 values per thread on the
     // cluster path (softmax fp32 at 40000 columns 4.5% faster than 16)
     static constexpr int kClusterVals = 32;

@@ -50,6 +50,11 @@ constexpr int kHdrBytes = 1024;   // reduction buffers, abort flags, mbarriers
 constexpr int kMaxStages = 16;
 constexpr int kMaxRowsInFlight = 8;  // resident CTAs per SM the planner aims for, at most
 constexpr int kCappedRegs = 40;   // registers per thread of rows_cta_kernel_capped
+// Local memory per thread (spilled registers) that the planners accept
+// without preferring another launch: a few bytes (a value kept across the row
+// loop, as in the two-slot bf16 LayerNorm kernel at 32 registers) cost nothing
+// measurable; the forms they pass over spill hundreds.
+constexpr size_t kSpillTolerance = 64;
 // Bytes of row reads and writes per SM in flight that keep HBM busy; the
 // planner aims for this many bytes' worth of resident rows, rounded to the
 // nearest row count (sweeps on GB300, fp32: LayerNorm rows of 48 KB in + out
@@ -327,6 +332,16 @@ __device__ __forceinline__ void rows_cta_body(const typename C::Args &a, int64_t
 template <class C, int VPT, int VEC, bool STAGED>
 __global__ void __launch_bounds__(kCtaMaxThreads)
 rows_cta_kernel(const typename C::Args a, int64_t rows, int cols, int nstage, unsigned *err) {
+    rows_cta_body<C, VPT, VEC, STAGED>(a, rows, cols, nstage, err);
+}
+
+// The same engine bounded at kWideThreads threads, so a thread may hold up to
+// 128 registers: the scalar (unaligned-row) forms with many slots per thread
+// (C::kWideScalarSlots), which spill under the 64 registers of the
+// 1024-thread bound.
+template <class C, int VPT, int VEC, bool STAGED>
+__global__ void __launch_bounds__(kWideThreads)
+rows_cta_kernel_wide(const typename C::Args a, int64_t rows, int cols, int nstage, unsigned *err) {
     rows_cta_body<C, VPT, VEC, STAGED>(a, rows, cols, nstage, err);
 }
 
@@ -798,10 +813,31 @@ template <class C> struct RowEngine {
     }
     // Vector slots per thread allowed on the CTA engine: VPT * VEC <= 32.
     static int max_vpt(bool vec) { return vec ? 32 / kVecN : 32; }
+    // A kernel's launch bound and whether it spills beyond kSpillTolerance.
+    static mb_status kernel_limits(const void *f, int *max_threads, bool *spills) {
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, f);
+        if (e != cudaSuccess) return cuda_fail(e);
+        *max_threads = fa.maxThreadsPerBlock;
+        *spills = fa.localSizeBytes > kSpillTolerance;
+        return MB_OK;
+    }
+    // Longest row (in vector slots) one CTA holds.
+    static int cta_max_nvec(bool vec) {
+        return vec ? kCtaMaxThreads * max_vpt(true)
+                   : (max_vpt(false) >= C::kWideScalarSlots ? kWideThreads : kCtaMaxThreads) *
+                         max_vpt(false);
+    }
     // The CTA engine's kernels: the register-capped form for chains that ask
-    // for it (C::kRegCap), the ordinary one otherwise.
+    // for it (C::kRegCap) on the staged vector shapes it was measured on (one
+    // or two slots; elsewhere the cap spills), the 512-thread form for the
+    // scalar slot counts that spill under the 1024-thread bound
+    // (C::kWideScalarSlots and up), the ordinary one otherwise.
     template <int VPT, int VEC, bool STAGED> static const void *cta_kernel() {
-        if constexpr (C::kRegCap) return (const void *)rows_cta_kernel_capped<C, VPT, VEC, STAGED>;
+        if constexpr (C::kRegCap && STAGED && VEC == kVecN && VPT <= 2)
+            return (const void *)rows_cta_kernel_capped<C, VPT, VEC, STAGED>;
+        else if constexpr (VEC == 1 && VPT >= C::kWideScalarSlots)
+            return (const void *)rows_cta_kernel_wide<C, VPT, VEC, STAGED>;
         else return (const void *)rows_cta_kernel<C, VPT, VEC, STAGED>;
     }
     static const void *cta_fn(int vpt, bool vec, bool staged) {
@@ -997,6 +1033,7 @@ template <class C> struct RowEngine {
         const int VEC = vec ? kVecN : 1;
         int best_n = 0, best_cs = 0, best_vpt = 0, best_threads = 0, best_slice = 0;
         int best_ring = 0, best_smem = 0;
+        bool best_spills = true;
         for (int cs0 : {2, 4, 8, 16}) {
             int cs = cs0;
             if (tun.stages >= 2 && tun.stages <= kMaxCluster) {
@@ -1032,18 +1069,25 @@ template <class C> struct RowEngine {
                 const int threads = round_up32(ceil_div(slice_v, vpt));
                 const void *f = cluster_fn(vpt, vec, ring > 0, threads);
                 if (!f) continue;
-                cudaFuncAttributes fa;
-                const cudaError_t fe = cudaFuncGetAttributes(&fa, f);
-                if (fe != cudaSuccess) return cuda_fail(fe);
-                if (threads > fa.maxThreadsPerBlock) continue;    // the kernel's launch bound
-                int n = 0;
-                mb_status st = active_clusters(ctx, f, cs, threads, smem, &n);
+                int max_threads = 0;
+                bool spills = false;
+                mb_status st = kernel_limits(f, &max_threads, &spills);
                 if (st != MB_OK) return st;
-                // ties keep the smaller cluster (fewer exchange partners), and
-                // within it the more values per thread (fewer, busier threads)
-                if (n > best_n || (n > 0 && n == best_n && cs == best_cs)) {
+                if (threads > max_threads) continue;    // the kernel's launch bound
+                int n = 0;
+                st = active_clusters(ctx, f, cs, threads, smem, &n);
+                if (st != MB_OK) return st;
+                // a spilling kernel only when no other serves; ties keep the
+                // smaller cluster (fewer exchange partners), and within it the
+                // more values per thread (fewer, busier threads)
+                const bool better =
+                    n > 0 && (best_n == 0 || (best_spills && !spills) ||
+                              (spills == best_spills &&
+                               (n > best_n || (n == best_n && cs == best_cs))));
+                if (better) {
                     best_n = n; best_cs = cs; best_vpt = vpt; best_threads = threads;
                     best_slice = slice_v; best_ring = ring; best_smem = smem;
+                    best_spills = spills;
                 }
             }
         }
@@ -1160,21 +1204,31 @@ template <class C> struct RowEngine {
         const int stage_bytes = C::kInputs * cols * (int)sizeof(T);
         const bool stage_fits = !tun.no_bulk && kHdrBytes + stage_bytes <= ctx.smem_optin;
 
-        const bool one_cta = nvec <= kCtaMaxThreads * max_vpt(vec);
+        const bool one_cta = nvec <= cta_max_nvec(vec);
+        int warp_vpl = 1;
+        while (warp_vpl * 32 < nvec) warp_vpl *= 2;
+        bool warp_spills = false;
+        if (warp_ok) {
+            int max_threads = 0;
+            mb_status st = kernel_limits(warp_fn(warp_vpl, vec), &max_threads, &warp_spills);
+            if (st != MB_OK) return st;
+        }
         int path = tun.path;
         if (path == MB_ROW_WARP && !warp_ok) path = MB_ROW_AUTO;
         if (path == MB_ROW_STAGED && (!vec || !stage_fits || !one_cta)) path = MB_ROW_AUTO;
         if (path == MB_ROW_DIRECT && !one_cta) path = MB_ROW_AUTO;
         if (path == MB_ROW_CLUSTER && nvec < 2) path = MB_ROW_AUTO;
+        // one warp per row unless its kernel for this length spills (the
+        // dropout chains' longest warp rows); then one CTA per row
         if (path == MB_ROW_AUTO)
             path = !one_cta ? MB_ROW_CLUSTER
-                 : warp_ok ? MB_ROW_WARP : (vec && stage_fits ? MB_ROW_STAGED : MB_ROW_DIRECT);
+                 : warp_ok && !warp_spills ? MB_ROW_WARP
+                 : (vec && stage_fits ? MB_ROW_STAGED : MB_ROW_DIRECT);
 
         p->vec = VEC;
         if (path == MB_ROW_CLUSTER) return plan_cluster(ctx, tun, rows, nvec, vec, p, fn);
         if (path == MB_ROW_WARP) {
-            int vpl = 1;
-            while (vpl * 32 < nvec) vpl *= 2;
+            const int vpl = warp_vpl;
             *fn = warp_fn(vpl, vec);
             int occ = 0;
             mb_status st = occupancy(ctx, *fn, kWarpBlock, 0, &occ);
@@ -1217,25 +1271,36 @@ template <class C> struct RowEngine {
         int target = want_rows < 2 ? 2 : (int)want_rows;
         if (C::kRowsTarget > 0) target = C::kRowsTarget;     // the chain's own measured target
         int best_vpt = 0, best_occ = 0, best_threads = 0;
+        bool best_spills = true;
         for (int cand = 1; cand <= max_vpt(vec); cand *= 2) {
             if (tun.vpt > 0 && cand != tun.vpt) continue;
             if (ceil_div(nvec, cand) > kCtaMaxThreads) continue;
             const int threads = round_up32(ceil_div(nvec, cand));
             const void *f = cta_fn(cand, vec, staged);
             if (!f) continue;
+            int max_threads = 0;
+            bool spills = false;
+            mb_status st = kernel_limits(f, &max_threads, &spills);
+            if (st != MB_OK) return st;
+            if (threads > max_threads) continue;          // the kernel's launch bound
             int occ = 0;
-            mb_status st = occupancy(ctx, f, threads, smem1, &occ);
+            st = occupancy(ctx, f, threads, smem1, &occ);
             if (st != MB_OK) return st;
             if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
             if (occ < 1) continue;
             const int rows_in_flight = occ < target ? occ : target;
             const int best_rows = best_occ < target ? best_occ : target;
-            // tie-break on threads per SM, counting the CTAs that will be
-            // resident once the target caps them
-            if (rows_in_flight > best_rows ||
-                (rows_in_flight == best_rows &&
-                 rows_in_flight * threads > best_rows * best_threads)) {
-                best_vpt = cand; best_occ = occ; best_threads = threads;
+            // a spilling kernel only when no other serves; then the most rows
+            // in flight, tie-broken on threads per SM, counting the CTAs that
+            // will be resident once the target caps them
+            const bool better =
+                best_vpt == 0 || (best_spills && !spills) ||
+                (spills == best_spills &&
+                 (rows_in_flight > best_rows ||
+                  (rows_in_flight == best_rows &&
+                   rows_in_flight * threads > best_rows * best_threads)));
+            if (better) {
+                best_vpt = cand; best_occ = occ; best_threads = threads; best_spills = spills;
             }
         }
         if (tun.ctas_per_sm <= 0 && best_occ > target) best_occ = target;

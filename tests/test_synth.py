@@ -99,5 +99,6 @@ def test_workload_ideal_bytes(w):
         "pointwise_bcast_f32_4096x1024": 2 * 4096 * 1024 * 4 + 2 * 1024 * 4,
         # 32 heads x (1 + 2 + ... + 4096) unmasked keys read, every output written
         "softmax_scale_causal_f32_131072x4096": (32 * 4096 * 4097 // 2 + 131072 * 4096) * 4,
+        "ln_gelu_f32_8192x4099": 3 * 8192 * 4099 * 4 + 2 * 4099 * 4,
     }[w.name]
     assert w.ideal_bytes() == want
