@@ -294,7 +294,7 @@ class CopyCase:
         import torch
         from types import SimpleNamespace
         self.w = SimpleNamespace(name=case.w.name)
-        n = case.ideal // 2 // 4
+        n = (case.ideal // 2 // 4) & ~3      # whole 16-byte vectors: torch's vector copy path
         self.src = [torch.ones(n, dtype=torch.float32, device=device) for _ in range(case.nsets)]
         self.dst = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(case.nsets)]
 
