@@ -46,7 +46,15 @@
  *   Alignment   Every pointer must be aligned to its element size, else
  *               MB_ERR_ALIGN.  Pointers that are 16-byte aligned (and rows
  *               whose byte length is a multiple of 16) take the vectorised
- *               paths; anything else still runs, on a scalar path.
+ *               paths.  Row chains whose rows are off that grid (a row
+ *               length that is not a whole number of 16-byte vectors, or
+ *               row tensors starting off a 16-byte boundary) still take
+ *               16-byte row accesses when all row tensors of the call (row
+ *               inputs and outputs) start at the same offset within 16
+ *               bytes and a row holds one CTA's worth or less (except with
+ *               dropout): each row is then read as a short head, whole
+ *               vectors and a short tail.  Anything else runs on a scalar
+ *               path.
  *   Aliasing    The output may not overlap any input (MB_ERR_OVERLAP).
  *               Inputs may overlap one another.
  *   Sizes       Zero rows / zero elements is a no-op returning MB_OK without
@@ -400,7 +408,11 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * a residual, without), 7 the LayerNorm family with a residual that also
  * writes the residual stream h, 8 the scaled softmax under a square causal
  * mask (period = cols, offset 0: row i reads keys 0 .. i mod cols).
- * `aligned` says whether every pointer is 16-byte aligned.  Queries the current device (SM count, shared memory).
+ * `aligned`: 1 every pointer is 16-byte aligned; 2 the row tensors start at
+ * one common offset within 16 bytes (per-column vectors anywhere); 0 neither;
+ * else MB_ERR_VALUE.  Rows planned on shifted vectors report path
+ * MB_ROW_DIRECT with the vector width in out[4] while cols is not a multiple
+ * of it.  Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,
                       int aligned, int32_t out[7]);

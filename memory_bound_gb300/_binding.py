@@ -389,13 +389,16 @@ def row_plan(chain, dtype, rows, cols, aligned=True):
     stages, smem).  chain: "ln", "inductor", "lnact_res", "lnact", "softmax",
     "lnact_res_dropout", "lnact_dropout", "lnact_res_h" (with the
     residual-stream output) or "softmax_mask" (the scaled softmax under a square
-    causal mask: period = cols, offset 0); dtype: "f32" or "bf16"."""
+    causal mask: period = cols, offset 0); dtype: "f32" or "bf16"; aligned:
+    True / 1 every pointer 16-byte aligned, 2 the row tensors at one common
+    offset within 16 bytes, False / 0 neither."""
     out = (ctypes.c_int32 * 7)()
     code = {"ln": 0, "inductor": 1, "lnact_res": 2, "lnact": 3, "softmax": 4,
             "lnact_res_dropout": 5, "lnact_dropout": 6, "lnact_res_h": 7,
             "softmax_mask": 8}[chain]
     dt = {"f32": MB_F32, "bf16": MB_BF16}[dtype]
-    st = load_library().mb_row_plan(code, dt, rows, cols, int(bool(aligned)), out)
+    al = int(aligned)
+    st = load_library().mb_row_plan(code, dt, rows, cols, al, out)
     _check("mb_row_plan", st)
     keys = ("path", "threads", "ctas", "vpt", "vec", "stages", "smem")
     d = dict(zip(keys, list(out)))

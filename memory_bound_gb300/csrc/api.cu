@@ -2,6 +2,7 @@
 // state, dispatch to the kernels, status reporting.
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -72,6 +73,25 @@ inline bool aligned_to(const void *p, uintptr_t a) { return (addr(p) & (a - 1)) 
 inline int elem_size(mb_dtype d) { return d == MB_BF16 ? 2 : 4; }
 
 bool valid_dtype(mb_dtype d) { return d == MB_F32 || d == MB_BF16; }
+
+// Alignment class of a row-chain call (the row engines' `aligned`): 1 when
+// every pointer is 16-byte aligned; 2 when every row tensor (the row inputs
+// and outputs, NULLs skipped) starts at the same offset within 16 bytes and
+// the per-column vectors are anywhere; 0 otherwise.
+int align_class(std::initializer_list<const void *> row_tensors,
+                std::initializer_list<const void *> col_vectors) {
+    bool all16 = true, same = true;
+    int phase = -1;
+    for (const void *p : row_tensors) {
+        if (!p) continue;
+        const int ph = (int)(addr(p) & 15u);
+        all16 = all16 && ph == 0;
+        if (phase < 0) phase = ph;
+        same = same && ph == phase;
+    }
+    for (const void *p : col_vectors) all16 = all16 && aligned_to(p, 16);
+    return all16 ? 1 : (same ? 2 : 0);
+}
 
 // Row-length check shared by the row chains.
 mb_status check_rows(int64_t rows, int64_t cols) {
@@ -209,9 +229,7 @@ mb_status fused_residual_layernorm_gelu(const void *x, const void *r, const void
     if (overlaps(out, big, x, big) || overlaps(out, big, r, big) ||
         overlaps(out, big, w, small) || overlaps(out, big, b, small))
         return MB_ERR_OVERLAP;
-    bool aligned = true;
-    for (const void *p : {x, r, w, b, static_cast<const void *>(out)})
-        aligned = aligned && aligned_to(p, 16);
+    const int aligned = align_class({x, r, out}, {w, b});
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
     RowTuning tun = ctx.tuning;
@@ -239,10 +257,7 @@ mb_status fused_bias_relu_branch_mean_epilogue(const float *x, const float *bias
     if (overlaps(y, big, x, big) || overlaps(y, big, bias, small) ||
         overlaps(y, big, gamma, small) || overlaps(y, big, beta, small))
         return MB_ERR_OVERLAP;
-    bool aligned = true;
-    for (const void *p : {(const void *)x, (const void *)bias, (const void *)gamma,
-                          (const void *)beta, (const void *)y})
-        aligned = aligned && aligned_to(p, 16);
+    const int aligned = align_class({x, y}, {bias, gamma, beta});
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
     return inductor_rows_f32(ctx, ctx.tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
@@ -265,9 +280,7 @@ mb_status fused_bias_relu_branch_mean_epilogue_bf16(const void *x, const void *b
     if (overlaps(y, big, x, big) || overlaps(y, big, bias, small) ||
         overlaps(y, big, gamma, small) || overlaps(y, big, beta, small))
         return MB_ERR_OVERLAP;
-    bool aligned = true;
-    for (const void *p : {x, bias, gamma, beta, static_cast<const void *>(y)})
-        aligned = aligned && aligned_to(p, 16);
+    const int aligned = align_class({x, y}, {bias, gamma, beta});
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
     return inductor_rows_bf16(ctx, ctx.tuning, x, bias, gamma, beta, y, rows, (int)cols, x_scale,
@@ -316,10 +329,7 @@ mb_status fused_layernorm_act_ex(const void *x, const void *r, const void *w, co
         for (int j = i + 1; j < 4; ++j)
             if (outs[j] && overlaps(o, n, outs[j], out_bytes[j])) return MB_ERR_OVERLAP;
     }
-    bool aligned = true;
-    for (const void *q : {x, r, w, b, static_cast<const void *>(out),
-                          static_cast<const void *>(h_out)})
-        aligned = aligned && (!q || aligned_to(q, 16));
+    const int aligned = align_class({x, r, out, h_out}, {w, b});
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
     LnExtras ex;
@@ -346,7 +356,7 @@ mb_status fused_row_softmax(const void *x, void *y, int64_t rows, int64_t cols, 
     if (!aligned_to(x, es) || !aligned_to(y, es)) return MB_ERR_ALIGN;
     const int64_t big = rows * cols * es;
     if (overlaps(y, big, x, big)) return MB_ERR_OVERLAP;
-    const bool aligned = aligned_to(x, 16) && aligned_to(y, 16);
+    const int aligned = align_class({x, y}, {});
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
     return softmax_rows(ctx, ctx.tuning, dtype, x, y, rows, (int)cols, aligned, nullptr, true);
@@ -366,7 +376,7 @@ mb_status fused_scale_mask_softmax(const void *x, void *y, int64_t rows, int64_t
     if (!aligned_to(x, es) || !aligned_to(y, es)) return MB_ERR_ALIGN;
     const int64_t big = rows * cols * es;
     if (overlaps(y, big, x, big)) return MB_ERR_OVERLAP;
-    const bool aligned = aligned_to(x, 16) && aligned_to(y, 16);
+    const int aligned = align_class({x, y}, {});
     LaunchCtx ctx;
     if ((st = device_ctx(stream, &ctx)) != MB_OK) return st;
     return softmax_mask_rows(ctx, ctx.tuning, dtype, x, y, rows, (int)cols, scale, causal != 0,
@@ -458,8 +468,9 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
     if (st != MB_OK) return st;
     LaunchCtx ctx;
     if ((st = device_ctx(0, &ctx)) != MB_OK) return st;
+    if (aligned < 0 || aligned > 2) return MB_ERR_VALUE;
     RowPlan p;
-    const bool al = aligned != 0;
+    const int al = aligned;
     if (chain == 1 && dtype == MB_F32)
         st = inductor_rows_f32(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
                                (int)cols, 1.0f, 1.0f, al, &p, false);
@@ -484,10 +495,10 @@ mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int
                                true, cols, 0, al, &p, false);
     else if (dtype == MB_F32)
         st = ln_gelu_rows_f32(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
-                              (int)cols, 0.0f, aligned != 0, &p, false);
+                              (int)cols, 0.0f, al, &p, false);
     else
         st = ln_gelu_rows_bf16(ctx, ctx.tuning, nullptr, nullptr, nullptr, nullptr, nullptr, rows,
-                               (int)cols, 0.0f, aligned != 0, &p, false);
+                               (int)cols, 0.0f, al, &p, false);
     if (st != MB_OK) return st;
     out[0] = p.path; out[1] = p.threads; out[2] = p.ctas; out[3] = p.vpt;
     out[4] = p.vec; out[5] = p.stages; out[6] = p.smem;

@@ -89,6 +89,7 @@ template <typename TT> struct LnGeluChain {
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
     static constexpr int kWideScalarSlots = 32;   // see LnActChain
+    static constexpr bool kShiftOk = true;        // see LnActChain
     // values per thread the cluster planner prefers for rows longer than a
     // CTA: 16 for fp32 (x, r, w and b held per value; 32 ran LN at 65536
     // columns 5% slower), 32 for bf16 rows (3% faster than 16)
@@ -113,12 +114,12 @@ template <typename TT> struct LnGeluChain {
     template <int VEC> using Early = NoEarly;
     template <int VEC>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
-        pc.w.load_cached(a.w + col);
-        pc.b.load_cached(a.b + col);
+        pc.w.template load_cached_as<AL>(a.w + col);
+        pc.b.template load_cached_as<AL>(a.b + col);
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[2], const PrePC<VEC> &,
@@ -171,6 +172,7 @@ template <typename TT> struct InductorChainT {
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
     static constexpr int kWideScalarSlots = 32;   // see LnActChain
+    static constexpr bool kShiftOk = true;        // see LnActChain
     static constexpr int kClusterVals = 16;   // see LnGeluChain
     static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
@@ -193,14 +195,14 @@ template <typename TT> struct InductorChainT {
     template <int VEC> using Early = NoEarly;
     template <int VEC>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc) {
-        pc.bias.load_cached(a.bias + col);
+        pc.bias.template load_cached_as<AL>(a.bias + col);
     }
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
-        pc.gamma.load_cached(a.gamma + col);
-        pc.beta.load_cached(a.beta + col);
+        pc.gamma.template load_cached_as<AL>(a.gamma + col);
+        pc.beta.template load_cached_as<AL>(a.beta + col);
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1],
@@ -283,6 +285,10 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     // scalar slots per thread from which the one-CTA engine takes its
     // 512-thread form (the 1024-thread one spills from there on)
     static constexpr int kWideScalarSlots = DROP ? 16 : 32;
+    // rows off the 16-byte grid may take the shifted-vector engine; dropout
+    // needs each slot to start at a multiple of 8 elements, so it keeps the
+    // scalar one
+    static constexpr bool kShiftOk = !DROP;
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;   // as LnGeluChain
     static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
@@ -313,12 +319,12 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     __device__ __forceinline__ static void early(const Args &a, int64_t off, Early<VEC> &e) {
         if constexpr (DROP) dropout_bits<VEC>(off, a.drop, e.bits);
     }
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
-        pc.w.load_cached(a.w + col);
-        pc.b.load_cached(a.b + col);
+        pc.w.template load_cached_as<AL>(a.w + col);
+        pc.b.template load_cached_as<AL>(a.b + col);
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[kInputs],
@@ -386,6 +392,7 @@ template <typename TT> struct SoftmaxChain {
     static constexpr bool kRegCap = false;     // see LnActChain
     static constexpr int kRowsTarget = 0;
     static constexpr int kWideScalarSlots = 32;   // see LnActChain
+    static constexpr bool kShiftOk = true;        // see LnActChain
     // one input and no per-column vectors: 32 values per thread on the
     // cluster path (softmax fp32 at 40000 columns 4.5% faster than 16)
     static constexpr int kClusterVals = 32;
@@ -408,9 +415,9 @@ template <typename TT> struct SoftmaxChain {
     template <int VEC> using Early = NoEarly;
     template <int VEC>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1], const PrePC<VEC> &,
@@ -479,6 +486,7 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     static constexpr bool kRegCap = false;
     static constexpr int kRowsTarget = 0;
     static constexpr int kWideScalarSlots = 32;   // see LnActChain
+    static constexpr bool kShiftOk = true;        // see LnActChain
     // one input and no per-column vectors: 32 values per thread on the
     // cluster path (softmax fp32 at 40000 columns 4.5% faster than 16)
     static constexpr int kClusterVals = 32;
@@ -508,9 +516,9 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     template <int VEC> using Early = NoEarly;
     template <int VEC>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC>
+    template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
     // row mod period: on the device a multiply-high by the reciprocal gives
     // the quotient or one less (the reciprocal is rounded down and the row is

@@ -279,6 +279,16 @@ template <typename T, int VEC> struct Frag {
                 unpack(__ldg(reinterpret_cast<const uint4 *>(p) + q), q);
         }
     }
+    // the cached load element by element, for per-column values whose
+    // columns do not start on a 16-byte boundary
+    __device__ __forceinline__ void load_cached_elems(const T *p) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = to_f(__ldg(p + e));
+    }
+    // load_cached when AL (16-byte aligned columns), else load_cached_elems
+    template <bool AL> __device__ __forceinline__ void load_cached_as(const T *p) {
+        if constexpr (AL) load_cached(p); else load_cached_elems(p);
+    }
     __device__ __forceinline__ void load_shared(const T *p) {
         if constexpr (VEC == 1) {
             f[0] = to_f(*p);

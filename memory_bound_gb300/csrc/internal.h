@@ -58,6 +58,7 @@ cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 
 struct RowPlan {
     int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
     int slice = 0;     // cluster path: vectors of the row each CTA holds
+    int shift = 0;     // one-CTA path on rows off the 16-byte grid (shifted vectors)
     int ring = 0;      // cluster path: staging ring depth (0: direct loads)
     int64_t cap = 0;   // CTAs (warp/CTA paths, at 256 threads for warp) or clusters resident at once
 };
@@ -76,21 +77,21 @@ mb_status add_relu_scale_bcast_run(const LaunchCtx &ctx, mb_dtype dtype, const v
 
 mb_status ln_gelu_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                            const void *r, const void *w, const void *b, void *out,
-                           int64_t rows, int cols, float eps, bool aligned,
+                           int64_t rows, int cols, float eps, int aligned,
                            RowPlan *plan, bool launch);
 mb_status ln_gelu_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                             const void *r, const void *w, const void *b, void *out,
-                            int64_t rows, int cols, float eps, bool aligned,
+                            int64_t rows, int cols, float eps, int aligned,
                             RowPlan *plan, bool launch);
 mb_status inductor_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, const float *x,
                             const float *bias, const float *gamma, const float *beta,
                             float *y, int64_t rows, int cols, float x_scale,
-                            float branch_scale, bool aligned, RowPlan *plan, bool launch);
+                            float branch_scale, int aligned, RowPlan *plan, bool launch);
 
 mb_status inductor_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                              const void *bias, const void *gamma, const void *beta, void *y,
                              int64_t rows, int cols, float x_scale, float branch_scale,
-                             bool aligned, RowPlan *plan, bool launch);
+                             int aligned, RowPlan *plan, bool launch);
 // Optional extras of the LayerNorm family: per-row statistics out (NULL: not
 // written) and dropout with probability p (0: none) keyed by (seed, offset).
 struct LnExtras {
@@ -107,7 +108,7 @@ struct LnExtras {
     mb_status name(const LaunchCtx &ctx, const RowTuning &tun, bool residual, const void *x, \
                    const void *r, const void *w, const void *b, void *out, void *h,          \
                    int64_t rows, int cols, float eps, int act, const LnExtras &ex,           \
-                   bool aligned, RowPlan *plan, bool launch)
+                   int aligned, RowPlan *plan, bool launch)
 MB_LNACT_DECL(lnact_rows_f32);
 MB_LNACT_DECL(lnact_rows_bf16);
 MB_LNACT_DECL(lnact_drop_rows_f32);
@@ -115,10 +116,10 @@ MB_LNACT_DECL(lnact_drop_rows_bf16);
 #undef MB_LNACT_DECL
 mb_status softmax_mask_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
                             const void *x, void *y, int64_t rows, int cols, float scale,
-                            bool causal, int64_t period, int64_t offset, bool aligned,
+                            bool causal, int64_t period, int64_t offset, int aligned,
                             RowPlan *plan, bool launch);
 mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
-                       const void *x, void *y, int64_t rows, int cols, bool aligned,
+                       const void *x, void *y, int64_t rows, int cols, int aligned,
                        RowPlan *plan, bool launch);
 
 mb_status selftest_wait_timeout(const LaunchCtx &ctx, uint32_t limit_us);

@@ -32,7 +32,7 @@ template <typename T, bool DROP>
 mb_status lnact_run(const LaunchCtx &ctx, const RowTuning &tun, bool residual, const void *x,
                     const void *r, const void *w, const void *b, void *out, void *h,
                     int64_t rows, int cols, float eps, int act, const LnExtras &ex,
-                    bool aligned, RowPlan *plan, bool launch) {
+                    int aligned, RowPlan *plan, bool launch) {
     auto fill = [&](auto &a) {
         a.w = static_cast<const T *>(w);
         a.b = static_cast<const T *>(b);

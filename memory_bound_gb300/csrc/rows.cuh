@@ -354,6 +354,145 @@ rows_cta_kernel_capped(const typename C::Args a, int64_t rows, int cols, int nst
 }
 
 // ---------------------------------------------------------------------------
+// one CTA per row, rows off the 16-byte grid (shifted vectors)
+// ---------------------------------------------------------------------------
+// Rows whose length is not a whole number of vectors, or whose tensors do not
+// start on a 16-byte boundary, when every row tensor (inputs, outputs) starts
+// at the same offset m0 within 16 bytes: each row splits into a head of h <
+// VEC elements up to its first 16-byte boundary, whole vectors from there,
+// and a tail of fewer than VEC elements.  The vectors take the vector hooks
+// with 16-byte row accesses and their per-column values loaded element by
+// element (those columns are off the grid); the head and tail elements take
+// the scalar hooks, one element per thread.  Persistent over rows like
+// rows_cta_kernel's direct path; the host guarantees cols >= 2 * VEC, so every
+// row holds at least one whole vector.
+template <class C, int VPT>
+__global__ void __launch_bounds__(kCtaMaxThreads)
+rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsigned *) {
+    using T = typename C::T;
+    constexpr int VEC = C::kVec;
+    constexpr int NIN = C::kInputs;
+    constexpr int ES = (int)sizeof(T);
+    constexpr bool kEarlyPost = VPT * VEC * C::kPostPC <= 8;
+    using PrePC = typename C::template PrePC<VEC>;
+    using PostPC = typename C::template PostPC<VEC>;
+    using PrePC1 = typename C::template PrePC<1>;
+    using PostPC1 = typename C::template PostPC<1>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float *red = reinterpret_cast<float *>(smem);                  // [2][32]
+    const int tid = threadIdx.x;
+    const int T_ = (int)blockDim.x;
+    const int64_t G = gridDim.x;
+    pdl_wait();
+    pdl_launch_dependents();
+    int rb = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += G) {
+        const int64_t base = row * cols;
+        // the row's first element sits `off` bytes past a 16-byte boundary
+        const int off = (int)(((uint64_t)m0 + (uint64_t)base * (uint64_t)ES) & 15u);
+        const int h = ((16 - off) & 15) / ES;                  // head elements
+        const int nb = (cols - h) / VEC;                       // whole vectors (>= 1)
+        const int ne = cols - nb * VEC;                        // head + tail elements
+        const int ext = C::kPartialRows ? C::row_extent(a, row, cols) : cols;
+        const bool has_e = tid < ne;
+        const int col_e = tid < h ? tid : h + nb * VEC + (tid - h);
+        const int64_t vbase = base + h;                        // first whole vector
+
+        // every load before any use; vector slots past the row's last vector
+        // re-read it (in bounds) and are masked below
+        PrePC pre[VPT];
+        PostPC post[kEarlyPost ? VPT : 1];
+        Frag<T, VEC> in[VPT][NIN];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vc = min(tid + k * T_, nb - 1);
+            C::template load_pre<VEC, false>(a, h + vc * VEC, pre[k]);
+            if constexpr (kEarlyPost) C::template load_post<VEC, false>(a, h + vc * VEC, post[k]);
+#pragma unroll
+            for (int i = 0; i < NIN; ++i)
+                in[k][i].load_stream_if(a.in[i] + vbase + (int64_t)vc * VEC,
+                                        !C::kPartialRows || h + vc * VEC < ext);
+        }
+        PrePC1 pre_e;
+        PostPC1 post_e;
+        Frag<T, 1> in_e[NIN];
+        if (has_e) {
+            C::template load_pre<1>(a, col_e, pre_e);
+            C::template load_post<1>(a, col_e, post_e);
+#pragma unroll
+            for (int i = 0; i < NIN; ++i)
+                in_e[i].load_stream_if(a.in[i] + base + col_e, !C::kPartialRows || col_e < ext);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) in_e[i].f[0] = 0.0f;
+        }
+        typename C::template Early<VEC> ea[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            C::template early<VEC>(a, vbase + (int64_t)min(tid + k * T_, nb - 1) * VEC, ea[k]);
+        typename C::template Early<1> ea_e;
+        C::template early<1>(a, base + (has_e ? col_e : 0), ea_e);
+
+        float v[VPT][VEC];
+        float ve[1];
+        float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vi = tid + k * T_;
+            C::template pre<VEC>(in[k], pre[k], a, row, h + vi * VEC, v[k]);
+            l1 = fold1<C, VEC>(l1, v[k], vi < nb);
+            if constexpr (C::kStorePre) {
+                if (vi < nb) C::template store_pre<VEC>(v[k], a, vbase + (int64_t)vi * VEC);
+            }
+        }
+        C::template pre<1>(in_e, pre_e, a, row, has_e ? col_e : 0, ve);
+        l1 = fold1<C, 1>(l1, ve, has_e);
+        if constexpr (C::kStorePre) {
+            if (has_e) C::template store_pre<1>(ve, a, base + col_e);
+        }
+        const float r1 = C::kMaxFirst ? block_max(l1, red + 32 * rb) : block_sum(l1, red + 32 * rb);
+        rb ^= 1;
+        const float mean = C::stat1(r1, cols, a);
+        float rstd = 0.0f;
+        if constexpr (C::kTwoPass) {
+            float l2 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const float part = C::template p2<VEC>(v[k], mean);
+                l2 += tid + k * T_ < nb ? part : 0.0f;
+            }
+            const float part_e = C::template p2<1>(ve, mean);
+            l2 += has_e ? part_e : 0.0f;
+            rstd = C::stat2(block_sum(l2, red + 32 * rb), cols, a);
+            rb ^= 1;
+        }
+        if (tid == 0) C::store_stats(a, row, mean, rstd);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int vi = tid + k * T_;
+            if (vi < nb) {
+                Frag<T, VEC> o;
+                if constexpr (kEarlyPost) {
+                    C::template post<VEC>(v[k], mean, rstd, post[k], a, vbase + (int64_t)vi * VEC,
+                                          ea[k], o.f);
+                } else {
+                    PostPC pc;
+                    C::template load_post<VEC, false>(a, h + vi * VEC, pc);
+                    C::template post<VEC>(v[k], mean, rstd, pc, a, vbase + (int64_t)vi * VEC,
+                                          ea[k], o.f);
+                }
+                o.store_stream(a.out + vbase + (int64_t)vi * VEC);
+            }
+        }
+        if (has_e) {
+            Frag<T, 1> o;
+            C::template post<1>(ve, mean, rstd, post_e, a, base + col_e, ea_e, o.f);
+            o.store_stream(a.out + base + col_e);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // one thread-block cluster per row (rows longer than one CTA can hold)
 // ---------------------------------------------------------------------------
 
@@ -872,6 +1011,20 @@ template <class C> struct RowEngine {
         return nullptr;
     }
 
+    // The shifted-vector kernel (rows off the 16-byte grid), vpt vector slots.
+    static const void *shift_fn(int vpt) {
+        if constexpr (C::kShiftOk) {
+            switch (vpt) {
+                case 1: return (const void *)rows_shift_kernel<C, 1>;
+                case 2: return (const void *)rows_shift_kernel<C, 2>;
+                case 4: return (const void *)rows_shift_kernel<C, 4>;
+                case 8: if constexpr (kVecN == 4) return (const void *)rows_shift_kernel<C, 8>;
+                        break;
+            }
+        }
+        return nullptr;
+    }
+
     // The cluster kernel for a launch of `threads` threads: the 512-thread
     // form for 32 or more values per thread when the CTA fits it, else the
     // 1024-thread form.
@@ -1139,7 +1292,7 @@ template <class C> struct RowEngine {
     }
 
     static mb_status plan(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows, int cols,
-                          bool aligned, RowPlan *p, const void **fn) {
+                          int aligned, RowPlan *p, const void **fn) {
         RowPlan core;
         const void *f = nullptr;
         bool hit = false;
@@ -1195,16 +1348,24 @@ template <class C> struct RowEngine {
         return MB_OK;
     }
 
+    // `aligned`: 1 every pointer of the call is 16-byte aligned; 2 every row
+    // tensor (inputs and outputs) starts at the same offset within 16 bytes,
+    // the per-column vectors anywhere; 0 neither.
     static mb_status plan_full(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows, int cols,
-                               bool aligned, RowPlan *p, const void **fn) {
-        const bool vec = aligned && (cols % kVecN) == 0;
+                               int aligned, RowPlan *p, const void **fn) {
+        const bool vec = aligned == 1 && (cols % kVecN) == 0;
+        // rows off the 16-byte grid whose tensors share their offset within
+        // 16 bytes: shifted vectors on one CTA (at least one whole vector a row)
+        const bool shift_ok = !vec && aligned >= 1 && C::kShiftOk && cols >= 2 * kVecN;
         const int VEC = vec ? kVecN : 1;
         const int nvec = cols / VEC;
+        const int nvec_shift = ceil_div(cols, kVecN);      // a row's vector slots, at most
         const bool warp_ok = nvec <= 32 * 8;
         const int stage_bytes = C::kInputs * cols * (int)sizeof(T);
         const bool stage_fits = !tun.no_bulk && kHdrBytes + stage_bytes <= ctx.smem_optin;
 
-        const bool one_cta = nvec <= cta_max_nvec(vec);
+        const bool shift = shift_ok && nvec_shift <= cta_max_nvec(true);
+        const bool one_cta = shift || nvec <= cta_max_nvec(vec);
         int warp_vpl = 1;
         while (warp_vpl * 32 < nvec) warp_vpl *= 2;
         bool warp_spills = false;
@@ -1260,6 +1421,8 @@ template <class C> struct RowEngine {
         // unless the chain sets its own; the grid holds no more resident CTAs
         // than the target.
         const bool staged = path == MB_ROW_STAGED;
+        const bool shifted = shift && path == MB_ROW_DIRECT;
+        const int nvec_cta = shifted ? nvec_shift : nvec;
         const int smem1 = kHdrBytes + (staged ? stage_bytes : 0);
         const int64_t row_io =
             ((int64_t)C::kInputs * cols * (staged ? tun.read_pct : 100) / 100 +
@@ -1272,11 +1435,11 @@ template <class C> struct RowEngine {
         if (C::kRowsTarget > 0) target = C::kRowsTarget;     // the chain's own measured target
         int best_vpt = 0, best_occ = 0, best_threads = 0;
         bool best_spills = true;
-        for (int cand = 1; cand <= max_vpt(vec); cand *= 2) {
+        for (int cand = 1; cand <= max_vpt(vec || shifted); cand *= 2) {
             if (tun.vpt > 0 && cand != tun.vpt) continue;
-            if (ceil_div(nvec, cand) > kCtaMaxThreads) continue;
-            const int threads = round_up32(ceil_div(nvec, cand));
-            const void *f = cta_fn(cand, vec, staged);
+            if (ceil_div(nvec_cta, cand) > kCtaMaxThreads) continue;
+            const int threads = round_up32(ceil_div(nvec_cta, cand));
+            const void *f = shifted ? shift_fn(cand) : cta_fn(cand, vec, staged);
             if (!f) continue;
             int max_threads = 0;
             bool spills = false;
@@ -1325,7 +1488,8 @@ template <class C> struct RowEngine {
             stages = want;
             smem = kHdrBytes + stages * stage_bytes;
         }
-        *fn = cta_fn(best_vpt, vec, staged);
+        *fn = shifted ? shift_fn(best_vpt) : cta_fn(best_vpt, vec, staged);
+        if (shifted) { p->vec = kVecN; p->shift = 1; }
         int occ2 = 0;
         mb_status st = occupancy(ctx, *fn, best_threads, smem, &occ2);
         if (st != MB_OK) return st;
@@ -1348,7 +1512,7 @@ template <class C> struct RowEngine {
     }
 
     static mb_status run(const LaunchCtx &ctx, const RowTuning &tun, const typename C::Args &a,
-                         int64_t rows, int cols, bool aligned, RowPlan *plan_out, bool launch) {
+                         int64_t rows, int cols, int aligned, RowPlan *plan_out, bool launch) {
         RowPlan p;
         const void *fn = nullptr;
         RowTuning tn = tun;      // the per-call planning inputs
@@ -1374,8 +1538,11 @@ template <class C> struct RowEngine {
         typename C::Args args = a;
         int64_t rows_arg = rows;
         int cols_arg = cols;
-        // the fourth kernel argument: ring depth, or the cluster's slice length
-        int stages_arg = p.path == MB_ROW_CLUSTER ? p.slice * p.vec : (p.stages > 0 ? p.stages : 1);
+        // the fourth kernel argument: ring depth, the cluster's slice length,
+        // or (shifted vectors) the row tensors' common offset within 16 bytes
+        int stages_arg = p.path == MB_ROW_CLUSTER ? p.slice * p.vec
+                       : p.shift ? (int)(reinterpret_cast<uintptr_t>(a.in[0]) & 15u)
+                       : (p.stages > 0 ? p.stages : 1);
         unsigned *err = ctx.dev_err;
         int ring_arg = p.ring;      // the cluster kernel's sixth argument
         void *kargs[] = {&args, &rows_arg, &cols_arg, &stages_arg, &err, &ring_arg};

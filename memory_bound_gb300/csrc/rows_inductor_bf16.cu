@@ -7,7 +7,7 @@ namespace mb {
 mb_status inductor_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                              const void *bias, const void *gamma, const void *beta, void *y,
                              int64_t rows, int cols, float x_scale, float branch_scale,
-                             bool aligned, RowPlan *plan, bool launch) {
+                             int aligned, RowPlan *plan, bool launch) {
     using C = InductorChainT<uint16_t>;
     C::Args a{{static_cast<const uint16_t *>(x)}, static_cast<const uint16_t *>(bias),
               static_cast<const uint16_t *>(gamma), static_cast<const uint16_t *>(beta),

@@ -5,7 +5,7 @@ namespace mb {
 
 mb_status ln_gelu_rows_bf16(const LaunchCtx &ctx, const RowTuning &tun, const void *x,
                             const void *r, const void *w, const void *b, void *out,
-                            int64_t rows, int cols, float eps, bool aligned, RowPlan *plan,
+                            int64_t rows, int cols, float eps, int aligned, RowPlan *plan,
                             bool launch) {
     using C = LnGeluChain<uint16_t>;
     C::Args a{{static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(r)},

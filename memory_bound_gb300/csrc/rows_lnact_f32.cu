@@ -8,7 +8,7 @@ namespace mb {
 mb_status lnact_rows_f32(const LaunchCtx &ctx, const RowTuning &tun, bool residual,
                          const void *x, const void *r, const void *w, const void *b, void *out,
                          void *h, int64_t rows, int cols, float eps, int act, const LnExtras &ex,
-                         bool aligned, RowPlan *plan, bool launch) {
+                         int aligned, RowPlan *plan, bool launch) {
     return lnact_run<float, false>(ctx, tun, residual, x, r, w, b, out, h, rows, cols, eps, act,
                                 ex, aligned, plan, launch);
 }

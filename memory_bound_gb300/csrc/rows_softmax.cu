@@ -4,7 +4,7 @@
 namespace mb {
 
 mb_status softmax_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
-                       const void *x, void *y, int64_t rows, int cols, bool aligned,
+                       const void *x, void *y, int64_t rows, int cols, int aligned,
                        RowPlan *plan, bool launch) {
     if (dtype == MB_F32) {
         using C = SoftmaxChain<float>;

@@ -6,7 +6,7 @@ namespace mb {
 
 mb_status softmax_mask_rows(const LaunchCtx &ctx, const RowTuning &tun, mb_dtype dtype,
                             const void *x, void *y, int64_t rows, int cols, float scale,
-                            bool causal, int64_t period, int64_t offset, bool aligned,
+                            bool causal, int64_t period, int64_t offset, int aligned,
                             RowPlan *plan, bool launch) {
     if (period < 1) period = 1;
     if (offset > cols) offset = cols;                 // masks nothing more

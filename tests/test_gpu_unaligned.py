@@ -1,9 +1,12 @@
-"""Rows that are not whole 16-byte vectors (the scalar path of every row
-engine): lengths from a few thousand to past one CTA's reach, where the
-one-CTA engine's 16- and 32-slot forms (bounded at 512 threads, so they hold
-their values in registers) and then the cluster engine serve them; plain and
-offset views; every chain against the oracle.  The full ragged workload
-(8192 x 4099 fp32, the benchmark's row) is checked on every element."""
+"""Rows off the 16-byte grid: lengths that are not whole 16-byte vectors, and
+tensors that start off a 16-byte boundary.  When every row tensor of a call
+starts at the same offset within 16 bytes, rows up to one CTA's reach take
+the shifted-vector engine (a short head, whole 16-byte vectors, a short
+tail); otherwise the scalar forms of the one-CTA engine (16 and 32 slots
+bounded at 512 threads where the 1024-thread form spills) and past one CTA
+the cluster engine.  Every chain against the oracle, with the placements
+that select each path; the full ragged workload (8192 x 4099 fp32, the
+benchmark's row) on every element."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +16,7 @@ import oracle
 import synth
 from synth import workloads as W
 
-from gpu_util import assert_close, report, to_dev, to_host
+from gpu_util import assert_bitexact, assert_close, bf16_to_f64, report, to_dev, to_host
 from row_blocks import map_row_blocks, worst
 
 pytestmark = pytest.mark.gpu
@@ -56,22 +59,102 @@ def _vecs(cols, seed, bf16):
             synth.normal(seed, 3, (cols,), 0.0, 0.1, dtype=dt))
 
 
-@pytest.mark.parametrize("cols", LENGTHS)
+def _out_like(x, bf16, offset):
+    """An output tensor like x, starting `offset` elements into its allocation."""
+    dt = torch.bfloat16 if bf16 else torch.float32
+    flat = torch.empty(x.size + offset, dtype=dt, device="cuda")
+    return flat[offset:].view(x.shape)
+
+
+# placements: every tensor 16-byte aligned; the row inputs one element off
+# (the output aligned: no common offset, the scalar path); inputs and output
+# one element off (a common offset: the shifted-vector path)
+PLACES = {"base": (0, 0), "inputs_off": (1, 0), "all_off": (1, 1)}
+
+
+@pytest.mark.parametrize("cols", LENGTHS + [1031, 2053])
 @pytest.mark.parametrize("path", ["auto", "direct", "cluster"])
-@pytest.mark.parametrize("offset", [0, 1], ids=["base", "offset"])
+@pytest.mark.parametrize("place", sorted(PLACES))
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
-def test_ln_gelu_unaligned(cols, path, offset, bf16):
+def test_ln_gelu_unaligned(cols, path, place, bf16):
     mb.set_row_path(path)
     try:
         rows = 37
+        xo, oo = PLACES[place]
         x, r = _rows(rows, cols, cols + 1, bf16, 2)
         w, b = _vecs(cols, cols + 1, bf16)
-        out = mb.fused_residual_layernorm_gelu(_dev(x, bf16, offset), _dev(r, bf16, offset),
-                                               to_dev(w, bf16), to_dev(b, bf16), 1e-5)
+        out = _out_like(x, bf16, oo)
+        mb.fused_residual_layernorm_gelu(_dev(x, bf16, xo), _dev(r, bf16, xo), to_dev(w, bf16),
+                                         to_dev(b, bf16), 1e-5, out=out)
         assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5), bf16=bf16,
-                     what=f"{cols} {path} offset={offset}")
+                     what=f"{cols} {path} {place}")
     finally:
         mb.set_row_path("auto")
+
+
+@pytest.mark.parametrize("cols", [4096 + 3, 8192 + 5, 1024 + 1])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_shifted_path_is_planned(cols, bf16):
+    """Rows off the 16-byte grid with a common offset plan on 16-byte
+    vectors (path direct, the vector width), not on the scalar path; the
+    dropout chains keep the scalar path."""
+    dt = "bf16" if bf16 else "f32"
+    vec = 8 if bf16 else 4
+    for chain in ("ln", "inductor", "lnact", "lnact_res", "softmax", "softmax_mask"):
+        if chain == "inductor" and bf16:
+            continue
+        for al in (1, 2):
+            p = mb.row_plan(chain, dt, 512, cols, aligned=al)
+            assert p["path"] == "direct" and p["vec"] == vec, (chain, al, p)
+        assert mb.row_plan(chain, dt, 512, cols, aligned=0)["vec"] == 1
+    assert mb.row_plan("lnact_dropout", dt, 512, cols, aligned=1)["vec"] == 1
+
+
+@pytest.mark.parametrize("cols", [1031, 4099, 12291])
+@pytest.mark.parametrize("chain", ["inductor", "lnact_h", "softmax", "softmax_mask"])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_shifted_chains(cols, chain, bf16):
+    """Every chain on the shifted-vector path with a non-zero common offset:
+    inputs and outputs two elements into their allocations."""
+    if chain == "inductor" and bf16:
+        pytest.skip("the bf16 Inductor entry point is tested by test_gpu_next")
+    rows, off = 23, 2
+    dt = "bf16" if bf16 else "f32"
+    x = synth.normal(cols + 3, 0, (rows, cols), dtype=dt)
+    if chain == "inductor":
+        bias = synth.normal(cols + 3, 1, (cols,), 0.0, 0.1)
+        gamma = synth.uniform(cols + 3, 2, (cols,), 0.5, 1.5)
+        beta = synth.normal(cols + 3, 3, (cols,), 0.0, 0.1)
+        y = _out_like(x, False, off)
+        mb.fused_bias_relu_branch_mean_epilogue(_dev(x, False, off), to_dev(bias), to_dev(gamma),
+                                                to_dev(beta), 1.1, 0.1, out=y)
+        assert_close(to_host(y), oracle.bias_relu_branch_mean_epilogue(x, bias, gamma, beta),
+                     what=f"inductor {cols}")
+    elif chain == "lnact_h":
+        r = synth.normal(cols + 3, 1, (rows, cols), dtype=dt)
+        w, b = _vecs(cols, cols + 3, bf16)
+        out, h = _out_like(x, bf16, off), _out_like(x, bf16, off)
+        mb.fused_layernorm_act(_dev(x, bf16, off), _dev(r, bf16, off), to_dev(w, bf16),
+                               to_dev(b, bf16), act="gelu_tanh", out=out, h_out=h)
+        want, want_h = oracle.layernorm_act(x, r, w, b, 1e-5, oracle.ACT_GELU, want_h=True)
+        assert_close(to_host(out), want, bf16=bf16, what=f"lnact {cols}")
+        assert_bitexact(to_host(h), want_h, f"h {cols}")
+    else:
+        y = _out_like(x, bf16, off)
+        if chain == "softmax":
+            mb.fused_row_softmax(_dev(x, bf16, off), out=y)
+            want = oracle.row_softmax(x)
+        else:
+            mb.fused_row_softmax(_dev(x, bf16, off), out=y, scale=0.25, causal=True, period=rows,
+                                 offset=cols // 3)
+            want = oracle.scale_mask_softmax(x, 0.25, True, rows, cols // 3)
+        g = bf16_to_f64(to_host(y)) if bf16 else to_host(y).astype(np.float64)
+        w_ = bf16_to_f64(want) if bf16 else want.astype(np.float64)
+        rtol = 1e-2 if bf16 else 1e-5
+        assert np.all(np.abs(g - w_) <= rtol * np.abs(w_) + 2.0 ** -126), f"{chain} {cols}"
+        if chain == "softmax_mask":
+            masked = np.arange(cols)[None, :] > (np.arange(rows)[:, None] % rows + cols // 3)
+            assert np.all(g[masked] == 0)
 
 
 @pytest.mark.parametrize("cols", LENGTHS)
@@ -110,7 +193,7 @@ def test_ragged_workload_full_size():
     """ln_gelu_f32_8192x4099 (the benchmark's unaligned row): every element."""
     w = W.LN_F32_RAGGED
     t = w.generate_all()
-    assert mb.row_plan("ln", "f32", w.rows, w.cols)["vec"] == 1
+    assert mb.row_plan("ln", "f32", w.rows, w.cols)["vec"] == 4      # shifted vectors
     out = mb.fused_residual_layernorm_gelu(to_dev(t["x"]), to_dev(t["r"]), to_dev(t["w"]),
                                            to_dev(t["b"]), 1e-5)
     torch.cuda.synchronize()
