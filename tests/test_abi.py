@@ -200,3 +200,24 @@ def test_scale_mask_softmax_argument_checks(lib):
     assert f(A + 2, B, 4, 64, 0.125, 0, 1, 0, 0, None) == MB_ERR_ALIGN
     assert f(A, None, 4, 64, 0.125, 0, 1, 0, 1, None) == MB_ERR_NULL
     assert f(A, B, 4, 0, 0.125, 0, 1, 0, 0, None) == MB_ERR_SHAPE
+
+
+def test_library_build_depends_on_its_build_script(tmp_path, monkeypatch):
+    """A change to the build script (its flags or architecture) makes the
+    library out of date, like a change to a source file."""
+    import time
+    from memory_bound_gb300 import build as b
+    lib = tmp_path / "lib.so"
+    lib.write_bytes(b"x")
+    monkeypatch.setattr(b, "LIB", str(lib))
+    future = time.time() + 3600
+    os.utime(lib, (future, future))
+    assert b._up_to_date()
+    later = future + 60
+    script = b.__file__
+    st = os.stat(script)
+    try:
+        os.utime(script, (later, later))
+        assert not b._up_to_date()
+    finally:
+        os.utime(script, (st.st_atime, st.st_mtime))

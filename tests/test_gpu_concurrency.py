@@ -98,3 +98,51 @@ def test_threads_on_separate_streams():
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
     assert res.returncode == 0, res.stdout[-3000:] + res.stderr[-3000:]
     assert "concurrent ok" in res.stdout
+
+
+def test_path_setter_racing_calls():
+    """One thread keeps switching the process-wide row path and launch shape
+    while another calls the LayerNorm chain on fixed inputs: every call reads
+    the setting whole (it is copied under the library's lock), so every
+    result matches the oracle whichever engine ran it."""
+    import threading
+
+    import numpy as np
+    import torch
+
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import memory_bound_gb300 as mb
+    import oracle
+    import synth
+    from gpu_util import assert_close, to_dev, to_host
+
+    torch.cuda.set_device(0)
+    x, r = synth.normal(1201, 0, (64, 4096)), synth.normal(1201, 1, (64, 4096))
+    w, b = synth.uniform(1201, 2, (4096,), 0.5, 1.5), synth.normal(1201, 3, (4096,), 0, 0.1)
+    want = oracle.residual_layernorm_gelu(x, r, w, b, 1e-5)
+    d = [to_dev(a) for a in (x, r, w, b)]
+    stop = threading.Event()
+    shapes = [("auto", 0, 0, 0), ("direct", 2, 0, 1), ("staged", 3, 2, 2), ("warp", 0, 0, 0),
+              ("cluster", 0, 2, 0), ("direct", 0, 0, 8)]
+
+    def flip():
+        k = 0
+        while not stop.is_set():
+            mb.set_row_path(*shapes[k % len(shapes)])
+            k += 1
+
+    t = threading.Thread(target=flip)
+    t.start()
+    try:
+        outs = []
+        for _ in range(200):
+            outs.append(mb.fused_residual_layernorm_gelu(*d, 1e-5))
+        torch.cuda.synchronize()
+    finally:
+        stop.set()
+        t.join()
+        mb.set_row_path("auto")
+    for o in outs:
+        assert_close(to_host(o), want)
+    assert mb.device_error() == 0
