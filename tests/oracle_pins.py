@@ -70,6 +70,29 @@ def pin_gelu_library(lib):
     assert np.all(err <= 1e-14 * np.abs(want) + 1e-15 * np.abs(z)), err.max()
 
 
+def pin_gelu_whole_range(lib):
+    """GeLU tanh form against torch's float64 gelu(approximate='tanh') over
+    the arguments the GPU range test feeds the kernels: a dense grid on
+    [-40, 40], both 2^t overflow edges (|z| in [9.4, 10.6]), magnitudes from
+    1e-45 to 1, signed zeros, subnormals, |z| up to 3e38, and every finite
+    bf16 value.  Negative arguments give a result <= 0, positive ones >= 0."""
+    grid = np.concatenate([
+        np.linspace(-40.0, 40.0, 8001), np.linspace(-10.6, -9.4, 1201),
+        np.linspace(9.4, 10.6, 1201), np.logspace(-45, 0, 226), -np.logspace(-45, 0, 226),
+        np.array([0.0, -0.0, 1e-3, -1e-3, 88.0, -88.0, 1e5, -1e5, 1e20, -1e20, 3.0e38,
+                  -3.0e38, 1e-40, -1e-40])]).astype(np.float32).astype(np.float64)
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    h = h[(h & 0x7F80) != 0x7F80]
+    bf = (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    z = np.concatenate([grid, bf])
+    want = F.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    got = np.array([oracle.gelu_tanh(v, lib=lib) for v in z])
+    err = np.abs(got - want)
+    assert np.all(err <= 1e-14 * np.abs(want) + 1e-15 * np.abs(z)), float(err.max())
+    assert np.all(got[z < 0] <= 0) and np.all(got[z > 0] >= 0)
+    assert np.all(got[np.abs(z) >= 30] == np.where(z[np.abs(z) >= 30] > 0, z[np.abs(z) >= 30], 0))
+
+
 def pin_gelu_invariants(lib):
     """GeLU(0) = 0; GeLU(z) - GeLU(-z) = z (the tanh term is odd);
     GeLU(z) -> z for large z and -> 0 for very negative z."""
