@@ -51,10 +51,9 @@
  *               row tensors starting off a 16-byte boundary) still take
  *               16-byte row accesses when all row tensors of the call (row
  *               inputs and outputs) start at the same offset within 16
- *               bytes and a row holds one CTA's worth or less (except with
- *               dropout): each row is then read as a short head, whole
- *               vectors and a short tail.  Anything else runs on a scalar
- *               path.
+ *               bytes and a row holds one CTA's worth or less: each row is
+ *               then read as a short head, whole vectors and a short tail.
+ *               Anything else runs on a scalar path.
  *   Aliasing    The output may not overlap any input (MB_ERR_OVERLAP).
  *               Inputs may overlap one another.
  *   Sizes       Zero rows / zero elements is a no-op returning MB_OK without

@@ -112,7 +112,7 @@ template <typename TT> struct LnGeluChain {
     template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
     static constexpr int kPostPC = 2;     // per-column vectors the epilogue reads
     template <int VEC> using Early = NoEarly;
-    template <int VEC>
+    template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
@@ -193,7 +193,7 @@ template <typename TT> struct InductorChainT {
     template <int VEC> struct PostPC { Frag<T, VEC> gamma, beta; };
     static constexpr int kPostPC = 2;
     template <int VEC> using Early = NoEarly;
-    template <int VEC>
+    template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc) {
@@ -285,10 +285,10 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     // scalar slots per thread from which the one-CTA engine takes its
     // 512-thread form (the 1024-thread one spills from there on)
     static constexpr int kWideScalarSlots = DROP ? 16 : 32;
-    // rows off the 16-byte grid may take the shifted-vector engine; dropout
-    // needs each slot to start at a multiple of 8 elements, so it keeps the
-    // scalar one
-    static constexpr bool kShiftOk = !DROP;
+    // rows off the 16-byte grid may take the shifted-vector engine (with
+    // dropout, a slot may start anywhere within a block of eight: its keep
+    // bits come from one or two blocks, dropout_bits)
+    static constexpr bool kShiftOk = true;
     static constexpr int kClusterVals = sizeof(T) == 2 ? 32 : 16;   // as LnGeluChain
     static constexpr bool kStageLargeSlices = false;   // measured slower staged
     static constexpr bool kPartialRows = false;   // every row read whole
@@ -315,9 +315,9 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     // flight (they depend only on the element index)
     template <int VEC> struct EarlyDrop { DropBits<VEC> bits; };
     template <int VEC> using Early = std::conditional_t<DROP, EarlyDrop<VEC>, NoEarly>;
-    template <int VEC>
+    template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &a, int64_t off, Early<VEC> &e) {
-        if constexpr (DROP) dropout_bits<VEC>(off, a.drop, e.bits);
+        if constexpr (DROP) dropout_bits<VEC, ANYOFF>(off, a.drop, e.bits);
     }
     template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
@@ -413,7 +413,7 @@ template <typename TT> struct SoftmaxChain {
     template <int VEC> struct PostPC {};
     static constexpr int kPostPC = 0;
     template <int VEC> using Early = NoEarly;
-    template <int VEC>
+    template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
@@ -514,7 +514,7 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     template <int VEC> struct PostPC {};
     static constexpr int kPostPC = 0;
     template <int VEC> using Early = NoEarly;
-    template <int VEC>
+    template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
     template <int VEC, bool AL = true>
     __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}

@@ -134,28 +134,51 @@ __device__ __forceinline__ float keep_scale(uint32_t half, const DropoutArgs &d)
     return half >= d.thr ? d.inv_keep : 0.0f;
 }
 
-// The 16-bit halves of one slot of VEC elements: a slot of eight or more
-// holds whole blocks (its first index is a multiple of 8, rows holding a whole
-// number of slots), four words per block; a scalar slot keeps its element's
-// half in the low bits of one word per element.
+// The keep decisions of the eight elements of block g, as bits (bit e: the
+// element of index 8 (g - offset) + e is kept).
+__device__ __forceinline__ uint32_t keep_bits8(uint64_t g, const DropoutArgs &d) {
+    const uint4 w = philox_block(g, d);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t m = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        m |= (uint32_t)((ws[k] & 0xFFFFu) >= d.thr) << (2 * k);
+        m |= (uint32_t)((ws[k] >> 16) >= d.thr) << (2 * k + 1);
+    }
+    return m;
+}
+
+// The dropout draws of one slot of VEC elements.  A slot of eight or more
+// keeps its keep decisions as bits (bit e: element e of the slot); a scalar
+// slot keeps its element's 16-bit half.
 template <int VEC> struct DropBits {
-    static constexpr int kWords = VEC % 8 == 0 ? VEC / 2 : VEC;
+    static constexpr bool kMask = VEC % 8 == 0;
+    static constexpr int kWords = kMask ? 1 : VEC;
     uint32_t w[kWords];
 };
 
-// The halves of the slot whose first element has index `off` in the whole
-// tensor (they depend on nothing else, so they can be drawn early).
-template <int VEC>
+// The draws of the slot whose first element has index `off` in the whole
+// tensor (they depend on nothing else, so they can be drawn early).  A slot
+// of eight elements starts on a block (off a multiple of 8) on the aligned
+// engines; with ANYOFF (the shifted-vector engine) it may start at s = off
+// mod 8 > 0 and then spans blocks off / 8 and the next one: their sixteen
+// keep bits shifted down by s (s is the same for every slot of a row, so the
+// branch is uniform).
+template <int VEC, bool ANYOFF = false>
 __device__ __forceinline__ void dropout_bits(int64_t off, const DropoutArgs &d, DropBits<VEC> &b) {
     if constexpr (VEC % 8 == 0) {
+        const uint64_t g0 = d.offset + (uint64_t)(off >> 3);
+        uint32_t m = 0u;
 #pragma unroll
         for (int q = 0; q < VEC / 8; ++q) {
-            const uint4 w = philox_block(d.offset + (uint64_t)(off >> 3) + (uint64_t)q, d);
-            b.w[4 * q + 0] = w.x;
-            b.w[4 * q + 1] = w.y;
-            b.w[4 * q + 2] = w.z;
-            b.w[4 * q + 3] = w.w;
+            uint32_t bits = keep_bits8(g0 + (uint64_t)q, d);
+            if constexpr (ANYOFF) {
+                const int sh = (int)(off & 7);
+                if (sh) bits = (bits | keep_bits8(g0 + (uint64_t)q + 1u, d) << 8) >> sh;
+            }
+            m |= (bits & 0xFFu) << (8 * q);
         }
+        b.w[0] = m;
     } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -174,10 +197,7 @@ __device__ __forceinline__ void dropout_apply(float (&o)[VEC], const DropBits<VE
                                               const DropoutArgs &d) {
     if constexpr (VEC % 8 == 0) {
 #pragma unroll
-        for (int k = 0; k < VEC / 2; ++k) {
-            o[2 * k] *= keep_scale(b.w[k] & 0xFFFFu, d);
-            o[2 * k + 1] *= keep_scale(b.w[k] >> 16, d);
-        }
+        for (int e = 0; e < VEC; ++e) o[e] *= ((b.w[0] >> e) & 1u) ? d.inv_keep : 0.0f;
     } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) o[e] *= keep_scale(b.w[e], d);

@@ -429,7 +429,7 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
         typename C::template Early<VEC> ea[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
-            C::template early<VEC>(a, vbase + (int64_t)min(tid + k * T_, nb - 1) * VEC, ea[k]);
+            C::template early<VEC, true>(a, vbase + (int64_t)min(tid + k * T_, nb - 1) * VEC, ea[k]);
         typename C::template Early<1> ea_e;
         C::template early<1>(a, base + (has_e ? col_e : 0), ea_e);
 

@@ -97,7 +97,7 @@ def test_ln_gelu_unaligned(cols, path, place, bf16):
 def test_shifted_path_is_planned(cols, bf16):
     """Rows off the 16-byte grid with a common offset plan on 16-byte
     vectors (path direct, the vector width), not on the scalar path; the
-    dropout chains keep the scalar path."""
+    dropout chains too (their slots are 8 elements)."""
     dt = "bf16" if bf16 else "f32"
     vec = 8 if bf16 else 4
     for chain in ("ln", "inductor", "lnact", "lnact_res", "softmax", "softmax_mask"):
@@ -107,7 +107,9 @@ def test_shifted_path_is_planned(cols, bf16):
             p = mb.row_plan(chain, dt, 512, cols, aligned=al)
             assert p["path"] == "direct" and p["vec"] == vec, (chain, al, p)
         assert mb.row_plan(chain, dt, 512, cols, aligned=0)["vec"] == 1
-    assert mb.row_plan("lnact_dropout", dt, 512, cols, aligned=1)["vec"] == 1
+    for chain in ("lnact_dropout", "lnact_res_dropout"):
+        p = mb.row_plan(chain, dt, 512, cols, aligned=1)
+        assert p["path"] == "direct" and p["vec"] == 8, (chain, p)
 
 
 @pytest.mark.parametrize("cols", [1031, 4099, 12291])
@@ -205,3 +207,37 @@ def test_ragged_workload_full_size():
 
     err, ratio = worst(map_row_blocks(w.rows, block))
     report(w.name, max_abs_err=err, max_err_over_bar=ratio)
+
+
+@pytest.mark.parametrize("cols", [1031, 4099, 4100, 12291])
+@pytest.mark.parametrize("res", [False, True], ids=["nores", "res"])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_shifted_dropout(cols, res, bf16):
+    """LayerNorm -> ReLU -> Dropout on the shifted-vector path (slots that
+    start anywhere within a Philox block of eight): the keep mask exact on
+    every element, values at the bar, row statistics; inputs and outputs at a
+    common offset of three elements, and a generator offset that is not a
+    multiple of the row's blocks."""
+    rows, off, p, seed, goff = 19, 3, 0.3, 4321, 7
+    dt = "bf16" if bf16 else "f32"
+    x = synth.normal(cols + 11, 0, (rows, cols), dtype=dt)
+    r = synth.normal(cols + 11, 1, (rows, cols), dtype=dt) if res else None
+    w, b = _vecs(cols, cols + 11, bf16)
+    out = _out_like(x, bf16, off)
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    mb.fused_layernorm_act(_dev(x, bf16, off), _dev(r, bf16, off) if res else None,
+                           to_dev(w, bf16), to_dev(b, bf16), act="relu", out=out, p=p, seed=seed,
+                           offset=goff, mean_out=mean, rstd_out=rstd)
+    want, _, wm, wr = oracle.layernorm_act_ex(x, r, w, b, 1e-5, oracle.ACT_RELU, p=p, seed=seed,
+                                              offset=goff, want_stats=True)
+    keep = oracle.dropout_mask(seed, goff, 0, x.size, p).reshape(x.shape)
+    got = to_host(out)
+    g = bf16_to_f64(got) if bf16 else got.astype(np.float64)
+    wv = bf16_to_f64(want) if bf16 else want.astype(np.float64)
+    assert np.all(g[~keep] == 0), "a dropped element is not zero"
+    assert np.all(g[keep & (wv != 0)] != 0), "a kept element was dropped"
+    assert_close(got, want, bf16=bf16, what=f"dropout {cols} res={res}")
+    m, rs = to_host(mean).astype(np.float64), to_host(rstd).astype(np.float64)
+    assert np.all(np.abs(m - wm) <= 1e-5 / wr + 1e-7 * np.abs(wm))
+    assert np.all(np.abs(rs - wr) <= 1e-5 * wr)
