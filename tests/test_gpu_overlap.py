@@ -94,3 +94,36 @@ def test_torch_writer_then_call(overlap):
         y = mb.fused_add_relu_scale(x, d1, d2, 0.5)
         want = oracle.add_relu_scale((a * np.float32(k + 1)).astype(np.float32), b1, b2, 0.5)
         assert np.array_equal(to_host(y).view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+@pytest.mark.parametrize("graph", [False, True])
+def test_dependent_chain_off_grid_rows(overlap, graph):
+    """The same composition on rows off the 16-byte grid (4099 columns: the
+    shifted-vector engine for the LayerNorm and softmax calls): pointwise ->
+    residual + LayerNorm + GeLU -> softmax, each call reading the previous
+    call's output at once."""
+    mb.set_launch_overlap(overlap)
+    rows, cols = 1031, 4099
+    x, b1, b2, r = (synth.normal(903, k, (rows, cols)) for k in range(4))
+    w = synth.uniform(903, 4, (cols,), 0.5, 1.5)
+    b = synth.normal(903, 5, (cols,), 0.0, 0.1)
+    assert mb.row_plan("ln", "f32", rows, cols)["vec"] == 4        # shifted vectors
+    d = {k: to_dev(v) for k, v in zip(("x", "b1", "b2", "r", "w", "b"), (x, b1, b2, r, w, b))}
+    y1, y2, y3 = (torch.empty((rows, cols), device="cuda") for _ in range(3))
+    if graph:
+        _device_chain(d, y1, y2, y3)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            _device_chain(d, y1, y2, y3)
+        for t in (y1, y2, y3):
+            t.zero_()
+        g.replay()
+    else:
+        _device_chain(d, y1, y2, y3)
+    torch.cuda.synchronize()
+    want = _oracle_chain(x, b1, b2, r, w, b)
+    got = to_host(y3)
+    err = np.abs(got.astype(np.float64) - want) / np.maximum(np.abs(want), 1e-30)
+    assert float(err.max()) < 1e-4, float(err.max())
