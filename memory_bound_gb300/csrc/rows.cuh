@@ -30,6 +30,14 @@
 //             slot of row i is refilled with row i + nstage as soon as the
 //             first reduction barrier shows that every thread has copied row
 //             i into registers.
+//     (rows_cta_kernel_wide: the scalar forms with many slots per thread,
+//     bounded at 512 threads; rows_cta_kernel_capped: the register-capped
+//     form a chain may ask for)
+//   rows_shift_kernel one CTA per row for rows off the 16-byte grid whose
+//                     tensors share one offset within 16 bytes: a short head,
+//                     whole 16-byte vectors, a short tail.
+//   rows_cluster_kernel / rows_cluster_smem_kernel  one thread-block cluster
+//                     per row, for rows longer than one CTA holds.
 // Several CTAs share an SM, each with its own row in flight, so one CTA's
 // loads overlap the others' reductions and epilogues.
 #pragma once
