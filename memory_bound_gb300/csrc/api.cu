@@ -462,13 +462,12 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll) {
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols, int aligned,
                       int32_t out[7]) {
     if (!out) return MB_ERR_NULL;
-    if (chain < 0 || chain > 8) return MB_ERR_VALUE;
+    if (chain < 0 || chain > 8 || aligned < 0 || aligned > 2) return MB_ERR_VALUE;
     if (!valid_dtype(dtype)) return MB_ERR_DTYPE;
     mb_status st = check_rows(rows, cols);
     if (st != MB_OK) return st;
     LaunchCtx ctx;
     if ((st = device_ctx(0, &ctx)) != MB_OK) return st;
-    if (aligned < 0 || aligned > 2) return MB_ERR_VALUE;
     RowPlan p;
     const int al = aligned;
     if (chain == 1 && dtype == MB_F32)

@@ -106,6 +106,16 @@ def test_row_path_setter_validates(lib):
     assert lib.mb_set_row_path(0, 0, 0, 0) == MB_OK
 
 
+def test_row_plan_validates_its_arguments(lib):
+    """mb_row_plan refuses a NULL output, an unknown chain and an alignment
+    class other than 0, 1 or 2 before it queries the device."""
+    out = (ctypes.c_int32 * 7)()
+    assert lib.mb_row_plan(0, 0, 8, 4096, 1, None) == MB_ERR_NULL
+    assert lib.mb_row_plan(9, 0, 8, 4096, 1, out) == MB_ERR_VALUE
+    assert lib.mb_row_plan(0, 0, 8, 4096, 3, out) == MB_ERR_VALUE
+    assert lib.mb_row_plan(0, 0, 8, 4096, -1, out) == MB_ERR_VALUE
+
+
 def test_launch_overlap_setter_validates(lib):
     assert lib.mb_set_launch_overlap(2) == MB_ERR_VALUE
     assert lib.mb_set_launch_overlap(0) == MB_OK
