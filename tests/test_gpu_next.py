@@ -195,3 +195,18 @@ def test_inductor_bf16(shape, path, row_path):
     want = oracle.bias_relu_branch_mean_epilogue_bf16(x, bias, gamma, beta)
     assert_close(to_host(y), want, bf16=True, what=f"{shape} {path}")
     check_guard(buf)
+
+
+def test_inductor_bf16_workload_full_size():
+    """The benchmark's bf16 Inductor workload (its own seed), every element
+    against the oracle."""
+    w = W.INDUCTOR_BF16
+    t = w.generate_all()
+    y = mb.fused_bias_relu_branch_mean_epilogue(to_dev(t["x"], True), to_dev(t["bias"], True),
+                                                to_dev(t["gamma"], True), to_dev(t["beta"], True),
+                                                w.params["x_scale"], w.params["branch_scale"])
+    want = oracle.bias_relu_branch_mean_epilogue_bf16(t["x"], t["bias"], t["gamma"], t["beta"],
+                                                      w.params["x_scale"],
+                                                      w.params["branch_scale"])
+    err, ratio = assert_close(to_host(y), want, bf16=True, what=w.name)
+    report(w.name, max_abs_err=err, max_err_over_bar=ratio)
