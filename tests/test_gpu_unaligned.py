@@ -241,3 +241,20 @@ def test_shifted_dropout(cols, res, bf16):
     m, rs = to_host(mean).astype(np.float64), to_host(rstd).astype(np.float64)
     assert np.all(np.abs(m - wm) <= 1e-5 / wr + 1e-7 * np.abs(wm))
     assert np.all(np.abs(rs - wr) <= 1e-5 * wr)
+
+
+def test_scalar_reach_and_cluster_boundary():
+    """Rows with no common offset take the scalar one-CTA forms up to 16384
+    elements (the reach of the 32-slot form, bounded at 512 threads so it
+    holds its values in registers), the cluster engine past that; with a
+    common offset the same rows take shifted vectors up to one CTA's vector
+    reach (32768 elements)."""
+    for cols in (16383, 16384):
+        p = mb.row_plan("ln", "f32", 64, cols, aligned=0)
+        assert p["path"] == "direct" and p["vec"] == 1, p
+    p = mb.row_plan("ln", "f32", 64, 16385, aligned=0)
+    assert p["path"] == "cluster" and p["vec"] == 1, p
+    for cols in (16385, 32767):
+        p = mb.row_plan("ln", "f32", 64, cols, aligned=2)
+        assert p["path"] == "direct" and p["vec"] == 4, p
+    assert mb.row_plan("ln", "f32", 64, 32769, aligned=2)["path"] == "cluster"
