@@ -411,7 +411,9 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * one common offset within 16 bytes (per-column vectors anywhere); 0 neither;
  * else MB_ERR_VALUE.  Rows planned on shifted vectors report path
  * MB_ROW_DIRECT with the vector width in out[4] while cols is not a multiple
- * of it.  Queries the current device (SM count, shared memory).
+ * of it; out[6] then includes the shared-memory copy of the chain's
+ * per-column arrays where one is planned (launches of several rows a CTA).
+ * Queries the current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,
                       int aligned, int32_t out[7]);

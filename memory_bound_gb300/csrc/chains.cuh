@@ -111,15 +111,22 @@ template <typename TT> struct LnGeluChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
     static constexpr int kPostPC = 2;     // per-column vectors the epilogue reads
+    // the per-column arrays, numbered as the load hooks number them
+    static constexpr int kColArrays = 2;
+    __host__ __device__ __forceinline__ static const T *col_array(const Args &a, int i) {
+        return i == 0 ? a.w : a.b;
+    }
     template <int VEC> using Early = NoEarly;
     template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
-        pc.w.template load_cached_as<AL>(a.w + col);
-        pc.b.template load_cached_as<AL>(a.b + col);
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &,
+                                                    const LD & = LD{}) {}
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc,
+                                                     const LD &ld = LD{}) {
+        ld(pc.w, a.w, col, 0);
+        ld(pc.b, a.b, col, 1);
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[2], const PrePC<VEC> &,
@@ -192,17 +199,23 @@ template <typename TT> struct InductorChainT {
     template <int VEC> struct PrePC { Frag<T, VEC> bias; };
     template <int VEC> struct PostPC { Frag<T, VEC> gamma, beta; };
     static constexpr int kPostPC = 2;
+    static constexpr int kColArrays = 3;      // bias, gamma, beta (see LnGeluChain)
+    __host__ __device__ __forceinline__ static const T *col_array(const Args &a, int i) {
+        return i == 0 ? a.bias : i == 1 ? a.gamma : a.beta;
+    }
     template <int VEC> using Early = NoEarly;
     template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc) {
-        pc.bias.template load_cached_as<AL>(a.bias + col);
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_pre(const Args &a, int col, PrePC<VEC> &pc,
+                                                    const LD &ld = LD{}) {
+        ld(pc.bias, a.bias, col, 0);
     }
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
-        pc.gamma.template load_cached_as<AL>(a.gamma + col);
-        pc.beta.template load_cached_as<AL>(a.beta + col);
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc,
+                                                     const LD &ld = LD{}) {
+        ld(pc.gamma, a.gamma, col, 1);
+        ld(pc.beta, a.beta, col, 2);
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1],
@@ -311,6 +324,10 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC { Frag<T, VEC> w, b; };
     static constexpr int kPostPC = 2;
+    static constexpr int kColArrays = 2;      // w, b (see LnGeluChain)
+    __host__ __device__ __forceinline__ static const T *col_array(const Args &a, int i) {
+        return i == 0 ? a.w : a.b;
+    }
     // with dropout: the slot's 16-bit uniforms, drawn while the row is in
     // flight (they depend only on the element index)
     template <int VEC> struct EarlyDrop { DropBits<VEC> bits; };
@@ -319,12 +336,14 @@ template <typename TT, bool RES, bool DROP = false> struct LnActChain {
     __device__ __forceinline__ static void early(const Args &a, int64_t off, Early<VEC> &e) {
         if constexpr (DROP) dropout_bits<VEC, ANYOFF>(off, a.drop, e.bits);
     }
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc) {
-        pc.w.template load_cached_as<AL>(a.w + col);
-        pc.b.template load_cached_as<AL>(a.b + col);
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &,
+                                                    const LD & = LD{}) {}
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_post(const Args &a, int col, PostPC<VEC> &pc,
+                                                     const LD &ld = LD{}) {
+        ld(pc.w, a.w, col, 0);
+        ld(pc.b, a.b, col, 1);
     }
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[kInputs],
@@ -412,13 +431,17 @@ template <typename TT> struct SoftmaxChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC {};
     static constexpr int kPostPC = 0;
+    static constexpr int kColArrays = 0;      // no per-column values
+    __host__ __device__ __forceinline__ static const T *col_array(const Args &, int) { return nullptr; }
     template <int VEC> using Early = NoEarly;
     template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &,
+                                                    const LD & = LD{}) {}
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &,
+                                                     const LD & = LD{}) {}
     template <int VEC>
     __device__ __forceinline__ static void pre(const Frag<T, VEC> (&in)[1], const PrePC<VEC> &,
                                                const Args &, int64_t, int, float (&v)[VEC]) {
@@ -513,13 +536,17 @@ template <typename TT> struct ScaleMaskSoftmaxChain {
     template <int VEC> struct PrePC {};
     template <int VEC> struct PostPC {};
     static constexpr int kPostPC = 0;
+    static constexpr int kColArrays = 0;      // no per-column values
+    __host__ __device__ __forceinline__ static const T *col_array(const Args &, int) { return nullptr; }
     template <int VEC> using Early = NoEarly;
     template <int VEC, bool ANYOFF = false>
     __device__ __forceinline__ static void early(const Args &, int64_t, Early<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &) {}
-    template <int VEC, bool AL = true>
-    __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &) {}
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_pre(const Args &, int, PrePC<VEC> &,
+                                                    const LD & = LD{}) {}
+    template <int VEC, class LD = ColsGlobal<true>>
+    __device__ __forceinline__ static void load_post(const Args &, int, PostPC<VEC> &,
+                                                     const LD & = LD{}) {}
     // row mod period: on the device a multiply-high by the reciprocal gives
     // the quotient or one less (the reciprocal is rounded down and the row is
     // below 2^63), so one conditional subtraction finishes it

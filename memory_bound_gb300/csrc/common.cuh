@@ -327,6 +327,32 @@ template <typename T, int VEC> struct Frag {
     }
 };
 
+// Where a vector slot's per-column values come from (the chains' load_pre /
+// load_post hooks take one; `i` numbers the chain's per-column arrays).
+// ColsGlobal: the arrays in global memory through the read-only cache, one
+// 16-byte access per 16 bytes when AL (the slot's columns start on a 16-byte
+// boundary), else element by element.
+template <bool AL> struct ColsGlobal {
+    template <typename T, int VEC>
+    __device__ __forceinline__ void operator()(Frag<T, VEC> &f, const T *arr, int col,
+                                               int) const {
+        f.template load_cached_as<AL>(arr + col);
+    }
+};
+// ColsShared: the CTA's copy of every per-column array in shared memory,
+// starting at column h: array i's column c sits at s[i * stride + c - h], so a
+// slot whose columns start at h + k * VEC is one 16-byte aligned access when
+// s and stride * sizeof(T) are multiples of 16 bytes.
+template <typename T> struct ColsShared {
+    const T *s;
+    int stride;
+    int h;
+    template <int VEC>
+    __device__ __forceinline__ void operator()(Frag<T, VEC> &f, const T *, int col, int i) const {
+        f.load_shared(s + i * stride + (col - h));
+    }
+};
+
 // ---------------------------------------------------------------------------
 // reductions (every lane / thread ends with the bitwise-same value)
 // ---------------------------------------------------------------------------
@@ -395,6 +421,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// One 4-byte asynchronous copy from global to shared memory (both addresses
+// 4-byte aligned); it is complete for the issuing thread after cp_async_wait_all.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),
+                 "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

@@ -21,8 +21,10 @@ struct RowTuning {
     int stages;            // 0 = automatic
     int vpt;               // vector slots per thread, 0 = automatic
     // per-call planning inputs (set by the row engine, not by the override)
-    int no_bulk = 0;       // 1: some row input is not device memory, so no
-                           // bulk-async copies (the STAGED path) are planned
+    int no_bulk = 0;       // 1: some input that the planned copies would read is
+                           // not device memory, so no asynchronous copies into
+                           // shared memory are planned (the STAGED path, the
+                           // cluster ring, the shifted kernel's per-column copies)
     int outs = 1;          // full-size outputs written per row (2 with the
                            // LayerNorm family's residual-stream output)
     int read_pct = 100;    // share of each row's input elements read, on
@@ -58,9 +60,11 @@ cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 
 struct RowPlan {
     int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
     int slice = 0;     // cluster path: vectors of the row each CTA holds
-    int shift = 0;     // one-CTA path on rows off the 16-byte grid (shifted vectors)
+    int shift = 0;     // one-CTA path on rows off the 16-byte grid (shifted vectors):
+                       // 1, or 2 with the per-column values copied to shared memory
     int ring = 0;      // cluster path: staging ring depth (0: direct loads)
     int64_t cap = 0;   // CTAs (warp/CTA paths, at 256 threads for warp) or clusters resident at once
+    int64_t cap1 = 0;  // shift 2: CTAs of the same launch without the copies resident at once
 };
 
 // Chains implemented in their own translation units.  `launch == false`

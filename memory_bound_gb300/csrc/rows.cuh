@@ -35,7 +35,9 @@
 //     form a chain may ask for)
 //   rows_shift_kernel one CTA per row for rows off the 16-byte grid whose
 //                     tensors share one offset within 16 bytes: a short head,
-//                     whole 16-byte vectors, a short tail.
+//                     whole 16-byte vectors, a short tail; the per-column
+//                     values copied once per CTA into shared memory, aligned
+//                     to the CTA's rows (CS).
 //   rows_cluster_kernel / rows_cluster_smem_kernel  one thread-block cluster
 //                     per row, for rows longer than one CTA holds.
 // Several CTAs share an SM, each with its own row in flight, so one CTA's
@@ -43,6 +45,7 @@
 #pragma once
 
 #include <mutex>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -369,43 +372,91 @@ rows_cta_kernel_capped(const typename C::Args a, int64_t rows, int cols, int nst
 // at the same offset m0 within 16 bytes: each row splits into a head of h <
 // VEC elements up to its first 16-byte boundary, whole vectors from there,
 // and a tail of fewer than VEC elements.  The vectors take the vector hooks
-// with 16-byte row accesses and their per-column values loaded element by
-// element (those columns are off the grid); the head and tail elements take
-// the scalar hooks, one element per thread.  Persistent over rows like
-// rows_cta_kernel's direct path; the host guarantees cols >= 2 * VEC, so every
-// row holds at least one whole vector.
-template <class C, int VPT>
+// with 16-byte row accesses; the head and tail elements take the scalar hooks,
+// one element per thread.  Persistent over rows like rows_cta_kernel's direct
+// path; the host guarantees cols >= 2 * VEC, so every row holds at least one
+// whole vector.
+// A vector slot's per-column values start at column h + k * VEC, off the
+// 16-byte grid of the arrays.  Without CS they are loaded element by element;
+// with CS the CTA copies every per-column array, from column h on, into
+// shared memory (after the reduction header, each copy 16-byte aligned and
+// `cstride` elements long), so a slot's values are 16-byte shared-memory
+// loads.  The copy is made of 4-byte cp.async copies issued just before the
+// row's loads, so it lands while they are in flight; each thread waits for
+// its own copies before the first reduction, whose barrier publishes them
+// (chains with per-column values before the reduction wait, and take a
+// barrier, ahead of those loads).  h depends only on the row, and a grid of G
+// CTAs keeps each CTA on one h when G * cols * sizeof(T) is a multiple of 16
+// (the host rounds the grid so where the SM count allows); the copy is
+// redone, behind a barrier, whenever a CTA's h changes.  The host plans CS
+// for launches of several rows a CTA only (one row a CTA would copy as many
+// values as it reads).
+template <class C, int VPT, bool CS = false>
 __global__ void __launch_bounds__(kCtaMaxThreads)
 rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsigned *) {
     using T = typename C::T;
     constexpr int VEC = C::kVec;
     constexpr int NIN = C::kInputs;
     constexpr int ES = (int)sizeof(T);
-    constexpr bool kEarlyPost = VPT * VEC * C::kPostPC <= 8;
+    // with CS the epilogue reads its values from shared memory, and only
+    // chains with values before the reduction (kPreCols) wait for the copy
+    // ahead of it; the others let the first reduction's barrier publish it
+    constexpr bool kEarlyPost = !CS && VPT * VEC * C::kPostPC <= 8;
     using PrePC = typename C::template PrePC<VEC>;
     using PostPC = typename C::template PostPC<VEC>;
     using PrePC1 = typename C::template PrePC<1>;
     using PostPC1 = typename C::template PostPC<1>;
+    constexpr bool kPreCols = !std::is_empty_v<PrePC>;
     extern __shared__ __align__(1024) unsigned char smem[];
     float *red = reinterpret_cast<float *>(smem);                  // [2][32]
+    T *cs = reinterpret_cast<T *>(smem + kHdrBytes);   // CS: [kColArrays][cstride]
+    const int cstride = (cols + 15) & ~15;
     const int tid = threadIdx.x;
     const int T_ = (int)blockDim.x;
     const int64_t G = gridDim.x;
     pdl_wait();
     pdl_launch_dependents();
     int rb = 0;
+    int hs = -1;                                               // CS: h of the copy held
     for (int64_t row = blockIdx.x; row < rows; row += G) {
         const int64_t base = row * cols;
         // the row's first element sits `off` bytes past a 16-byte boundary
         const int off = (int)(((uint64_t)m0 + (uint64_t)base * (uint64_t)ES) & 15u);
         const int h = ((16 - off) & 15) / ES;                  // head elements
         const int nb = (cols - h) / VEC;                       // whole vectors (>= 1)
+        const auto vld = [&] {
+            if constexpr (CS) return ColsShared<T>{cs, cstride, h};
+            else return ColsGlobal<false>{};
+        }();
         const int ne = cols - nb * VEC;                        // head + tail elements
         const int ext = C::kPartialRows ? C::row_extent(a, row, cols) : cols;
         const bool has_e = tid < ne;
         const int col_e = tid < h ? tid : h + nb * VEC + (tid - h);
         const int64_t vbase = base + h;                        // first whole vector
 
+        // CS: a CTA meeting a new h starts its per-column copy (asynchronous
+        // 4-byte copies, no registers held while they fly; bf16 arrays whose
+        // column h is not 4-byte aligned are copied element by element)
+        const bool restage = CS && h != hs;                    // uniform across the CTA
+        if constexpr (CS) {
+            if (restage) {
+                if (hs >= 0) __syncthreads();   // every read of the old copy is done
+                const int n = cols - h;
+#pragma unroll
+                for (int i = 0; i < C::kColArrays; ++i) {
+                    const T *src = C::col_array(a, i) + h;
+                    T *dst = cs + i * cstride;
+                    if (ES == 4 || (reinterpret_cast<uintptr_t>(src) & 3u) == 0) {
+                        constexpr int PER = 4 / ES;             // elements per copy
+                        for (int m = tid; m < n / PER; m += T_)
+                            cp_async4(smem_addr(dst + m * PER), src + m * PER);
+                        if (PER == 2 && (n & 1) && tid == 0) dst[n - 1] = src[n - 1];
+                    } else {
+                        for (int j = tid; j < n; j += T_) dst[j] = src[j];
+                    }
+                }
+            }
+        }
         // every load before any use; vector slots past the row's last vector
         // re-read it (in bounds) and are masked below
         PrePC pre[VPT];
@@ -414,12 +465,26 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vc = min(tid + k * T_, nb - 1);
-            C::template load_pre<VEC, false>(a, h + vc * VEC, pre[k]);
-            if constexpr (kEarlyPost) C::template load_post<VEC, false>(a, h + vc * VEC, post[k]);
+            if constexpr (!CS) {
+                C::template load_pre<VEC>(a, h + vc * VEC, pre[k], vld);
+                if constexpr (kEarlyPost) C::template load_post<VEC>(a, h + vc * VEC, post[k], vld);
+            }
 #pragma unroll
             for (int i = 0; i < NIN; ++i)
                 in[k][i].load_stream_if(a.in[i] + vbase + (int64_t)vc * VEC,
                                         !C::kPartialRows || h + vc * VEC < ext);
+        }
+        if constexpr (CS && kPreCols) {
+            // the copies land while the row's loads are in flight
+            if (restage) {
+                cp_async_wait_all();
+                __syncthreads();
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int vc = min(tid + k * T_, nb - 1);
+                C::template load_pre<VEC>(a, h + vc * VEC, pre[k], vld);
+            }
         }
         PrePC1 pre_e;
         PostPC1 post_e;
@@ -458,6 +523,14 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
         if constexpr (C::kStorePre) {
             if (has_e) C::template store_pre<1>(ve, a, base + col_e);
         }
+        if constexpr (CS) {
+            // this thread's copies are done; the reduction's barrier makes
+            // every thread's visible before the epilogue reads them
+            if (restage) {
+                if constexpr (!kPreCols) cp_async_wait_all();
+                hs = h;
+            }
+        }
         const float r1 = C::kMaxFirst ? block_max(l1, red + 32 * rb) : block_sum(l1, red + 32 * rb);
         rb ^= 1;
         const float mean = C::stat1(r1, cols, a);
@@ -485,7 +558,7 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
                                           ea[k], o.f);
                 } else {
                     PostPC pc;
-                    C::template load_post<VEC, false>(a, h + vi * VEC, pc);
+                    C::template load_post<VEC>(a, h + vi * VEC, pc, vld);
                     C::template post<VEC>(v[k], mean, rstd, pc, a, vbase + (int64_t)vi * VEC,
                                           ea[k], o.f);
                 }
@@ -1029,18 +1102,30 @@ template <class C> struct RowEngine {
         return nullptr;
     }
 
-    // The shifted-vector kernel (rows off the 16-byte grid), vpt vector slots.
-    static const void *shift_fn(int vpt) {
-        if constexpr (C::kShiftOk) {
-            switch (vpt) {
-                case 1: return (const void *)rows_shift_kernel<C, 1>;
-                case 2: return (const void *)rows_shift_kernel<C, 2>;
-                case 4: return (const void *)rows_shift_kernel<C, 4>;
-                case 8: if constexpr (kVecN == 4) return (const void *)rows_shift_kernel<C, 8>;
-                        break;
-            }
+    // The shifted-vector kernel (rows off the 16-byte grid), vpt vector slots;
+    // cs: per-column arrays copied to shared memory (chains that have some).
+    template <bool CS> static const void *shift_fn_cs(int vpt) {
+        switch (vpt) {
+            case 1: return (const void *)rows_shift_kernel<C, 1, CS>;
+            case 2: return (const void *)rows_shift_kernel<C, 2, CS>;
+            case 4: return (const void *)rows_shift_kernel<C, 4, CS>;
+            case 8: if constexpr (kVecN == 4) return (const void *)rows_shift_kernel<C, 8, CS>;
+                    break;
         }
         return nullptr;
+    }
+    static const void *shift_fn(int vpt, bool cs) {
+        if constexpr (C::kShiftOk) {
+            if constexpr (C::kColArrays > 0) {
+                if (cs) return shift_fn_cs<true>(vpt);
+            }
+            return shift_fn_cs<false>(vpt);
+        }
+        return nullptr;
+    }
+    // Shared memory of the shifted kernel's per-column copies (its CS form).
+    static int64_t shift_col_bytes(int cols) {
+        return (int64_t)C::kColArrays * (((int64_t)cols + 15) & ~(int64_t)15) * (int64_t)sizeof(T);
     }
 
     // The cluster kernel for a launch of `threads` threads: the 512-thread
@@ -1309,6 +1394,31 @@ template <class C> struct RowEngine {
         return c;
     }
 
+    // The one-CTA engines' grid for `rows` rows on `cap` resident CTAs.
+    // Balanced: as many row rounds as the full grid needs, but only as many
+    // CTAs as those rounds need, so the last round is not mostly idle (8192
+    // rows on 608 slots: 14 rounds on 586 CTAs, not 13.5 on 608).  With the
+    // shifted kernel's per-column copies (cs), a multiple of the period of
+    // the rows' offsets within 16 bytes where the cap allows, so that each CTA
+    // meets one offset and makes its copy once (the cap, SMs x CTAs per SM,
+    // is a multiple of 8 on 152 SMs; elsewhere the copy is redone as a CTA's
+    // offset changes).
+    static int64_t cta_grid(int64_t rows, int64_t cap, int cols, bool cs) {
+        int64_t grid = rows < cap ? rows : cap;
+        if (grid > 0) {
+            const int64_t rounds = (rows + grid - 1) / grid;
+            grid = (rows + rounds - 1) / rounds;
+        }
+        if (cs && rows > grid) {
+            const int64_t step = ((int64_t)cols * (int64_t)sizeof(T)) & 15;
+            int64_t period = 1;
+            while ((step * period) & 15) period *= 2;
+            const int64_t up = (grid + period - 1) / period * period;
+            if (grid > period && up <= cap) grid = up;
+        }
+        return grid;
+    }
+
     static mb_status plan(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows, int cols,
                           int aligned, RowPlan *p, const void **fn) {
         RowPlan core;
@@ -1350,14 +1460,14 @@ template <class C> struct RowEngine {
             const int64_t ncl = rows < core.cap ? rows : core.cap;
             p->ctas = (int)(ncl * core.stages);
         } else {
-            // Balanced grid: as many row rounds as the full grid needs, but
-            // only as many CTAs as those rounds need.
-            int64_t grid = rows < core.cap ? rows : core.cap;
-            if (grid > 0) {
-                const int64_t rounds = (rows + grid - 1) / grid;
-                grid = (rows + rounds - 1) / rounds;
+            if (core.shift == 2 && rows <= core.cap1) {
+                // one row per CTA: copying the per-column values would cost
+                // as much as reading them once, so the kernel without copies
+                *fn = shift_fn(core.vpt, false);
+                p->shift = 1;
+                p->smem = kHdrBytes;
             }
-            p->ctas = (int)grid;
+            p->ctas = (int)cta_grid(rows, core.cap, cols, p->shift == 2);
         }
         return MB_OK;
     }
@@ -1433,7 +1543,10 @@ template <class C> struct RowEngine {
         const bool staged = path == MB_ROW_STAGED;
         const bool shifted = shift && path == MB_ROW_DIRECT;
         const int nvec_cta = shifted ? nvec_shift : nvec;
-        const int smem1 = kHdrBytes + (staged ? stage_bytes : 0);
+        // shifted rows read their per-column values from a shared-memory copy
+        // when the chain has some and the copy fits one CTA (see below)
+        bool cstage = shifted && C::kColArrays > 0 && !tun.no_bulk &&
+                      kHdrBytes + shift_col_bytes(cols) <= ctx.smem_optin;
         const int64_t row_io =
             ((int64_t)C::kInputs * cols * (staged ? tun.read_pct : 100) / 100 +
              (int64_t)tun.outs * cols) *
@@ -1443,39 +1556,62 @@ template <class C> struct RowEngine {
         if (want_rows > kMaxRowsInFlight) want_rows = kMaxRowsInFlight;
         int target = want_rows < 2 ? 2 : (int)want_rows;
         if (C::kRowsTarget > 0) target = C::kRowsTarget;     // the chain's own measured target
-        int best_vpt = 0, best_occ = 0, best_threads = 0;
-        bool best_spills = true;
-        for (int cand = 1; cand <= max_vpt(vec || shifted); cand *= 2) {
-            if (tun.vpt > 0 && cand != tun.vpt) continue;
-            if (ceil_div(nvec_cta, cand) > kCtaMaxThreads) continue;
-            const int threads = round_up32(ceil_div(nvec_cta, cand));
-            const void *f = shifted ? shift_fn(cand) : cta_fn(cand, vec, staged);
-            if (!f) continue;
-            int max_threads = 0;
-            bool spills = false;
-            mb_status st = kernel_limits(f, &max_threads, &spills);
-            if (st != MB_OK) return st;
-            if (threads > max_threads) continue;          // the kernel's launch bound
-            int occ = 0;
-            st = occupancy(ctx, f, threads, smem1, &occ);
-            if (st != MB_OK) return st;
-            if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
-            if (occ < 1) continue;
-            const int rows_in_flight = occ < target ? occ : target;
-            const int best_rows = best_occ < target ? best_occ : target;
-            // a spilling kernel only when no other serves; then the most rows
-            // in flight, tie-broken on threads per SM, counting the CTAs that
-            // will be resident once the target caps them
-            const bool better =
-                best_vpt == 0 || (best_spills && !spills) ||
-                (spills == best_spills &&
-                 (rows_in_flight > best_rows ||
-                  (rows_in_flight == best_rows &&
-                   rows_in_flight * threads > best_rows * best_threads)));
-            if (better) {
-                best_vpt = cand; best_occ = occ; best_threads = threads; best_spills = spills;
+        struct Pick {
+            int vpt = 0, occ = 0, threads = 0;
+            bool spills = true;
+        };
+        auto pick = [&](bool cs, Pick &best) -> mb_status {
+            const int smem_q = kHdrBytes + (staged ? stage_bytes : 0) +
+                               (cs ? (int)shift_col_bytes(cols) : 0);
+            for (int cand = 1; cand <= max_vpt(vec || shifted); cand *= 2) {
+                if (tun.vpt > 0 && cand != tun.vpt) continue;
+                if (ceil_div(nvec_cta, cand) > kCtaMaxThreads) continue;
+                const int threads = round_up32(ceil_div(nvec_cta, cand));
+                const void *f = shifted ? shift_fn(cand, cs) : cta_fn(cand, vec, staged);
+                if (!f) continue;
+                int max_threads = 0;
+                bool spills = false;
+                mb_status st = kernel_limits(f, &max_threads, &spills);
+                if (st != MB_OK) return st;
+                if (threads > max_threads) continue;          // the kernel's launch bound
+                int occ = 0;
+                st = occupancy(ctx, f, threads, smem_q, &occ);
+                if (st != MB_OK) return st;
+                if (tun.ctas_per_sm > 0 && tun.ctas_per_sm < occ) occ = tun.ctas_per_sm;
+                if (occ < 1) continue;
+                const int rows_in_flight = occ < target ? occ : target;
+                const int best_rows = best.occ < target ? best.occ : target;
+                // a spilling kernel only when no other serves; then the most
+                // rows in flight, tie-broken on threads per SM, counting the
+                // CTAs that will be resident once the target caps them
+                const bool better =
+                    best.vpt == 0 || (best.spills && !spills) ||
+                    (spills == best.spills &&
+                     (rows_in_flight > best_rows ||
+                      (rows_in_flight == best_rows &&
+                       rows_in_flight * threads > best_rows * best.threads)));
+                if (better) best = Pick{cand, occ, threads, spills};
+            }
+            return MB_OK;
+        };
+        Pick best;
+        mb_status pst = pick(cstage, best);
+        if (pst != MB_OK) return pst;
+        if (cstage) {
+            // The copies take shared memory (w and b of an fp32 row of 16383:
+            // 128 KB a CTA): they are kept unless the kernel without them
+            // keeps more rows in flight, or spills where they would.
+            Pick plain;
+            if ((pst = pick(false, plain)) != MB_OK) return pst;
+            const int rc = best.occ < target ? best.occ : target;
+            const int rp = plain.occ < target ? plain.occ : target;
+            if (plain.vpt && (!best.vpt || (best.spills && !plain.spills) ||
+                              (best.spills == plain.spills && rp > rc))) {
+                best = plain;
+                cstage = false;
             }
         }
+        int best_vpt = best.vpt, best_occ = best.occ, best_threads = best.threads;
         if (tun.ctas_per_sm <= 0 && best_occ > target) best_occ = target;
         if (!best_vpt && tun.vpt > 0) {
             RowTuning t2 = tun;
@@ -1498,8 +1634,9 @@ template <class C> struct RowEngine {
             stages = want;
             smem = kHdrBytes + stages * stage_bytes;
         }
-        *fn = shifted ? shift_fn(best_vpt) : cta_fn(best_vpt, vec, staged);
+        *fn = shifted ? shift_fn(best_vpt, cstage) : cta_fn(best_vpt, vec, staged);
         if (shifted) { p->vec = kVecN; p->shift = 1; }
+        if (cstage) { smem = kHdrBytes + (int)shift_col_bytes(cols); p->shift = 2; }
         int occ2 = 0;
         mb_status st = occupancy(ctx, *fn, best_threads, smem, &occ2);
         if (st != MB_OK) return st;
@@ -1507,17 +1644,16 @@ template <class C> struct RowEngine {
         if (occ < 1) occ = 1;
         const int64_t cap = (int64_t)occ * ctx.sm_count;
         p->cap = cap;
-        // Balanced grid: as many row rounds as the full grid needs, but only
-        // as many CTAs as those rounds need, so the last round is not mostly
-        // idle (8192 rows on 608 slots: 14 rounds on 586 CTAs, not 13.5 on 608).
-        int64_t grid = rows < cap ? rows : cap;
-        if (grid > 0) {
-            const int64_t rounds = (rows + grid - 1) / grid;
-            grid = (rows + rounds - 1) / rounds;
+        if (cstage) {
+            // a launch of one row per CTA skips the copies (plan() below)
+            int occ1 = 0;
+            st = occupancy(ctx, shift_fn(best_vpt, false), best_threads, kHdrBytes, &occ1);
+            if (st != MB_OK) return st;
+            p->cap1 = (int64_t)(occ1 < occ ? occ1 : occ) * ctx.sm_count;
         }
         p->path = path; p->threads = best_threads; p->vpt = best_vpt; p->stages = stages;
         p->smem = smem;
-        p->ctas = (int)grid;
+        p->ctas = (int)cta_grid(rows, cap, cols, p->shift == 2);
         return MB_OK;
     }
 
@@ -1530,11 +1666,18 @@ template <class C> struct RowEngine {
         tn.read_pct = C::read_percent(a, rows, cols);
         mb_status st = plan(ctx, tn, rows, cols, aligned, &p, &fn);
         if (st != MB_OK) return st;
-        if (launch && (p.path == MB_ROW_STAGED || (p.path == MB_ROW_CLUSTER && p.ring > 0))) {
-            // Bulk-async copies read device memory only: rows held in host
-            // memory (pinned, read over the host link) take a plain-load path.
+        if (launch &&
+            (p.path == MB_ROW_STAGED || (p.path == MB_ROW_CLUSTER && p.ring > 0) || p.shift == 2)) {
+            // Asynchronous copies into shared memory are planned for device
+            // memory only: rows (bulk copies) or per-column arrays (the
+            // shifted kernel's copies) held in host memory (pinned, read over
+            // the host link) take a plain-load path.
             bool dev = true;
-            for (int i = 0; i < C::kInputs; ++i) dev = dev && device_resident(a.in[i]);
+            if (p.shift == 2) {
+                for (int i = 0; i < C::kColArrays; ++i) dev = dev && device_resident(C::col_array(a, i));
+            } else {
+                for (int i = 0; i < C::kInputs; ++i) dev = dev && device_resident(a.in[i]);
+            }
             if (!dev) {
                 RowTuning t2 = tn;
                 t2.no_bulk = 1;

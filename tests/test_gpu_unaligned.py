@@ -258,3 +258,116 @@ def test_scalar_reach_and_cluster_boundary():
         p = mb.row_plan("ln", "f32", 64, cols, aligned=2)
         assert p["path"] == "direct" and p["vec"] == 4, p
     assert mb.row_plan("ln", "f32", 64, 32769, aligned=2)["path"] == "cluster"
+
+
+def _multi_round_rows(chain, dt, cols):
+    """A row count that gives every CTA of the shifted launch two or three
+    rows (the per-column copies are planned from two rows a CTA on)."""
+    cap = mb.row_plan(chain, dt, 1 << 22, cols, aligned=2)["ctas"]
+    return 2 * cap + 5
+
+
+@pytest.mark.parametrize("cols", [1031, 4099])
+@pytest.mark.parametrize("chain", ["ln", "inductor", "lnact_h", "lnact_dropout"])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+@pytest.mark.parametrize("col_off", [0, 1], ids=["cols16", "cols_off"])
+def test_shifted_column_copies(cols, chain, bf16, col_off):
+    """The shifted kernel with its per-column arrays copied to shared memory
+    (several rows a CTA): every chain that has such arrays, inputs and outputs
+    at a common offset of one element, the per-column arrays 16-byte aligned
+    or one element off (bf16: copied element by element where column h is not
+    4-byte aligned), every element against the oracle."""
+    dt = "bf16" if bf16 else "f32"
+    pchain = {"ln": "ln", "inductor": "inductor", "lnact_h": "lnact_res_h",
+              "lnact_dropout": "lnact_res_dropout"}[chain]
+    rows, off = _multi_round_rows(pchain, dt, cols), 1
+    es = 2 if bf16 else 4
+    plan = mb.row_plan(pchain, dt, rows, cols, aligned=2)
+    narr = 3 if chain == "inductor" else 2
+    assert plan["path"] == "direct" and plan["vec"] in (8, 16 // es), plan
+    assert plan["smem"] == 1024 + narr * ((cols + 15) // 16 * 16) * es, plan   # the copies
+    seed = cols + 17
+    x = synth.normal(seed, 0, (rows, cols), dtype=dt)
+    if chain == "inductor":
+        bias = synth.normal(seed, 1, (cols,), 0.0, 0.1, dtype=dt)
+        gamma = synth.uniform(seed, 2, (cols,), 0.5, 1.5, dtype=dt)
+        beta = synth.normal(seed, 3, (cols,), 0.0, 0.1, dtype=dt)
+        y = _out_like(x, bf16, off)
+        mb.fused_bias_relu_branch_mean_epilogue(
+            _dev(x, bf16, off), _dev(bias, bf16, col_off), _dev(gamma, bf16, col_off),
+            _dev(beta, bf16, col_off), 1.1, 0.1, out=y)
+        want = (oracle.bias_relu_branch_mean_epilogue_bf16(x, bias, gamma, beta) if bf16
+                else oracle.bias_relu_branch_mean_epilogue(x, bias, gamma, beta))
+        assert_close(to_host(y), want, bf16=bf16, what=f"inductor {cols}")
+        return
+    w, b = _vecs(cols, seed, bf16)
+    wd, bd = _dev(w, bf16, col_off), _dev(b, bf16, col_off)
+    if chain == "ln":
+        r = synth.normal(seed, 1, (rows, cols), dtype=dt)
+        out = _out_like(x, bf16, off)
+        mb.fused_residual_layernorm_gelu(_dev(x, bf16, off), _dev(r, bf16, off), wd, bd, 1e-5,
+                                         out=out)
+        assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5), bf16=bf16,
+                     what=f"ln {cols}")
+    elif chain == "lnact_h":
+        r = synth.normal(seed, 1, (rows, cols), dtype=dt)
+        out, h = _out_like(x, bf16, off), _out_like(x, bf16, off)
+        mb.fused_layernorm_act(_dev(x, bf16, off), _dev(r, bf16, off), wd, bd, act="gelu_tanh",
+                               out=out, h_out=h)
+        want, want_h = oracle.layernorm_act(x, r, w, b, 1e-5, oracle.ACT_GELU, want_h=True)
+        assert_close(to_host(out), want, bf16=bf16, what=f"lnact {cols}")
+        assert_bitexact(to_host(h), want_h, f"h {cols}")
+    else:
+        r = synth.normal(seed, 1, (rows, cols), dtype=dt)
+        p, dseed, goff = 0.2, 77, 5
+        out = _out_like(x, bf16, off)
+        mean = torch.empty(rows, device="cuda")
+        rstd = torch.empty(rows, device="cuda")
+        mb.fused_layernorm_act(_dev(x, bf16, off), _dev(r, bf16, off), wd, bd, act="relu",
+                               out=out, p=p, seed=dseed, offset=goff, mean_out=mean,
+                               rstd_out=rstd)
+        want, _, wm, wr = oracle.layernorm_act_ex(x, r, w, b, 1e-5, oracle.ACT_RELU, p=p,
+                                                  seed=dseed, offset=goff, want_stats=True)
+        keep = oracle.dropout_mask(dseed, goff, 0, x.size, p).reshape(x.shape)
+        got = to_host(out)
+        g = bf16_to_f64(got) if bf16 else got.astype(np.float64)
+        assert np.all(g[~keep] == 0), "a dropped element is not zero"
+        assert_close(got, want, bf16=bf16, what=f"dropout {cols}")
+        m, rs = to_host(mean).astype(np.float64), to_host(rstd).astype(np.float64)
+        assert np.all(np.abs(m - wm) <= 1e-5 / wr + 1e-7 * np.abs(wm))
+        assert np.all(np.abs(rs - wr) <= 1e-5 * wr)
+
+
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_shifted_column_copies_planning(bf16):
+    """The copies are planned for launches of several rows a CTA, not for one
+    row a CTA (there a copy costs as much as reading the values once), not
+    for chains without per-column arrays, and not where they would not fit
+    one CTA's shared memory (fp32 rows of 32767: 256 KB for w and b)."""
+    dt = "bf16" if bf16 else "f32"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for chain in ("ln", "inductor", "lnact", "lnact_res_dropout"):
+        cap = mb.row_plan(chain, dt, 1 << 22, 4099, aligned=2)["ctas"]
+        assert mb.row_plan(chain, dt, sms, 4099, aligned=2)["smem"] == 1024
+        assert mb.row_plan(chain, dt, cap + 1, 4099, aligned=2)["smem"] > 1024
+        # aligned rows keep their engines
+        assert mb.row_plan(chain, dt, 4 * cap, 4096, aligned=1)["vec"] in (4, 8)
+    assert mb.row_plan("softmax", dt, 1 << 20, 4099, aligned=2)["smem"] == 1024
+    big = mb.row_plan("ln", dt, 1 << 20, 32767, aligned=2)
+    assert big["path"] == "direct" and (big["smem"] == 1024) == (not bf16), big
+
+
+def test_shifted_column_copies_host_vectors():
+    """Per-column arrays in pinned host memory: the launch takes the kernel
+    without copies (asynchronous copies are planned for device memory only)
+    and still matches the oracle."""
+    cols = 4099
+    rows = _multi_round_rows("ln", "f32", cols)
+    x, r = _rows(rows, cols, 5, False, 2)
+    w, b = _vecs(cols, 5, False)
+    hw, hb = (torch.from_numpy(v.copy()).pin_memory() for v in (w, b))
+    out = _out_like(x, False, 1)
+    mb.fused_residual_layernorm_gelu(_dev(x, False, 1), _dev(r, False, 1), hw, hb, 1e-5, out=out)
+    torch.cuda.synchronize()
+    assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5),
+                 what="host w, b")
