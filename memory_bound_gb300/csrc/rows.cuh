@@ -66,6 +66,11 @@ constexpr int kCappedRegs = 40;   // registers per thread of rows_cta_kernel_cap
 // loop, as in the two-slot bf16 LayerNorm kernel at 32 registers) cost nothing
 // measurable; the forms they pass over spill hundreds.
 constexpr size_t kSpillTolerance = 64;
+// The same for the shifted-vector kernel, whose forms keep 16-20 bytes (the
+// dropout chains' four-slot forms, measured no slower than the others) or
+// spill 60 and more (eight slots of LayerNorm + residual, fp32 rows of 6147:
+// 30% slower at three CTAs an SM than two CTAs of two slots without spills).
+constexpr size_t kShiftSpillTolerance = 32;
 // Bytes of row reads and writes per SM in flight that keep HBM busy; the
 // planner aims for this many bytes' worth of resident rows, rounded to the
 // nearest row count (sweeps on GB300, fp32: LayerNorm rows of 48 KB in + out
@@ -1033,13 +1038,14 @@ template <class C> struct RowEngine {
     }
     // Vector slots per thread allowed on the CTA engine: VPT * VEC <= 32.
     static int max_vpt(bool vec) { return vec ? 32 / kVecN : 32; }
-    // A kernel's launch bound and whether it spills beyond kSpillTolerance.
-    static mb_status kernel_limits(const void *f, int *max_threads, bool *spills) {
+    // A kernel's launch bound and whether it spills beyond `tolerance` bytes.
+    static mb_status kernel_limits(const void *f, int *max_threads, bool *spills,
+                                   size_t tolerance = kSpillTolerance) {
         cudaFuncAttributes fa;
         const cudaError_t e = cudaFuncGetAttributes(&fa, f);
         if (e != cudaSuccess) return cuda_fail(e);
         *max_threads = fa.maxThreadsPerBlock;
-        *spills = fa.localSizeBytes > kSpillTolerance;
+        *spills = fa.localSizeBytes > tolerance;
         return MB_OK;
     }
     // Threads per CTA of the one-warp-per-row engine: with at most
@@ -1551,7 +1557,12 @@ template <class C> struct RowEngine {
             ((int64_t)C::kInputs * cols * (staged ? tun.read_pct : 100) / 100 +
              (int64_t)tun.outs * cols) *
             (int64_t)sizeof(T);
-        const int64_t budget = sizeof(T) == 2 ? kFlightBytesBf16 : kFlightBytesF32;
+        // The shifted kernel loads its rows straight into registers; with two
+        // row inputs its fp32 rows keep HBM busy only from the bf16 budget on
+        // (sweeps on GB300, LayerNorm + residual rows of 2051 to 8195 fp32
+        // values: fastest at 8, 5, 4, 3 and 2 rows an SM).
+        const int64_t budget = sizeof(T) == 2 || (shifted && C::kInputs == 2)
+                                   ? kFlightBytesBf16 : kFlightBytesF32;
         int64_t want_rows = row_io > 0 ? (budget + row_io / 2) / row_io : kMaxRowsInFlight;
         if (want_rows > kMaxRowsInFlight) want_rows = kMaxRowsInFlight;
         int target = want_rows < 2 ? 2 : (int)want_rows;
@@ -1567,11 +1578,16 @@ template <class C> struct RowEngine {
                 if (tun.vpt > 0 && cand != tun.vpt) continue;
                 if (ceil_div(nvec_cta, cand) > kCtaMaxThreads) continue;
                 const int threads = round_up32(ceil_div(nvec_cta, cand));
+                // shifted rows: no CTA of fewer than four warps where the row
+                // allows more (LayerNorm + residual, fp32 rows of 2051: eight
+                // CTAs of 96 threads an SM ran 13% slower than five of 288)
+                if (shifted && threads < 128 && nvec_cta >= 128) continue;
                 const void *f = shifted ? shift_fn(cand, cs) : cta_fn(cand, vec, staged);
                 if (!f) continue;
                 int max_threads = 0;
                 bool spills = false;
-                mb_status st = kernel_limits(f, &max_threads, &spills);
+                mb_status st = kernel_limits(f, &max_threads, &spills,
+                                             shifted ? kShiftSpillTolerance : kSpillTolerance);
                 if (st != MB_OK) return st;
                 if (threads > max_threads) continue;          // the kernel's launch bound
                 int occ = 0;
