@@ -1014,6 +1014,14 @@ inline cudaError_t allow_smem(const void *fn, const LaunchCtx &ctx, int bytes) {
                                 ctx.smem_optin - (int)fa.sharedSizeBytes);
 }
 
+// The shifted kernel's form with per-column copies (CS) for chain C and vpt
+// slots, or nullptr: defined and instantiated in the rows_shift_cs_*.cu units
+// only.  In a chain's own unit those kernels changed how ptxas allocated that
+// unit's other kernels (the two-slot staged bf16 LayerNorm kernel went from 32
+// registers and an 8-byte stack to 38 registers: three 512-thread CTAs an SM
+// instead of four).
+template <class C> const void *shift_cs_fn(int vpt);
+
 template <class C> struct RowEngine {
     using T = typename C::T;
     static constexpr int kVecN = C::kVec;     // elements per vector slot
@@ -1110,22 +1118,18 @@ template <class C> struct RowEngine {
 
     // The shifted-vector kernel (rows off the 16-byte grid), vpt vector slots;
     // cs: per-column arrays copied to shared memory (chains that have some).
-    template <bool CS> static const void *shift_fn_cs(int vpt) {
-        switch (vpt) {
-            case 1: return (const void *)rows_shift_kernel<C, 1, CS>;
-            case 2: return (const void *)rows_shift_kernel<C, 2, CS>;
-            case 4: return (const void *)rows_shift_kernel<C, 4, CS>;
-            case 8: if constexpr (kVecN == 4) return (const void *)rows_shift_kernel<C, 8, CS>;
-                    break;
-        }
-        return nullptr;
-    }
     static const void *shift_fn(int vpt, bool cs) {
         if constexpr (C::kShiftOk) {
             if constexpr (C::kColArrays > 0) {
-                if (cs) return shift_fn_cs<true>(vpt);
+                if (cs) return shift_cs_fn<C>(vpt);
             }
-            return shift_fn_cs<false>(vpt);
+            switch (vpt) {
+                case 1: return (const void *)rows_shift_kernel<C, 1>;
+                case 2: return (const void *)rows_shift_kernel<C, 2>;
+                case 4: return (const void *)rows_shift_kernel<C, 4>;
+                case 8: if constexpr (kVecN == 4) return (const void *)rows_shift_kernel<C, 8>;
+                        break;
+            }
         }
         return nullptr;
     }

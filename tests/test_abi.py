@@ -231,3 +231,22 @@ def test_library_build_depends_on_its_build_script(tmp_path, monkeypatch):
         assert not b._up_to_date()
     finally:
         os.utime(script, (st.st_atime, st.st_mtime))
+
+
+def test_dominant_kernel_fits_four_ctas_an_sm(tmp_path):
+    """The two-slot staged bf16 LayerNorm kernel (the 32768 x 8192 bench row's
+    kernel) compiles to at most 32 registers a thread, so four 512-thread CTAs
+    share an SM; kernels added to its translation unit have pushed ptxas to 38
+    (three CTAs) before.  Reads only ptxas's resource report."""
+    import subprocess
+    src = os.path.join(lib_build.CSRC, "rows_ln_bf16.cu")
+    res = subprocess.run([lib_build.NVCC, *lib_build.ARCH, *lib_build.FLAGS, "-Xptxas", "-v",
+                          "-c", src, "-o", str(tmp_path / "ln_bf16.o")],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr[-2000:]
+    name = "rows_cta_kernelINS_11LnGeluChainItEELi2ELi8ELb1EE"
+    blocks = re.split(r"Compiling entry function '", res.stderr)
+    block = [b for b in blocks if b.split("'")[0].find(name) >= 0]
+    assert len(block) == 1, "kernel not found in the ptxas report"
+    regs = int(re.search(r"Used (\d+) registers", block[0]).group(1))
+    assert regs <= 32, f"{regs} registers"
