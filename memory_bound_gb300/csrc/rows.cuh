@@ -396,13 +396,21 @@ rows_cta_kernel_capped(const typename C::Args a, int64_t rows, int cols, int nst
 // redone, behind a barrier, whenever a CTA's h changes.  The host plans CS
 // for launches of several rows a CTA only (one row a CTA would copy as many
 // values as it reads).
-template <class C, int VPT, bool CS = false>
+// STG (with CS): the rows' whole vectors are streamed into a ring of nstage
+// shared-memory stages by bulk copies, as on rows_cta_kernel's staged path:
+// a row's vector body starts on a 16-byte boundary and is a whole number of
+// 16-byte words, so one bulk copy per input moves it; head and tail elements
+// stay plain loads.  The fourth argument then carries m0 | nstage << 8.
+template <class C, int VPT, bool CS = false, bool STG = false>
 __global__ void __launch_bounds__(kCtaMaxThreads)
-rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsigned *) {
+rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0_arg, unsigned *err) {
+    static_assert(!STG || CS, "the staged form is planned with the per-column copies");
     using T = typename C::T;
     constexpr int VEC = C::kVec;
     constexpr int NIN = C::kInputs;
     constexpr int ES = (int)sizeof(T);
+    const int m0 = m0_arg & 15;
+    const int nstage = STG ? m0_arg >> 8 : 0;
     // with CS the epilogue reads its values from shared memory, and only
     // chains with values before the reduction (kPreCols) wait for the copy
     // ahead of it; the others let the first reduction's barrier publish it
@@ -414,16 +422,55 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
     constexpr bool kPreCols = !std::is_empty_v<PrePC>;
     extern __shared__ __align__(1024) unsigned char smem[];
     float *red = reinterpret_cast<float *>(smem);                  // [2][32]
+    volatile int *abort_flag = reinterpret_cast<int *>(smem + 256); // STG: [2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 512);     // STG: [kMaxStages]
     T *cs = reinterpret_cast<T *>(smem + kHdrBytes);   // CS: [kColArrays][cstride]
     const int cstride = (cols + 15) & ~15;
+    // STG: the ring, [nstage][NIN][cstride] after the per-column copies
+    unsigned char *ring = smem + kHdrBytes + (size_t)C::kColArrays * cstride * ES;
+    const uint32_t stage_bytes = (uint32_t)NIN * (uint32_t)cstride * (uint32_t)ES;
     const int tid = threadIdx.x;
     const int T_ = (int)blockDim.x;
     const int64_t G = gridDim.x;
+    const int64_t first = blockIdx.x;
+    const int64_t nlocal = STG && first < rows ? (rows - first + G - 1) / G : 0;   // STG
+    if constexpr (STG) {
+        if (tid == 0) {
+            abort_flag[0] = 0;
+            abort_flag[1] = 0;
+            for (int q = 0; q < nstage; ++q) mbar_init(smem_addr(&bars[q]), 1);
+            fence_mbar_init();
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
+    // STG: refill stage q with local row li's whole vectors (one elected thread)
+    auto issue = [&](int q, int64_t li) {
+        const int64_t row = first + li * G;
+        const int64_t base = row * cols;
+        const int off = (int)(((uint64_t)m0 + (uint64_t)base * (uint64_t)ES) & 15u);
+        const int h = ((16 - off) & 15) / ES;
+        const uint32_t bytes = (uint32_t)((cols - h) / VEC * VEC) * (uint32_t)ES;
+        const uint32_t bar = smem_addr(&bars[q]);
+        mbar_arrive_expect_tx(bar, (uint32_t)NIN * bytes);
+#pragma unroll
+        for (int i = 0; i < NIN; ++i)
+            bulk_g2s(smem_addr(ring + (size_t)q * stage_bytes + (size_t)i * cstride * ES),
+                     a.in[i] + base + h, bytes, bar);
+    };
+    if constexpr (STG) {
+        __syncthreads();        // the barriers are initialised
+        if (tid == 0) {
+            const int64_t n0 = nlocal < nstage ? nlocal : nstage;
+            for (int q = 0; q < (int)n0; ++q) issue(q, q);
+        }
+    }
     int rb = 0;
     int hs = -1;                                               // CS: h of the copy held
-    for (int64_t row = blockIdx.x; row < rows; row += G) {
+    int sq = 0;                 // STG: ring stage of local row li
+    uint32_t parity = 0;        // STG: its phase parity
+    int64_t li = 0;             // STG: the CTA's rows done
+    for (int64_t row = first; row < rows; row += G) {
         const int64_t base = row * cols;
         // the row's first element sits `off` bytes past a 16-byte boundary
         const int off = (int)(((uint64_t)m0 + (uint64_t)base * (uint64_t)ES) & 15u);
@@ -467,6 +514,35 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
         PrePC pre[VPT];
         PostPC post[kEarlyPost ? VPT : 1];
         Frag<T, VEC> in[VPT][NIN];
+        PrePC1 pre_e;
+        PostPC1 post_e;
+        Frag<T, 1> in_e[NIN];
+        typename C::template Early<VEC> ea[VPT];
+        typename C::template Early<1> ea_e;
+        if constexpr (STG) {
+            // head and tail elements, and the values the epilogue needs that
+            // do not depend on the row's data, before the ring wait (their
+            // work hides it); the unstaged form takes them after its loads
+            if (has_e) {
+                C::template load_pre<1>(a, col_e, pre_e);
+                C::template load_post<1>(a, col_e, post_e);
+#pragma unroll
+                for (int i = 0; i < NIN; ++i) in_e[i].load_stream(a.in[i] + base + col_e);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NIN; ++i) in_e[i].f[0] = 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+                C::template early<VEC, true>(a, vbase + (int64_t)min(tid + k * T_, nb - 1) * VEC,
+                                             ea[k]);
+            C::template early<1>(a, base + (has_e ? col_e : 0), ea_e);
+        }
+        const T *stage = nullptr;
+        if constexpr (STG) {
+            if (!mbar_wait_bounded(smem_addr(&bars[sq]), parity)) abort_flag[li & 1] = 1;
+            stage = reinterpret_cast<const T *>(ring + (size_t)sq * stage_bytes);
+        }
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vc = min(tid + k * T_, nb - 1);
@@ -475,9 +551,11 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
                 if constexpr (kEarlyPost) C::template load_post<VEC>(a, h + vc * VEC, post[k], vld);
             }
 #pragma unroll
-            for (int i = 0; i < NIN; ++i)
-                in[k][i].load_stream_if(a.in[i] + vbase + (int64_t)vc * VEC,
-                                        !C::kPartialRows || h + vc * VEC < ext);
+            for (int i = 0; i < NIN; ++i) {
+                if constexpr (STG) in[k][i].load_shared(stage + (size_t)i * cstride + vc * VEC);
+                else in[k][i].load_stream_if(a.in[i] + vbase + (int64_t)vc * VEC,
+                                             !C::kPartialRows || h + vc * VEC < ext);
+            }
         }
         if constexpr (CS && kPreCols) {
             // the copies land while the row's loads are in flight
@@ -491,25 +569,24 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
                 C::template load_pre<VEC>(a, h + vc * VEC, pre[k], vld);
             }
         }
-        PrePC1 pre_e;
-        PostPC1 post_e;
-        Frag<T, 1> in_e[NIN];
-        if (has_e) {
-            C::template load_pre<1>(a, col_e, pre_e);
-            C::template load_post<1>(a, col_e, post_e);
+        if constexpr (!STG) {
+            if (has_e) {
+                C::template load_pre<1>(a, col_e, pre_e);
+                C::template load_post<1>(a, col_e, post_e);
 #pragma unroll
-            for (int i = 0; i < NIN; ++i)
-                in_e[i].load_stream_if(a.in[i] + base + col_e, !C::kPartialRows || col_e < ext);
-        } else {
+                for (int i = 0; i < NIN; ++i)
+                    in_e[i].load_stream_if(a.in[i] + base + col_e,
+                                           !C::kPartialRows || col_e < ext);
+            } else {
 #pragma unroll
-            for (int i = 0; i < NIN; ++i) in_e[i].f[0] = 0.0f;
+                for (int i = 0; i < NIN; ++i) in_e[i].f[0] = 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+                C::template early<VEC, true>(a, vbase + (int64_t)min(tid + k * T_, nb - 1) * VEC,
+                                             ea[k]);
+            C::template early<1>(a, base + (has_e ? col_e : 0), ea_e);
         }
-        typename C::template Early<VEC> ea[VPT];
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-            C::template early<VEC, true>(a, vbase + (int64_t)min(tid + k * T_, nb - 1) * VEC, ea[k]);
-        typename C::template Early<1> ea_e;
-        C::template early<1>(a, base + (has_e ? col_e : 0), ea_e);
 
         float v[VPT][VEC];
         float ve[1];
@@ -538,6 +615,11 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
         }
         const float r1 = C::kMaxFirst ? block_max(l1, red + 32 * rb) : block_sum(l1, red + 32 * rb);
         rb ^= 1;
+        if constexpr (STG) {
+            // after the barrier every thread holds its part of the row
+            if (abort_flag[li & 1]) break;
+            if (tid == 0 && li + nstage < nlocal) issue(sq, li + nstage);
+        }
         const float mean = C::stat1(r1, cols, a);
         float rstd = 0.0f;
         if constexpr (C::kTwoPass) {
@@ -574,6 +656,29 @@ rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0, unsi
             Frag<T, 1> o;
             C::template post<1>(ve, mean, rstd, post_e, a, base + col_e, ea_e, o.f);
             o.store_stream(a.out + base + col_e);
+        }
+        if constexpr (STG) {
+            if (++sq == nstage) {
+                sq = 0;
+                parity ^= 1u;
+            }
+            ++li;
+        }
+    }
+    if constexpr (STG) {
+        // Only after a timed-out wait: record it, and wait (bounded) for this
+        // CTA's copies still in flight before its shared memory goes away.
+        if (li < nlocal && tid == 0) {
+            atomicOr(err, kDevErrWaitTimeout);
+            int qq = sq;
+            uint32_t pp = parity;
+            for (int64_t lj = li; lj < nlocal && lj < li + nstage; ++lj) {
+                (void)mbar_wait_bounded(smem_addr(&bars[qq]), pp);
+                if (++qq == nstage) {
+                    qq = 0;
+                    pp ^= 1u;
+                }
+            }
         }
     }
 }
@@ -1015,12 +1120,12 @@ inline cudaError_t allow_smem(const void *fn, const LaunchCtx &ctx, int bytes) {
 }
 
 // The shifted kernel's form with per-column copies (CS) for chain C and vpt
-// slots, or nullptr: defined and instantiated in the rows_shift_cs_*.cu units
-// only.  In a chain's own unit those kernels changed how ptxas allocated that
+// slots, with the staged ring when stg, or nullptr: defined and instantiated
+// in the rows_shift_cs_*.cu units only.  In a chain's own unit those kernels changed how ptxas allocated that
 // unit's other kernels (the two-slot staged bf16 LayerNorm kernel went from 32
 // registers and an 8-byte stack to 38 registers: three 512-thread CTAs an SM
 // instead of four).
-template <class C> const void *shift_cs_fn(int vpt);
+template <class C> const void *shift_cs_fn(int vpt, bool stg);
 
 template <class C> struct RowEngine {
     using T = typename C::T;
@@ -1117,11 +1222,12 @@ template <class C> struct RowEngine {
     }
 
     // The shifted-vector kernel (rows off the 16-byte grid), vpt vector slots;
-    // cs: per-column arrays copied to shared memory (chains that have some).
-    static const void *shift_fn(int vpt, bool cs) {
+    // cs: per-column arrays copied to shared memory (chains that have some),
+    // stg: with them, the rows' vectors staged by bulk copies.
+    static const void *shift_fn(int vpt, bool cs, bool stg = false) {
         if constexpr (C::kShiftOk) {
             if constexpr (C::kColArrays > 0) {
-                if (cs) return shift_cs_fn<C>(vpt);
+                if (cs) return shift_cs_fn<C>(vpt, stg);
             }
             switch (vpt) {
                 case 1: return (const void *)rows_shift_kernel<C, 1>;
@@ -1133,9 +1239,13 @@ template <class C> struct RowEngine {
         }
         return nullptr;
     }
-    // Shared memory of the shifted kernel's per-column copies (its CS form).
+    // Shared memory of the shifted kernel's per-column copies (its CS form),
+    // and of one stage of its ring (STG: the row inputs' whole vectors).
     static int64_t shift_col_bytes(int cols) {
         return (int64_t)C::kColArrays * (((int64_t)cols + 15) & ~(int64_t)15) * (int64_t)sizeof(T);
+    }
+    static int64_t shift_stage_bytes(int cols) {
+        return (int64_t)C::kInputs * (((int64_t)cols + 15) & ~(int64_t)15) * (int64_t)sizeof(T);
     }
 
     // The cluster kernel for a launch of `threads` threads: the 512-thread
@@ -1470,14 +1580,16 @@ template <class C> struct RowEngine {
             const int64_t ncl = rows < core.cap ? rows : core.cap;
             p->ctas = (int)(ncl * core.stages);
         } else {
-            if (core.shift == 2 && rows <= core.cap1) {
+            if (core.shift >= 2 && rows <= core.cap1) {
                 // one row per CTA: copying the per-column values would cost
                 // as much as reading them once, so the kernel without copies
                 *fn = shift_fn(core.vpt, false);
+                p->path = MB_ROW_DIRECT;
                 p->shift = 1;
                 p->smem = kHdrBytes;
+                p->stages = 0;
             }
-            p->ctas = (int)cta_grid(rows, core.cap, cols, p->shift == 2);
+            p->ctas = (int)cta_grid(rows, core.cap, cols, p->shift >= 2);
         }
         return MB_OK;
     }
@@ -1557,6 +1669,11 @@ template <class C> struct RowEngine {
         // when the chain has some and the copy fits one CTA (see below)
         bool cstage = shifted && C::kColArrays > 0 && !tun.no_bulk &&
                       kHdrBytes + shift_col_bytes(cols) <= ctx.smem_optin;
+        // and, with them, stream the rows' vectors through a staged ring when
+        // one stage fits beside the copies (not when the direct path is asked
+        // for: it keeps the unstaged forms)
+        bool sstaged = cstage && C::kShiftStaged && tun.path != MB_ROW_DIRECT &&
+                       kHdrBytes + shift_col_bytes(cols) + shift_stage_bytes(cols) <= ctx.smem_optin;
         const int64_t row_io =
             ((int64_t)C::kInputs * cols * (staged ? tun.read_pct : 100) / 100 +
              (int64_t)tun.outs * cols) *
@@ -1575,9 +1692,10 @@ template <class C> struct RowEngine {
             int vpt = 0, occ = 0, threads = 0;
             bool spills = true;
         };
-        auto pick = [&](bool cs, Pick &best) -> mb_status {
+        auto pick = [&](bool cs, bool stg, Pick &best) -> mb_status {
             const int smem_q = kHdrBytes + (staged ? stage_bytes : 0) +
-                               (cs ? (int)shift_col_bytes(cols) : 0);
+                               (cs ? (int)shift_col_bytes(cols) : 0) +
+                               (stg ? (int)shift_stage_bytes(cols) : 0);
             for (int cand = 1; cand <= max_vpt(vec || shifted); cand *= 2) {
                 if (tun.vpt > 0 && cand != tun.vpt) continue;
                 if (ceil_div(nvec_cta, cand) > kCtaMaxThreads) continue;
@@ -1586,7 +1704,7 @@ template <class C> struct RowEngine {
                 // allows more (LayerNorm + residual, fp32 rows of 2051: eight
                 // CTAs of 96 threads an SM ran 13% slower than five of 288)
                 if (shifted && threads < 128 && nvec_cta >= 128) continue;
-                const void *f = shifted ? shift_fn(cand, cs) : cta_fn(cand, vec, staged);
+                const void *f = shifted ? shift_fn(cand, cs, stg) : cta_fn(cand, vec, staged);
                 if (!f) continue;
                 int max_threads = 0;
                 bool spills = false;
@@ -1614,21 +1732,36 @@ template <class C> struct RowEngine {
             }
             return MB_OK;
         };
+        // Shifted rows: the staged form where it fits, unless it spills where
+        // the copies alone do not (a staged CTA keeps a second row in flight
+        // in its ring, so it is not judged by its CTAs an SM: LN fp32 4099
+        // columns ran 82.2 us staged at three CTAs an SM against 86.9 with
+        // the copies alone at four); else the copies alone, or neither when
+        // that keeps more rows in flight or spills less (the copies take
+        // shared memory: w and b of an fp32 row of 16383, 128 KB a CTA).
         Pick best;
-        mb_status pst = pick(cstage, best);
+        mb_status pst = pick(cstage, sstaged, best);
         if (pst != MB_OK) return pst;
-        if (cstage) {
-            // The copies take shared memory (w and b of an fp32 row of 16383:
-            // 128 KB a CTA): they are kept unless the kernel without them
-            // keeps more rows in flight, or spills where they would.
+        auto wins = [&](const Pick &c, const Pick &b) {
+            const int rb_ = b.occ < target ? b.occ : target;
+            const int rc_ = c.occ < target ? c.occ : target;
+            return c.vpt && (!b.vpt || (b.spills && !c.spills) || (b.spills == c.spills && rc_ > rb_));
+        };
+        if (sstaged) {
+            Pick copies;
+            if ((pst = pick(true, false, copies)) != MB_OK) return pst;
+            if (copies.vpt && (!best.vpt || (best.spills && !copies.spills))) {
+                best = copies;
+                sstaged = false;
+            }
+        }
+        if (cstage && !sstaged) {
             Pick plain;
-            if ((pst = pick(false, plain)) != MB_OK) return pst;
-            const int rc = best.occ < target ? best.occ : target;
-            const int rp = plain.occ < target ? plain.occ : target;
-            if (plain.vpt && (!best.vpt || (best.spills && !plain.spills) ||
-                              (best.spills == plain.spills && rp > rc))) {
+            if ((pst = pick(false, false, plain)) != MB_OK) return pst;
+            if (wins(plain, best)) {
                 best = plain;
                 cstage = false;
+                sstaged = false;
             }
         }
         int best_vpt = best.vpt, best_occ = best.occ, best_threads = best.threads;
@@ -1654,9 +1787,20 @@ template <class C> struct RowEngine {
             stages = want;
             smem = kHdrBytes + stages * stage_bytes;
         }
-        *fn = shifted ? shift_fn(best_vpt, cstage) : cta_fn(best_vpt, vec, staged);
+        *fn = shifted ? shift_fn(best_vpt, cstage, sstaged) : cta_fn(best_vpt, vec, staged);
         if (shifted) { p->vec = kVecN; p->shift = 1; }
         if (cstage) { smem = kHdrBytes + (int)shift_col_bytes(cols); p->shift = 2; }
+        if (sstaged) {
+            // the staged path's ring depth rule, beside the copies
+            const int64_t sb = shift_stage_bytes(cols);
+            int want = tun.stages > 0 ? tun.stages : (best_occ >= 2 ? 1 : 2);
+            if (want > kMaxStages) want = kMaxStages;
+            while (want > 1 && (int64_t)occ * (smem + 1024 + want * sb) > ctx.smem_per_sm) --want;
+            while (want > 1 && smem + want * sb > ctx.smem_optin) --want;
+            stages = want;
+            smem += (int)(want * sb);
+            p->shift = 3;
+        }
         int occ2 = 0;
         mb_status st = occupancy(ctx, *fn, best_threads, smem, &occ2);
         if (st != MB_OK) return st;
@@ -1671,9 +1815,10 @@ template <class C> struct RowEngine {
             if (st != MB_OK) return st;
             p->cap1 = (int64_t)(occ1 < occ ? occ1 : occ) * ctx.sm_count;
         }
-        p->path = path; p->threads = best_threads; p->vpt = best_vpt; p->stages = stages;
+        p->path = sstaged ? MB_ROW_STAGED : path;
+        p->threads = best_threads; p->vpt = best_vpt; p->stages = stages;
         p->smem = smem;
-        p->ctas = (int)cta_grid(rows, cap, cols, p->shift == 2);
+        p->ctas = (int)cta_grid(rows, cap, cols, p->shift >= 2);
         return MB_OK;
     }
 
@@ -1687,15 +1832,16 @@ template <class C> struct RowEngine {
         mb_status st = plan(ctx, tn, rows, cols, aligned, &p, &fn);
         if (st != MB_OK) return st;
         if (launch &&
-            (p.path == MB_ROW_STAGED || (p.path == MB_ROW_CLUSTER && p.ring > 0) || p.shift == 2)) {
+            (p.path == MB_ROW_STAGED || (p.path == MB_ROW_CLUSTER && p.ring > 0) || p.shift >= 2)) {
             // Asynchronous copies into shared memory are planned for device
             // memory only: rows (bulk copies) or per-column arrays (the
             // shifted kernel's copies) held in host memory (pinned, read over
             // the host link) take a plain-load path.
             bool dev = true;
-            if (p.shift == 2) {
+            if (p.shift >= 2) {
                 for (int i = 0; i < C::kColArrays; ++i) dev = dev && device_resident(C::col_array(a, i));
-            } else {
+            }
+            if (p.shift != 2) {
                 for (int i = 0; i < C::kInputs; ++i) dev = dev && device_resident(a.in[i]);
             }
             if (!dev) {
@@ -1712,9 +1858,11 @@ template <class C> struct RowEngine {
         int64_t rows_arg = rows;
         int cols_arg = cols;
         // the fourth kernel argument: ring depth, the cluster's slice length,
-        // or (shifted vectors) the row tensors' common offset within 16 bytes
+        // or (shifted vectors) the row tensors' common offset within 16 bytes,
+        // with the ring depth above it on the staged shifted form
         int stages_arg = p.path == MB_ROW_CLUSTER ? p.slice * p.vec
-                       : p.shift ? (int)(reinterpret_cast<uintptr_t>(a.in[0]) & 15u)
+                       : p.shift ? (int)(reinterpret_cast<uintptr_t>(a.in[0]) & 15u) |
+                                       (p.shift == 3 ? p.stages << 8 : 0)
                        : (p.stages > 0 ? p.stages : 1);
         unsigned *err = ctx.dev_err;
         int ring_arg = p.ring;      // the cluster kernel's sixth argument

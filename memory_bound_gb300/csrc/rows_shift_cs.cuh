@@ -7,15 +7,22 @@
 
 namespace mb {
 
-template <class C> const void *shift_cs_fn(int vpt) {
+template <class C, bool STG> const void *shift_cs_form(int vpt) {
     switch (vpt) {
-        case 1: return (const void *)rows_shift_kernel<C, 1, true>;
-        case 2: return (const void *)rows_shift_kernel<C, 2, true>;
-        case 4: return (const void *)rows_shift_kernel<C, 4, true>;
-        case 8: if constexpr (C::kVec == 4) return (const void *)rows_shift_kernel<C, 8, true>;
+        case 1: return (const void *)rows_shift_kernel<C, 1, true, STG>;
+        case 2: return (const void *)rows_shift_kernel<C, 2, true, STG>;
+        case 4: return (const void *)rows_shift_kernel<C, 4, true, STG>;
+        case 8: if constexpr (C::kVec == 4) return (const void *)rows_shift_kernel<C, 8, true, STG>;
                 break;
     }
     return nullptr;
+}
+
+template <class C> const void *shift_cs_fn(int vpt, bool stg) {
+    if constexpr (C::kShiftStaged) {
+        if (stg) return shift_cs_form<C, true>(vpt);
+    }
+    return shift_cs_form<C, false>(vpt);
 }
 
 }  // namespace mb

@@ -4,9 +4,9 @@
 
 namespace mb {
 
-template const void *shift_cs_fn<LnActChain<float, false, true>>(int);
-template const void *shift_cs_fn<LnActChain<float, true, true>>(int);
-template const void *shift_cs_fn<LnActChain<uint16_t, false, true>>(int);
-template const void *shift_cs_fn<LnActChain<uint16_t, true, true>>(int);
+template const void *shift_cs_fn<LnActChain<float, false, true>>(int, bool);
+template const void *shift_cs_fn<LnActChain<float, true, true>>(int, bool);
+template const void *shift_cs_fn<LnActChain<uint16_t, false, true>>(int, bool);
+template const void *shift_cs_fn<LnActChain<uint16_t, true, true>>(int, bool);
 
 }  // namespace mb

@@ -4,9 +4,9 @@
 
 namespace mb {
 
-template const void *shift_cs_fn<LnGeluChain<float>>(int);
-template const void *shift_cs_fn<LnGeluChain<uint16_t>>(int);
-template const void *shift_cs_fn<InductorChainT<float>>(int);
-template const void *shift_cs_fn<InductorChainT<uint16_t>>(int);
+template const void *shift_cs_fn<LnGeluChain<float>>(int, bool);
+template const void *shift_cs_fn<LnGeluChain<uint16_t>>(int, bool);
+template const void *shift_cs_fn<InductorChainT<float>>(int, bool);
+template const void *shift_cs_fn<InductorChainT<uint16_t>>(int, bool);
 
 }  // namespace mb

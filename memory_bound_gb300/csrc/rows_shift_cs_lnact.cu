@@ -5,9 +5,9 @@
 
 namespace mb {
 
-template const void *shift_cs_fn<LnActChain<float, false, false>>(int);
-template const void *shift_cs_fn<LnActChain<float, true, false>>(int);
-template const void *shift_cs_fn<LnActChain<uint16_t, false, false>>(int);
-template const void *shift_cs_fn<LnActChain<uint16_t, true, false>>(int);
+template const void *shift_cs_fn<LnActChain<float, false, false>>(int, bool);
+template const void *shift_cs_fn<LnActChain<float, true, false>>(int, bool);
+template const void *shift_cs_fn<LnActChain<uint16_t, false, false>>(int, bool);
+template const void *shift_cs_fn<LnActChain<uint16_t, true, false>>(int, bool);
 
 }  // namespace mb

@@ -96,8 +96,9 @@ def test_ln_gelu_unaligned(cols, path, place, bf16):
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_shifted_path_is_planned(cols, bf16):
     """Rows off the 16-byte grid with a common offset plan on 16-byte
-    vectors (path direct, the vector width), not on the scalar path; the
-    dropout chains too (their slots are 8 elements)."""
+    vectors (path direct, or staged with the per-column copies and a ring;
+    the vector width), not on the scalar path; the dropout chains too (their
+    slots are 8 elements)."""
     dt = "bf16" if bf16 else "f32"
     vec = 8 if bf16 else 4
     for chain in ("ln", "inductor", "lnact", "lnact_res", "softmax", "softmax_mask"):
@@ -105,11 +106,11 @@ def test_shifted_path_is_planned(cols, bf16):
             continue
         for al in (1, 2):
             p = mb.row_plan(chain, dt, 512, cols, aligned=al)
-            assert p["path"] == "direct" and p["vec"] == vec, (chain, al, p)
+            assert p["path"] in ("direct", "staged") and p["vec"] == vec, (chain, al, p)
         assert mb.row_plan(chain, dt, 512, cols, aligned=0)["vec"] == 1
     for chain in ("lnact_dropout", "lnact_res_dropout"):
         p = mb.row_plan(chain, dt, 512, cols, aligned=1)
-        assert p["path"] == "direct" and p["vec"] == 8, (chain, p)
+        assert p["path"] in ("direct", "staged") and p["vec"] == 8, (chain, p)
 
 
 @pytest.mark.parametrize("cols", [1031, 4099, 12291])
@@ -267,36 +268,55 @@ def _multi_round_rows(chain, dt, cols):
     return 2 * cap + 5
 
 
-def _copy_shape(pchain, dt):
+def _copy_shape(pchain, dt, staged):
     """The first of a few row lengths off the 16-byte grid (with a row count
     of several rows a CTA) that the planner serves with the per-column
-    copies; every chain with per-column arrays has one."""
+    copies, on the staged path (staged; the automatic choice) or the direct
+    one (the path asked for); every chain with per-column arrays has both."""
     for cols in (4099, 1031, 2051, 8195):
         rows = _multi_round_rows(pchain, dt, cols)
         plan = mb.row_plan(pchain, dt, rows, cols, aligned=2)
-        if plan["smem"] > 1024:
+        if plan["smem"] > 1024 and (plan["path"] == "staged") == staged:
             return cols, rows, plan
-    pytest.fail(f"no length takes the per-column copies for {pchain} {dt}")
+    pytest.fail(f"no length takes the {'staged' if staged else 'direct'} per-column copies "
+                f"for {pchain} {dt}")
 
 
-@pytest.mark.parametrize("chain", ["ln", "inductor", "lnact_h", "lnact_dropout"])
+@pytest.mark.parametrize("form,chain", [("staged", "ln"), ("staged", "inductor"),
+                                        ("staged", "lnact_h"), ("copies", "ln"),
+                                        ("copies", "inductor"), ("copies", "lnact_h"),
+                                        ("copies", "lnact_dropout")])
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 @pytest.mark.parametrize("col_off", [0, 1], ids=["cols16", "cols_off"])
-def test_shifted_column_copies(chain, bf16, col_off):
+def test_shifted_column_copies(form, chain, bf16, col_off):
     """The shifted kernel with its per-column arrays copied to shared memory
-    (several rows a CTA): every chain that has such arrays, inputs and outputs
-    at a common offset of one element, the per-column arrays 16-byte aligned
-    or one element off (bf16: copied element by element where column h is not
-    4-byte aligned), every element against the oracle."""
+    (several rows a CTA), with and without its bulk-copy ring for the rows'
+    vectors (the dropout chains have no staged form): every chain that has
+    such arrays, inputs and outputs at a common offset of one element, the
+    per-column arrays 16-byte aligned or one element off (bf16: copied
+    element by element where column h is not 4-byte aligned), every element
+    against the oracle."""
     dt = "bf16" if bf16 else "f32"
     pchain = {"ln": "ln", "inductor": "inductor", "lnact_h": "lnact_res_h",
               "lnact_dropout": "lnact_res_dropout"}[chain]
-    cols, rows, plan = _copy_shape(pchain, dt)
+    mb.set_row_path("auto" if form == "staged" else "direct")
+    try:
+        _shifted_column_copies(pchain, chain, dt, bf16, col_off, form == "staged")
+    finally:
+        mb.set_row_path("auto")
+
+
+def _shifted_column_copies(pchain, chain, dt, bf16, col_off, staged):
+    cols, rows, plan = _copy_shape(pchain, dt, staged)
     off = 1
     es = 2 if bf16 else 4
     narr = 3 if chain == "inductor" else 2
-    assert plan["path"] == "direct" and plan["vec"] in (8, 16 // es), plan
-    assert plan["smem"] == 1024 + narr * ((cols + 15) // 16 * 16) * es, plan   # the copies
+    nin = 1 if chain == "inductor" else 2
+    assert plan["path"] == ("staged" if staged else "direct"), plan
+    assert plan["vec"] in (8, 16 // es) and (plan["stages"] > 0) == staged, plan
+    padded = (cols + 15) // 16 * 16
+    # the copies, and the staged form's ring of plan["stages"] stages
+    assert plan["smem"] == 1024 + (narr + plan["stages"] * nin) * padded * es, plan
     seed = cols + 17
     x = synth.normal(seed, 0, (rows, cols), dtype=dt)
     if chain == "inductor":
@@ -354,7 +374,8 @@ def test_shifted_column_copies_planning(bf16):
     """The copies are planned for launches of several rows a CTA, not for one
     row a CTA (there a copy costs as much as reading the values once), not
     for chains without per-column arrays, and not where they would not fit
-    one CTA's shared memory (fp32 rows of 32767: 256 KB for w and b)."""
+    one CTA's shared memory (fp32 rows of 32767: 256 KB for w and b); the
+    staged form with them, except for the dropout chains."""
     dt = "bf16" if bf16 else "f32"
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for chain in ("ln", "inductor", "lnact", "lnact_res_dropout"):
@@ -364,6 +385,12 @@ def test_shifted_column_copies_planning(bf16):
         # aligned rows keep their engines
         assert mb.row_plan(chain, dt, 4 * cap, 4096, aligned=1)["vec"] in (4, 8)
     assert mb.row_plan("softmax", dt, 1 << 20, 4099, aligned=2)["smem"] == 1024
+    # the dropout chains keep the unstaged form; the others stage their rows
+    for chain in ("lnact_dropout", "lnact_res_dropout"):
+        p = mb.row_plan(chain, dt, 1 << 20, 4099, aligned=2)
+        assert p["path"] == "direct" and p["stages"] == 0 and p["smem"] > 1024, p
+    p = mb.row_plan("ln", dt, 1 << 20, 4099, aligned=2)
+    assert p["path"] == "staged" and p["stages"] >= 1, p
     big = mb.row_plan("ln", dt, 1 << 20, 32767, aligned=2)
     assert big["path"] == "direct" and (big["smem"] == 1024) == (not bf16), big
 
