@@ -371,9 +371,12 @@ typedef enum mb_row_path {
  * "choose automatically"; a
  * value that cannot serve a shape is ignored.  A forced path that cannot
  * serve a shape (MB_ROW_WARP beyond 256 vectors per row, MB_ROW_STAGED on
- * unaligned rows or rows too long for one stage, one-CTA paths on rows longer
- * than one CTA holds) falls back to the automatic choice.  Returns
- * MB_ERR_VALUE on a bad code or a negative count.
+ * rows too long for one stage or off the 16-byte grid without a common
+ * offset, one-CTA paths on rows longer than one CTA holds) falls back to the
+ * automatic choice.  Rows off the 16-byte grid with a common offset (shifted
+ * vectors) take a staged form when the chain has per-column arrays and it
+ * fits; MB_ROW_DIRECT keeps them unstaged.  Returns MB_ERR_VALUE on a bad
+ * code or a negative count.
  */
 mb_status mb_set_row_path(mb_row_path path, int ctas_per_sm, int stages,
                           int vec_per_thread);
@@ -410,10 +413,11 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * `aligned`: 1 every pointer is 16-byte aligned; 2 the row tensors start at
  * one common offset within 16 bytes (per-column vectors anywhere); 0 neither;
  * else MB_ERR_VALUE.  Rows planned on shifted vectors report path
- * MB_ROW_DIRECT with the vector width in out[4] while cols is not a multiple
- * of it; out[6] then includes the shared-memory copy of the chain's
- * per-column arrays where one is planned (launches of several rows a CTA).
- * Queries the current device (SM count, shared memory).
+ * MB_ROW_DIRECT, or MB_ROW_STAGED with their ring depth in out[5], with the
+ * vector width in out[4] while cols is not a multiple of it; out[6] then
+ * includes the shared-memory copy of the chain's per-column arrays where one
+ * is planned (launches of several rows a CTA) and the ring.  Queries the
+ * current device (SM count, shared memory).
  */
 mb_status mb_row_plan(int chain, mb_dtype dtype, int64_t rows, int64_t cols,
                       int aligned, int32_t out[7]);
