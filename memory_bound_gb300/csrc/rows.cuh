@@ -1226,7 +1226,7 @@ template <class C> struct RowEngine {
     // stg: with them, the rows' vectors staged by bulk copies.
     static const void *shift_fn(int vpt, bool cs, bool stg = false) {
         if constexpr (C::kShiftOk) {
-            if constexpr (C::kColArrays > 0) {
+            if constexpr (C::kColArrays > 0 || C::kShiftStaged) {
                 if (cs) return shift_cs_fn<C>(vpt, stg);
             }
             switch (vpt) {
@@ -1667,13 +1667,15 @@ template <class C> struct RowEngine {
         const int nvec_cta = shifted ? nvec_shift : nvec;
         // shifted rows read their per-column values from a shared-memory copy
         // when the chain has some and the copy fits one CTA (see below)
-        bool cstage = shifted && C::kColArrays > 0 && !tun.no_bulk &&
+        bool cstage = shifted && (C::kColArrays > 0 || C::kShiftStaged) && !tun.no_bulk &&
                       kHdrBytes + shift_col_bytes(cols) <= ctx.smem_optin;
         // and, with them, stream the rows' vectors through a staged ring when
         // one stage fits beside the copies (not when the direct path is asked
-        // for: it keeps the unstaged forms)
+        // for: it keeps the unstaged forms); chains without per-column arrays
+        // (the softmax chains) have the ring only
         bool sstaged = cstage && C::kShiftStaged && tun.path != MB_ROW_DIRECT &&
                        kHdrBytes + shift_col_bytes(cols) + shift_stage_bytes(cols) <= ctx.smem_optin;
+        if (C::kColArrays == 0 && !sstaged) cstage = false;
         const int64_t row_io =
             ((int64_t)C::kInputs * cols * (staged ? tun.read_pct : 100) / 100 +
              (int64_t)tun.outs * cols) *
@@ -1748,11 +1750,14 @@ template <class C> struct RowEngine {
             return c.vpt && (!b.vpt || (b.spills && !c.spills) || (b.spills == c.spills && rc_ > rb_));
         };
         if (sstaged) {
-            Pick copies;
-            if ((pst = pick(true, false, copies)) != MB_OK) return pst;
-            if (copies.vpt && (!best.vpt || (best.spills && !copies.spills))) {
-                best = copies;
+            // the copies alone, or (no per-column arrays) the plain form
+            const bool next_cs = C::kColArrays > 0;
+            Pick next;
+            if ((pst = pick(next_cs, false, next)) != MB_OK) return pst;
+            if (next.vpt && (!best.vpt || (best.spills && !next.spills))) {
+                best = next;
                 sstaged = false;
+                cstage = next_cs;
             }
         }
         if (cstage && !sstaged) {

@@ -1,6 +1,7 @@
-// rows_shift_cs.cuh -- the shifted kernel's form with per-column copies
-// (rows_shift_kernel<C, VPT, true>), included only by the rows_shift_cs_*.cu
-// units, which instantiate shift_cs_fn for each chain with per-column arrays.
+// rows_shift_cs.cuh -- the shifted kernel's forms with per-column copies and
+// the staged ring (rows_shift_kernel<C, VPT, true, STG>), included only by
+// the rows_shift_cs_*.cu units, which instantiate shift_cs_fn for each chain
+// with per-column arrays or a staged form.
 #pragma once
 
 #include "chains.cuh"
@@ -22,7 +23,8 @@ template <class C> const void *shift_cs_fn(int vpt, bool stg) {
     if constexpr (C::kShiftStaged) {
         if (stg) return shift_cs_form<C, true>(vpt);
     }
-    return shift_cs_form<C, false>(vpt);
+    if constexpr (C::kColArrays > 0) return shift_cs_form<C, false>(vpt);
+    return nullptr;
 }
 
 }  // namespace mb

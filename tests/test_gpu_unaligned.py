@@ -375,7 +375,8 @@ def test_shifted_column_copies_planning(bf16):
     row a CTA (there a copy costs as much as reading the values once), not
     for chains without per-column arrays, and not where they would not fit
     one CTA's shared memory (fp32 rows of 32767: 256 KB for w and b); the
-    staged form with them, except for the dropout chains."""
+    staged form with them, except for the dropout chains, and the staged
+    ring alone for the row softmax."""
     dt = "bf16" if bf16 else "f32"
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for chain in ("ln", "inductor", "lnact", "lnact_res_dropout"):
@@ -384,7 +385,12 @@ def test_shifted_column_copies_planning(bf16):
         assert mb.row_plan(chain, dt, cap + 1, 4099, aligned=2)["smem"] > 1024
         # aligned rows keep their engines
         assert mb.row_plan(chain, dt, 4 * cap, 4096, aligned=1)["vec"] in (4, 8)
-    assert mb.row_plan("softmax", dt, 1 << 20, 4099, aligned=2)["smem"] == 1024
+    # softmax has no per-column arrays: the ring alone, for bf16 rows
+    p = mb.row_plan("softmax", dt, 1 << 20, 4099, aligned=2)
+    if bf16:
+        assert p["path"] == "staged" and p["smem"] == 1024 + p["stages"] * 4112 * 2, p
+    else:
+        assert p["path"] == "direct" and p["smem"] == 1024, p
     # the dropout chains keep the unstaged form; the others stage their rows
     for chain in ("lnact_dropout", "lnact_res_dropout"):
         p = mb.row_plan(chain, dt, 1 << 20, 4099, aligned=2)
@@ -409,3 +415,36 @@ def test_shifted_column_copies_host_vectors():
     torch.cuda.synchronize()
     assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5),
                  what="host w, b")
+
+
+@pytest.mark.parametrize("cols", [1031, 4099, 8195])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_shifted_softmax_staged(cols, bf16):
+    """Row softmax on shifted rows of several rows a CTA: bf16 rows on the
+    staged ring alone (the chain has no per-column arrays), fp32 rows
+    unstaged; inputs and outputs one element into their allocations, every
+    element against the oracle, and the unstaged form the direct path
+    keeps."""
+    dt = "bf16" if bf16 else "f32"
+    rows = _multi_round_rows("softmax", dt, cols)
+    plan = mb.row_plan("softmax", dt, rows, cols, aligned=2)
+    es = 2 if bf16 else 4
+    if bf16:
+        assert plan["path"] == "staged" and plan["stages"] >= 1, plan
+        assert plan["smem"] == 1024 + plan["stages"] * ((cols + 15) // 16 * 16) * es, plan
+    else:
+        assert plan["path"] == "direct" and plan["smem"] == 1024, plan
+    x = synth.normal(cols + 29, 0, (rows, cols), 0.0, 2.0, dtype=dt)
+    want = oracle.row_softmax(x)
+    w_ = bf16_to_f64(want) if bf16 else want.astype(np.float64)
+    rtol = 1e-2 if bf16 else 1e-5
+    for path in ("auto", "direct"):
+        mb.set_row_path(path)
+        try:
+            y = _out_like(x, bf16, 1)
+            mb.fused_row_softmax(_dev(x, bf16, 1), out=y)
+            g = to_host(y)
+        finally:
+            mb.set_row_path("auto")
+        gv = bf16_to_f64(g) if bf16 else g.astype(np.float64)
+        assert np.all(np.abs(gv - w_) <= rtol * np.abs(w_) + 2.0 ** -126), f"softmax {cols} {path}"
