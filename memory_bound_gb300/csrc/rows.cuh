@@ -734,13 +734,27 @@ __device__ __forceinline__ float cluster_reduce(float v, float *xch, uint64_t *b
 // most kWideThreads threads take the kWideThreads form, whose threads may hold
 // up to 128 registers (the slice, the next row's prefetch and the per-column
 // values), where under the 64 of the 1024-thread form they spill.
-template <class C, int VPT, int VEC, bool STAGED, int MAXT>
+// SH: rows off the 16-byte grid whose tensors share the offset m0 within 16
+// bytes (the sixth argument carries m0 << 8 above the ring depth), as the
+// shifted one-CTA kernel reads them: a row's head of h < VEC elements, its
+// nb = (cols - h) / VEC whole vectors, of which CTA `rank` holds those from
+// vector rank * slice / VEC on (as many as remain, up to slice / VEC; the
+// host sizes slice for the most any row has), and its tail; the head and tail
+// elements go to rank 0, one a thread.  The per-column values of a slot start
+// off the arrays' 16-byte grid and are loaded element by element.
+template <class C, int VPT, int VEC, bool STAGED, int MAXT, bool SH = false>
 __global__ void __launch_bounds__(MAXT, 1)
 rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice, unsigned *err,
-                    int nstage) {
+                    int nstage_arg) {
+    static_assert(!SH || !C::kPartialRows, "shifted cluster rows are read whole");
     namespace cg = cooperative_groups;
     using T = typename C::T;
     constexpr int NIN = C::kInputs;
+    constexpr int ES = (int)sizeof(T);
+    const int nstage = SH ? nstage_arg & 255 : nstage_arg;
+    const int m0 = SH ? (nstage_arg >> 8) & 15 : 0;
+    using PrePC1 = typename C::template PrePC<1>;
+    using PostPC1 = typename C::template PostPC<1>;
     constexpr bool kEarlyPost = VPT * VEC * C::kPostPC <= 8;
     using PrePC = typename C::template PrePC<VEC>;
     using PostPC = typename C::template PostPC<VEC>;
@@ -764,6 +778,24 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     const uint32_t pitch = (uint32_t)slice * (uint32_t)sizeof(T);           // per input, in a stage
     const uint32_t my_bytes = (uint32_t)(nvec * VEC) * (uint32_t)sizeof(T);
     const uint32_t stage_bytes = (uint32_t)NIN * pitch;
+    // SH: a row's head, and the whole vectors of it this CTA holds
+    auto head_of = [&](int64_t row) -> int {
+        if constexpr (SH) {
+            const int off =
+                (int)(((uint64_t)m0 + (uint64_t)row * (uint64_t)cols * (uint64_t)ES) & 15u);
+            return ((16 - off) & 15) / ES;
+        } else {
+            return 0;
+        }
+    };
+    auto nv_of = [&](int h) -> int {
+        if constexpr (SH) {
+            const int n = (cols - h) / VEC - lo / VEC;
+            return n < 0 ? 0 : (n < slice / VEC ? n : slice / VEC);
+        } else {
+            return nvec;
+        }
+    };
     if (tid == 0) {
         mbar_init(smem_addr(&xbar[0]), 1);
         mbar_init(smem_addr(&xbar[1]), 1);
@@ -782,18 +814,25 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     auto issue = [&](int q, int64_t li) {
         const int64_t row = cid + li * nclusters;
         const uint32_t bar = smem_addr(&sbar[q]);
-        // this rank's part of the row's first row_extent() elements, rounded
-        // up to whole vectors (16 or 32 bytes) within the slice
-        const int ext = C::row_extent(a, row, cols) - lo;
-        uint32_t bytes = ext <= 0 ? 0u
-                       : ((uint32_t)((ext + VEC - 1) / VEC) * VEC) * (uint32_t)sizeof(T);
-        if (bytes > my_bytes) bytes = my_bytes;
+        const int h = head_of(row);
+        uint32_t bytes;
+        if constexpr (SH) {
+            // this rank's whole vectors of the row
+            bytes = (uint32_t)(nv_of(h) * VEC) * (uint32_t)sizeof(T);
+        } else {
+            // this rank's part of the row's first row_extent() elements,
+            // rounded up to whole vectors (16 or 32 bytes) within the slice
+            const int ext = C::row_extent(a, row, cols) - lo;
+            bytes = ext <= 0 ? 0u
+                  : ((uint32_t)((ext + VEC - 1) / VEC) * VEC) * (uint32_t)sizeof(T);
+            if (bytes > my_bytes) bytes = my_bytes;
+        }
         mbar_arrive_expect_tx(bar, (uint32_t)NIN * bytes);
         if (bytes == 0) return;
 #pragma unroll
         for (int i = 0; i < NIN; ++i)
             bulk_g2s(smem_addr(ring + (size_t)q * stage_bytes + (size_t)i * pitch),
-                     a.in[i] + row * cols + lo, bytes, bar);
+                     a.in[i] + row * cols + h + lo, bytes, bar);
     };
     if constexpr (STAGED) {
         if (tid == 0) {
@@ -808,28 +847,58 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     PrePC pre[VPT];
     PostPC post[kEarlyPost ? VPT : 1];
     Frag<T, VEC> in[VPT][NIN];
-    auto load_cols = [&]() {
-        if (nvec == 0) return;
+    // (SH: the row's head h and this CTA's vectors nv of it)
+    auto load_cols = [&](int h, int nv) {
+        if (nv == 0) return;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
-            C::template load_pre<VEC>(a, lo + vc * VEC, pre[k]);
-            if constexpr (kEarlyPost) C::template load_post<VEC>(a, lo + vc * VEC, post[k]);
+            const int vc = min(tid + k * (int)blockDim.x, nv - 1);
+            C::template load_pre<VEC>(a, h + lo + vc * VEC, pre[k], ColsGlobal<!SH>{});
+            if constexpr (kEarlyPost)
+                C::template load_post<VEC>(a, h + lo + vc * VEC, post[k], ColsGlobal<!SH>{});
         }
     };
     auto load_row = [&](int64_t r) {
-        if (nvec == 0) return;
-        load_cols();
+        const int h = head_of(r);
+        const int nv = nv_of(h);
+        if (nv == 0) return;
+        load_cols(h, nv);
         const int ext = C::kPartialRows ? C::row_extent(a, r, cols) : cols;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
+            const int vc = min(tid + k * (int)blockDim.x, nv - 1);
 #pragma unroll
             for (int i = 0; i < NIN; ++i)
-                in[k][i].load_stream_if(a.in[i] + r * cols + lo + vc * VEC,
+                in[k][i].load_stream_if(a.in[i] + r * cols + h + lo + vc * VEC,
                                         !C::kPartialRows || lo + vc * VEC < ext);
         }
     };
+    // SH: a row's head and tail elements, one a thread on rank 0.  Loaded at
+    // the top of the row's iteration, where the staged path's wait or the
+    // chain's first pass hides them; the direct path of a chain whose first
+    // pass is a bare maximum (the softmax) loads them with the previous row
+    // in flight instead (softmax fp32, 50257 columns: 82.0 us against 126.9;
+    // the others ran 6-12% slower that way, the held values pushing the
+    // 1024-thread forms into spills).
+    constexpr bool kEdgesAhead = SH && !STAGED && C::kMaxFirst;
+    Frag<T, 1> in_e[NIN];
+    auto load_edges = [&](int64_t r) {
+        if constexpr (SH) {
+            const int h = head_of(r);
+            const int nb = (cols - h) / VEC;
+            const int col_e = tid < h ? tid : h + nb * VEC + (tid - h);
+            if (rank == 0 && tid < cols - nb * VEC) {
+#pragma unroll
+                for (int i = 0; i < NIN; ++i) in_e[i].load_stream(a.in[i] + r * cols + col_e);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NIN; ++i) in_e[i].f[0] = 0.0f;
+            }
+        }
+    };
+    if constexpr (kEdgesAhead) {
+        if (nlocal > 0) load_edges(cid);
+    }
     if constexpr (!STAGED) {
         if (nlocal > 0) load_row(cid);
     }
@@ -841,21 +910,39 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
     int64_t li = 0;
     for (; li < nlocal; ++li) {
         const int64_t row = cid + li * nclusters;
-        const int64_t base = row * cols + lo;
+        const int h = head_of(row);                            // SH; else 0
+        const int nvr = nv_of(h);                              // SH: this row's; else nvec
+        const int64_t base = row * cols + h + lo;
         typename C::template Early<VEC> ea[VPT];
-        if (nvec > 0) {
+        if (nvr > 0) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
-                C::template early<VEC>(a, base + min(tid + k * (int)blockDim.x, nvec - 1) * VEC, ea[k]);
+                C::template early<VEC, SH>(a, base + min(tid + k * (int)blockDim.x, nvr - 1) * VEC,
+                                           ea[k]);
+        }
+        // SH: the row's head and tail elements, one a thread on rank 0
+        const int nb = SH ? (cols - h) / VEC : 0;
+        const bool has_e = SH && rank == 0 && tid < cols - nb * VEC;
+        const int col_e = tid < h ? tid : h + nb * VEC + (tid - h);
+        PrePC1 pre_e;
+        PostPC1 post_e;
+        typename C::template Early<1> ea_e;
+        if constexpr (SH) {
+            if constexpr (!kEdgesAhead) load_edges(row);
+            if (has_e) {
+                C::template load_pre<1>(a, col_e, pre_e);
+                C::template load_post<1>(a, col_e, post_e);
+            }
+            C::template early<1>(a, row * cols + (has_e ? col_e : 0), ea_e);
         }
         if constexpr (STAGED) {
-            load_cols();
+            load_cols(h, nvr);
             if (!mbar_wait_bounded(smem_addr(&sbar[q]), parity)) stage_abort[li & 1] = 1;
             const T *stage = reinterpret_cast<const T *>(ring + (size_t)q * stage_bytes);
-            if (nvec > 0) {
+            if (nvr > 0) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    const int vc = min(tid + k * (int)blockDim.x, nvec - 1);
+                    const int vc = min(tid + k * (int)blockDim.x, nvr - 1);
 #pragma unroll
                     for (int i = 0; i < NIN; ++i)
                         in[k][i].load_shared(stage + (size_t)i * slice + vc * VEC);
@@ -863,14 +950,25 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
             }
         }
         float v[VPT][VEC];
+        float ve[1];
         float l1 = C::kMaxFirst ? -INFINITY : 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vi = tid + k * (int)blockDim.x;
-            C::template pre<VEC>(in[k], pre[k], a, row, lo + vi * VEC, v[k]);
-            l1 = fold1<C, VEC>(l1, v[k], vi < nvec);
+            C::template pre<VEC>(in[k], pre[k], a, row, h + lo + vi * VEC, v[k]);
+            l1 = fold1<C, VEC>(l1, v[k], vi < nvr);
             if constexpr (C::kStorePre) {
-                if (vi < nvec) C::template store_pre<VEC>(v[k], a, base + vi * VEC);
+                if (vi < nvr) C::template store_pre<VEC>(v[k], a, base + vi * VEC);
+            }
+        }
+        if constexpr (SH) {
+            C::template pre<1>(in_e, pre_e, a, row, has_e ? col_e : 0, ve);
+            l1 = fold1<C, 1>(l1, ve, has_e);
+            if constexpr (C::kStorePre) {
+                if (has_e) C::template store_pre<1>(ve, a, row * cols + col_e);
+            }
+            if constexpr (kEdgesAhead) {
+                if (li + 1 < nlocal) load_edges(row + nclusters);
             }
         }
         // DIRECT: the input registers are free now, so the next row's loads
@@ -896,7 +994,11 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const float part = C::template p2<VEC>(v[k], mean);
-                l2 += tid + k * (int)blockDim.x < nvec ? part : 0.0f;
+                l2 += tid + k * (int)blockDim.x < nvr ? part : 0.0f;
+            }
+            if constexpr (SH) {
+                const float part_e = C::template p2<1>(ve, mean);
+                l2 += has_e ? part_e : 0.0f;
             }
             const float c2 = block_sum(l2, red[rb]);
             rb ^= 1;
@@ -908,16 +1010,23 @@ rows_cluster_kernel(const typename C::Args a, int64_t rows, int cols, int slice,
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int vi = tid + k * blockDim.x;
-            if (vi < nvec) {
+            if (vi < nvr) {
                 Frag<T, VEC> o;
                 if constexpr (kEarlyPost) {
                     C::template post<VEC>(v[k], mean, rstd, post[k], a, base + vi * VEC, ea[k], o.f);
                 } else {
                     PostPC pc;
-                    C::template load_post<VEC>(a, lo + vi * VEC, pc);
+                    C::template load_post<VEC>(a, h + lo + vi * VEC, pc, ColsGlobal<!SH>{});
                     C::template post<VEC>(v[k], mean, rstd, pc, a, base + vi * VEC, ea[k], o.f);
                 }
                 o.store_stream(a.out + base + vi * VEC);
+            }
+        }
+        if constexpr (SH) {
+            if (has_e) {
+                Frag<T, 1> o;
+                C::template post<1>(ve, mean, rstd, post_e, a, row * cols + col_e, ea_e, o.f);
+                o.store_stream(a.out + row * cols + col_e);
             }
         }
         if constexpr (STAGED) {
@@ -1126,6 +1235,11 @@ inline cudaError_t allow_smem(const void *fn, const LaunchCtx &ctx, int bytes) {
 // registers and an 8-byte stack to 38 registers: three 512-thread CTAs an SM
 // instead of four).
 template <class C> const void *shift_cs_fn(int vpt, bool stg);
+// The cluster kernel's form for rows off the 16-byte grid (SH) for chain C,
+// vpt slots, staged or not, on a launch of `threads` threads, or nullptr:
+// defined and instantiated in the rows_cluster_sh_*.cu units only, for the
+// same reason.
+template <class C> const void *cluster_sh_fn(int vpt, bool staged, int threads);
 
 template <class C> struct RowEngine {
     using T = typename C::T;
@@ -1258,7 +1372,11 @@ template <class C> struct RowEngine {
         }
         return (const void *)rows_cluster_kernel<C, VPT, VEC, STAGED, kCtaMaxThreads>;
     }
-    static const void *cluster_fn(int vpt, bool vec, bool staged, int threads) {
+    static const void *cluster_fn(int vpt, bool vec, bool staged, int threads, bool sh = false) {
+        if constexpr (C::kShiftOk && !C::kPartialRows) {
+            if (sh) return cluster_sh_fn<C>(vpt, staged, threads);
+        }
+        if (sh) return nullptr;
         if (vec) {
             if (staged) {
                 switch (vpt) {
@@ -1324,12 +1442,16 @@ template <class C> struct RowEngine {
     // values per thread); no rank is empty.  Launches holding at most the
     // chain's C::kClusterVals values per thread come first: a thread keeps
     // its slice and the next row's prefetch in registers.
+    // sh: rows off the 16-byte grid on the cluster kernel's SH form (nvec:
+    // the most whole vectors any row has).
     static mb_status plan_cluster(const LaunchCtx &ctx, const RowTuning &tun, int64_t rows,
-                                  int nvec, bool vec, RowPlan *p, const void **fn) {
+                                  int nvec, bool vec, RowPlan *p, const void **fn,
+                                  bool sh = false) {
         const int VEC = vec ? kVecN : 1;
         for (int pass = 0; pass < 2; ++pass) {
             mb_status st = plan_cluster_pass(ctx, tun, rows, nvec, vec,
-                                             pass == 0 ? C::kClusterVals / VEC : 1 << 30, p, fn);
+                                             pass == 0 ? C::kClusterVals / VEC : 1 << 30, p, fn,
+                                             sh);
             if (st != MB_ERR_SHAPE) return st;
         }
         return MB_ERR_SHAPE;
@@ -1387,7 +1509,7 @@ template <class C> struct RowEngine {
 
     static mb_status plan_cluster_pass(const LaunchCtx &ctx, const RowTuning &tun,
                                        int64_t rows, int nvec, bool vec, int max_vpt_regs,
-                                       RowPlan *p, const void **fn) {
+                                       RowPlan *p, const void **fn, bool sh) {
         // Staged (bulk-async ring) for bf16 rows that are vectorised and in
         // device memory, ring depth kClusterRing; fp32 rows load directly,
         // except for chains that ask (C::kStageLargeSlices) when a CTA's slice
@@ -1401,7 +1523,7 @@ template <class C> struct RowEngine {
         const bool may_stage = vec && !tun.no_bulk;
         const bool staged = may_stage && (sizeof(T) == 2 || tun.ctas_per_sm > 0);
         if constexpr (C::kStageLargeSlices && sizeof(T) == 2) {
-            if (staged) {
+            if (staged && !sh) {
                 const mb_status st = plan_cluster_smem(ctx, tun, rows, nvec, p, fn);
                 if (st != MB_ERR_SHAPE) return st;
             }
@@ -1443,7 +1565,7 @@ template <class C> struct RowEngine {
                     continue;
                 if (ceil_div(slice_v, vpt) > kCtaMaxThreads) continue;
                 const int threads = round_up32(ceil_div(slice_v, vpt));
-                const void *f = cluster_fn(vpt, vec, ring > 0, threads);
+                const void *f = cluster_fn(vpt, vec, ring > 0, threads, sh);
                 if (!f) continue;
                 int max_threads = 0;
                 bool spills = false;
@@ -1470,11 +1592,12 @@ template <class C> struct RowEngine {
         if (!best_n && tun.vpt > 0) {
             RowTuning t2 = tun;
             t2.vpt = 0;
-            return plan_cluster(ctx, t2, rows, nvec, vec, p, fn);
+            return plan_cluster(ctx, t2, rows, nvec, vec, p, fn, sh);
         }
         if (!best_n) return MB_ERR_SHAPE;       // the caller tries the next pass
-        *fn = cluster_fn(best_vpt, vec, best_ring > 0, best_threads);
+        *fn = cluster_fn(best_vpt, vec, best_ring > 0, best_threads, sh);
         const int64_t ncl = rows < best_n ? rows : best_n;
+        p->shift = sh ? 1 : 0;
         p->path = MB_ROW_CLUSTER; p->threads = best_threads; p->vpt = best_vpt;
         p->stages = best_cs; p->smem = best_smem;
         p->ctas = (int)(ncl * best_cs);
@@ -1633,7 +1756,15 @@ template <class C> struct RowEngine {
                  : (vec && stage_fits ? MB_ROW_STAGED : MB_ROW_DIRECT);
 
         p->vec = VEC;
-        if (path == MB_ROW_CLUSTER) return plan_cluster(ctx, tun, rows, nvec, vec, p, fn);
+        if (path == MB_ROW_CLUSTER) {
+            // rows off the 16-byte grid with a common offset: the cluster
+            // kernel's shifted form, on the most whole vectors a row has
+            if (shift_ok && !C::kPartialRows) {
+                p->vec = kVecN;
+                return plan_cluster(ctx, tun, rows, cols / kVecN, true, p, fn, true);
+            }
+            return plan_cluster(ctx, tun, rows, nvec, vec, p, fn);
+        }
         if (path == MB_ROW_WARP) {
             const int vpl = warp_vpl;
             *fn = warp_fn(vpl, vec);
@@ -1870,7 +2001,11 @@ template <class C> struct RowEngine {
                                        (p.shift == 3 ? p.stages << 8 : 0)
                        : (p.stages > 0 ? p.stages : 1);
         unsigned *err = ctx.dev_err;
-        int ring_arg = p.ring;      // the cluster kernel's sixth argument
+        // the cluster kernel's sixth argument: the ring depth, with (shifted
+        // rows) the row tensors' common offset within 16 bytes above it
+        int ring_arg = p.ring | (p.path == MB_ROW_CLUSTER && p.shift
+                                     ? (int)(reinterpret_cast<uintptr_t>(a.in[0]) & 15u) << 8
+                                     : 0);
         void *kargs[] = {&args, &rows_arg, &cols_arg, &stages_arg, &err, &ring_arg};
         cudaError_t e = launch_kernel(lctx, fn, dim3(p.ctas), dim3(p.threads), kargs, p.smem,
                                       p.path == MB_ROW_CLUSTER ? p.stages : 1);

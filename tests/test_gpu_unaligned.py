@@ -448,3 +448,81 @@ def test_shifted_softmax_staged(cols, bf16):
             mb.set_row_path("auto")
         gv = bf16_to_f64(g) if bf16 else g.astype(np.float64)
         assert np.all(np.abs(gv - w_) <= rtol * np.abs(w_) + 2.0 ** -126), f"softmax {cols} {path}"
+
+
+@pytest.mark.parametrize("cols", [32769, 50257, 65537])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+@pytest.mark.parametrize("ring", [0, 1, 2], ids=["auto", "ring1", "ring2"])
+def test_shifted_cluster_rows(cols, bf16, ring):
+    """Rows longer than a CTA and off the 16-byte grid, whose tensors share an
+    offset (here three elements): the cluster kernel's shifted form, each
+    CTA's whole vectors loaded directly or staged through a ring of one or
+    two stages, head and tail on rank 0.  LayerNorm + GeLU, the LayerNorm
+    family with the residual stream and statistics, dropout (keep mask exact),
+    softmax and the Inductor chain, every element against the oracle."""
+    dt = "bf16" if bf16 else "f32"
+    rows, off = 7, 3
+    mb.set_row_path("cluster", ring, 0) if ring else mb.set_row_path("auto")
+    try:
+        p = mb.row_plan("ln", dt, rows, cols, aligned=2)
+        assert p["path"] == "cluster" and p["vec"] == (8 if bf16 else 4), p
+        assert (p["smem"] > 0) == (bool(ring) or bf16), p
+        seed = cols % 1013
+        x, r = _rows(rows, cols, seed, bf16, 2)
+        w, b = _vecs(cols, seed, bf16)
+        xd, rd, wd, bd = _dev(x, bf16, off), _dev(r, bf16, off), to_dev(w, bf16), to_dev(b, bf16)
+        out = _out_like(x, bf16, off)
+        mb.fused_residual_layernorm_gelu(xd, rd, wd, bd, 1e-5, out=out)
+        assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5), bf16=bf16,
+                     what=f"ln {cols}")
+        out, h = _out_like(x, bf16, off), _out_like(x, bf16, off)
+        mean = torch.empty(rows, device="cuda")
+        rstd = torch.empty(rows, device="cuda")
+        mb.fused_layernorm_act(xd, rd, wd, bd, act="gelu_tanh", out=out, h_out=h,
+                               mean_out=mean, rstd_out=rstd)
+        want, want_h, wm, wr = oracle.layernorm_act_ex(x, r, w, b, 1e-5, oracle.ACT_GELU,
+                                                       want_h=True, want_stats=True)
+        assert_close(to_host(out), want, bf16=bf16, what=f"lnact {cols}")
+        assert_bitexact(to_host(h), want_h, f"h {cols}")
+        m, rs = to_host(mean).astype(np.float64), to_host(rstd).astype(np.float64)
+        assert np.all(np.abs(m - wm) <= 1e-5 / wr + 1e-7 * np.abs(wm))
+        assert np.all(np.abs(rs - wr) <= 1e-5 * wr)
+        pd, seed_d, goff = 0.25, 99, 5
+        out = _out_like(x, bf16, off)
+        mb.fused_layernorm_act(xd, None, wd, bd, act="relu", out=out, p=pd, seed=seed_d,
+                               offset=goff)
+        want, _, _, _ = oracle.layernorm_act_ex(x, None, w, b, 1e-5, oracle.ACT_RELU, p=pd,
+                                                seed=seed_d, offset=goff)
+        keep = oracle.dropout_mask(seed_d, goff, 0, x.size, pd).reshape(x.shape)
+        got = to_host(out)
+        g = bf16_to_f64(got) if bf16 else got.astype(np.float64)
+        assert np.all(g[~keep] == 0), "a dropped element is not zero"
+        assert_close(got, want, bf16=bf16, what=f"dropout {cols}")
+        y = _out_like(x, bf16, off)
+        mb.fused_row_softmax(xd, out=y)
+        ws = oracle.row_softmax(x)
+        gv = bf16_to_f64(to_host(y)) if bf16 else to_host(y).astype(np.float64)
+        wv = bf16_to_f64(ws) if bf16 else ws.astype(np.float64)
+        rtol = 1e-2 if bf16 else 1e-5
+        assert np.all(np.abs(gv - wv) <= rtol * np.abs(wv) + 2.0 ** -126), f"softmax {cols}"
+        y = _out_like(x, bf16, off)
+        mb.fused_bias_relu_branch_mean_epilogue(xd, bd, wd, bd, 1.1, 0.1, out=y)
+        want = (oracle.bias_relu_branch_mean_epilogue_bf16(x, b, w, b) if bf16
+                else oracle.bias_relu_branch_mean_epilogue(x, b, w, b))
+        assert_close(to_host(y), want, bf16=bf16, what=f"inductor {cols}")
+    finally:
+        mb.set_row_path("auto")
+
+
+def test_shifted_cluster_rows_many():
+    """More shifted long rows than clusters fit at once (each cluster loops
+    over rows whose heads differ), bf16 on the staged ring."""
+    rows, cols, off = 300, 40001, 1
+    x, r = _rows(rows, cols, 77, True, 2)
+    w, b = _vecs(cols, 77, True)
+    out = _out_like(x, True, off)
+    assert mb.row_plan("ln", "bf16", rows, cols, aligned=2)["vec"] == 8
+    mb.fused_residual_layernorm_gelu(_dev(x, True, off), _dev(r, True, off), to_dev(w, True),
+                                     to_dev(b, True), 1e-5, out=out)
+    assert_close(to_host(out), oracle.residual_layernorm_gelu(x, r, w, b, 1e-5), bf16=True,
+                 what="ln 300 x 40001")
