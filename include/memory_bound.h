@@ -413,8 +413,9 @@ mb_status mb_set_pointwise_shape(int blocks_per_sm, int unroll);
  * `aligned`: 1 every pointer is 16-byte aligned; 2 the row tensors start at
  * one common offset within 16 bytes (per-column vectors anywhere); 0 neither;
  * else MB_ERR_VALUE.  Rows planned on shifted vectors report path
- * MB_ROW_DIRECT, or MB_ROW_STAGED with their ring depth in out[5], with the
- * vector width in out[4] while cols is not a multiple of it; out[6] then
+ * MB_ROW_DIRECT, or MB_ROW_STAGED with their ring depth in out[5] (or, longer
+ * than a CTA holds, MB_ROW_CLUSTER), with the vector width in out[4] while
+ * cols is not a multiple of it; out[6] then
  * includes the shared-memory copy of the chain's per-column arrays where one
  * is planned (launches of several rows a CTA) and the ring.  Queries the
  * current device (SM count, shared memory).
