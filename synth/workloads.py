@@ -160,8 +160,9 @@ SOFTMAX_CAUSAL_F32 = Workload("softmax_scale_causal_f32_131072x4096", "softmax_m
                               32 * 4096, 4096, 11, SOFTMAX_F32.tensors,
                               {"scale": 0.125, "causal": True, "period": 4096, "offset": 0})
 # Residual + LayerNorm + GeLU on rows whose length is not a whole number of
-# 16-byte vectors (4099 fp32 values, 16396 bytes): every row starts at a
-# different offset within 16 bytes, so the kernels take their scalar path.
+# 16-byte vectors (4099 fp32 values, 16396 bytes): consecutive rows start 0,
+# 12, 8 and 4 bytes past a 16-byte boundary, so each row is read as a short
+# head, whole 16-byte vectors and a short tail.
 LN_F32_RAGGED = _ln("ln_gelu_f32_8192x4099", "f32", 8192, 4099, 12)
 NEXT = (SOFTMAX_F32, LNACT_RES_BF16, LNACT_RELU_F32, INDUCTOR_BF16, LNACT_RELU_DROP_F32,
         POINTWISE_BCAST_F32, SOFTMAX_CAUSAL_F32, LN_F32_RAGGED)
