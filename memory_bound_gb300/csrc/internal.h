@@ -60,11 +60,13 @@ cudaError_t launch_kernel(const LaunchCtx &ctx, const void *fn, dim3 grid, dim3 
 struct RowPlan {
     int path = 0, threads = 0, ctas = 0, vpt = 0, vec = 0, stages = 0, smem = 0;
     int slice = 0;     // cluster path: vectors of the row each CTA holds
-    int shift = 0;     // one-CTA path on rows off the 16-byte grid (shifted vectors):
-                       // 1, or 2 with the per-column values copied to shared memory
+    int shift = 0;     // rows off the 16-byte grid (shifted vectors): 1; on the one-CTA
+                       // path 2 with the per-column values copied to shared memory, 3
+                       // with the copies and the staged ring
     int ring = 0;      // cluster path: staging ring depth (0: direct loads)
     int64_t cap = 0;   // CTAs (warp/CTA paths, at 256 threads for warp) or clusters resident at once
-    int64_t cap1 = 0;  // shift 2: CTAs of the same launch without the copies resident at once
+    int64_t cap1 = 0;  // shift 2, 3: CTAs of the same launch in the plain shifted form
+                       // resident at once
 };
 
 // Chains implemented in their own translation units.  `launch == false`

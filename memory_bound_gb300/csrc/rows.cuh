@@ -396,11 +396,17 @@ rows_cta_kernel_capped(const typename C::Args a, int64_t rows, int cols, int nst
 // redone, behind a barrier, whenever a CTA's h changes.  The host plans CS
 // for launches of several rows a CTA only (one row a CTA would copy as many
 // values as it reads).
-// STG (with CS): the rows' whole vectors are streamed into a ring of nstage
-// shared-memory stages by bulk copies, as on rows_cta_kernel's staged path:
-// a row's vector body starts on a 16-byte boundary and is a whole number of
-// 16-byte words, so one bulk copy per input moves it; head and tail elements
-// stay plain loads.  The fourth argument then carries m0 | nstage << 8.
+// STG (with CS, which copies nothing for chains without per-column arrays):
+// the rows' whole vectors are streamed into a ring of nstage shared-memory
+// stages after the copies, by bulk copies, as on rows_cta_kernel's staged
+// path: a row's vector body starts on a 16-byte boundary and is a whole
+// number of 16-byte words, so one bulk copy per input moves it, and a stage
+// is refilled for the CTA's next row once the first reduction's barrier
+// shows every thread holds the current one.  Head and tail elements stay
+// plain loads, taken (with the values the epilogue draws early) before the
+// stage wait, which their work hides.  Waits are bounded; a timeout ends the
+// CTA's row loop after its copies in flight have landed and is reported in
+// `err`.  The fourth argument then carries m0 | nstage << 8.
 template <class C, int VPT, bool CS = false, bool STG = false>
 __global__ void __launch_bounds__(kCtaMaxThreads)
 rows_shift_kernel(const typename C::Args a, int64_t rows, int cols, int m0_arg, unsigned *err) {
@@ -1796,14 +1802,15 @@ template <class C> struct RowEngine {
         const bool staged = path == MB_ROW_STAGED;
         const bool shifted = shift && path == MB_ROW_DIRECT;
         const int nvec_cta = shifted ? nvec_shift : nvec;
-        // shifted rows read their per-column values from a shared-memory copy
-        // when the chain has some and the copy fits one CTA (see below)
+        // Shifted rows may take the kernel's shared-memory forms: cstage, the
+        // copies of the chain's per-column arrays (when they fit one CTA), and
+        // sstaged, with them a ring streaming the rows' vectors (when one stage
+        // fits beside the copies, for chains that take it, and not when the
+        // direct path is asked for).  A chain without per-column arrays (the
+        // row softmax) has the ring alone, or neither.  The choice among the
+        // forms that fit is made below.
         bool cstage = shifted && (C::kColArrays > 0 || C::kShiftStaged) && !tun.no_bulk &&
                       kHdrBytes + shift_col_bytes(cols) <= ctx.smem_optin;
-        // and, with them, stream the rows' vectors through a staged ring when
-        // one stage fits beside the copies (not when the direct path is asked
-        // for: it keeps the unstaged forms); chains without per-column arrays
-        // (the softmax chains) have the ring only
         bool sstaged = cstage && C::kShiftStaged && tun.path != MB_ROW_DIRECT &&
                        kHdrBytes + shift_col_bytes(cols) + shift_stage_bytes(cols) <= ctx.smem_optin;
         if (C::kColArrays == 0 && !sstaged) cstage = false;
