@@ -1,5 +1,6 @@
 """A seeded random sweep over every chain: row counts, row lengths (short,
-ragged, just past a vector or a CTA, long enough for the cluster path),
+ragged, just past a vector or a CTA, long enough for the cluster path, off
+the 16-byte grid at every length),
 dtypes, 16-byte-aligned or offset views, forced row engines, host or device
 memory for the rows, and the chains' options; each case against the CPU
 oracle.  Rows of 65544 and 131080 elements reach the cluster kernels that
@@ -27,8 +28,9 @@ def _cases(n=300, seed=20240601):
     out = []
     for i in range(n):
         chain = CHAINS[i % len(CHAINS)]
-        cols = int(rng.choice([1, 2, 3, 7, 8, 31, 64, 255, 256, 257, 1000, 1024, 2049, 4096, 4100,
-                               8192, 16384, 32769, 40000, 65544, 131080]))
+        cols = int(rng.choice([1, 2, 3, 7, 8, 31, 64, 255, 256, 257, 1000, 1024, 2049, 4096, 4099,
+                               4100, 8192, 12291, 16384, 32769, 40000, 50257, 65537, 65544,
+                               131080]))
         rows = int(rng.integers(1, 40 if cols > 16384 else 200))
         out.append(dict(i=i, chain=chain, rows=rows, cols=cols,
                         bf16=bool(rng.integers(0, 2)) and chain != "inductor",
